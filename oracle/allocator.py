@@ -1,0 +1,134 @@
+"""Block-pool model -- the oracle for block allocation, forks and copy-on-write.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and
+bench.py's CPU-baseline leg, never by the CUDA library or its binding.
+
+It restates the block manager sketched on page 3 ("KV Cache ... PagedAttention",
+devpress.csdn.net, §七 "PagedAttention 如何解决显存碎片"):
+
+* a free list that starts as the given order (the page uses range(n)) and is
+  popped from its end;
+* a sequence of n tokens holds ceil(n / block_size) blocks, and a new block is
+  taken exactly when the token count reaches the capacity (used >= capacity);
+* running out of free blocks is an error;
+* releasing a sequence returns its blocks to the end of the free list.
+
+and adds what that section lists as missing from its sketch (block reference
+counts, prefix sharing, copy-on-write), as page 2 ("ybb.press" §2.1, best-of-N
+sharing that copies a block only when it is modified) describes:
+
+* fork(parent) gives the child the parent's block table and raises the
+  reference count of every block in it;
+* appending into a partially filled tail block whose reference count is above
+  one first takes a fresh block, records the pair (old, fresh) as a block copy,
+  moves this sequence's table entry to the fresh block and lowers the old
+  block's count. The copy block is taken before any new tail blocks;
+* release lowers every count and frees the blocks that reach zero, in table
+  order.
+
+An append is all-or-nothing: if the free list cannot cover it, nothing changes.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence, Tuple
+
+
+class OutOfBlocks(RuntimeError):
+    pass
+
+
+class BadSequence(KeyError):
+    pass
+
+
+class BlockPool:
+    def __init__(self, num_blocks: int, block_size: int = 16,
+                 free_order: Optional[Sequence[int]] = None):
+        if num_blocks < 0 or block_size <= 0:
+            raise ValueError("bad pool shape")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        if free_order is None:
+            free_order = range(num_blocks)
+        self.free: List[int] = [int(b) for b in free_order]
+        if sorted(self.free) != list(range(num_blocks)):
+            raise ValueError("free_order must be a permutation of range(num_blocks)")
+        self.ref: List[int] = [0] * num_blocks
+        self.tables: Dict[int, List[int]] = {}
+        self.lens: Dict[int, int] = {}
+        self._next = 0
+
+    # -- sequences ---------------------------------------------------------
+    def create(self) -> int:
+        sid = self._next
+        self._next += 1
+        self.tables[sid] = []
+        self.lens[sid] = 0
+        return sid
+
+    def _get(self, sid: int) -> List[int]:
+        if sid not in self.tables:
+            raise BadSequence(sid)
+        return self.tables[sid]
+
+    def fork(self, parent: int) -> int:
+        table = self._get(parent)
+        child = self.create()
+        self.tables[child] = list(table)
+        self.lens[child] = self.lens[parent]
+        for b in table:
+            self.ref[b] += 1
+        return child
+
+    def append_slots(self, sid: int, n: int) -> Tuple[List[int], Optional[Tuple[int, int]]]:
+        """Reserve n token slots; returns (slots, copy pair or None)."""
+        table = self._get(sid)
+        if n < 0:
+            raise ValueError("n < 0")
+        bs = self.block_size
+        L = self.lens[sid]
+        if n == 0:
+            return [], None
+        cow = (L % bs != 0) and self.ref[table[-1]] > 1
+        new_blocks = -(-(L + n) // bs) - len(table)
+        if new_blocks + (1 if cow else 0) > len(self.free):
+            raise OutOfBlocks(f"need {new_blocks + int(cow)} blocks, {len(self.free)} free")
+        pair = None
+        if cow:
+            src = table[-1]
+            dst = self.free.pop()
+            self.ref[src] -= 1
+            self.ref[dst] = 1
+            table[-1] = dst
+            pair = (src, dst)
+        slots = []
+        for i in range(n):
+            pos = L + i
+            if pos >= len(table) * bs:
+                b = self.free.pop()
+                self.ref[b] = 1
+                table.append(b)
+            slots.append(table[pos // bs] * bs + pos % bs)
+        self.lens[sid] = L + n
+        return slots, pair
+
+    def release(self, sid: int) -> None:
+        table = self._get(sid)
+        for b in table:
+            if self.ref[b] <= 0:
+                raise RuntimeError(f"refcount underflow on block {b}")
+        for b in table:
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free.append(b)
+        del self.tables[sid]
+        del self.lens[sid]
+
+    # -- views -------------------------------------------------------------
+    def block_table(self, sid: int) -> List[int]:
+        return list(self._get(sid))
+
+    def stats(self) -> Tuple[int, int, int]:
+        used = sum(1 for r in self.ref if r > 0)
+        shared = sum(1 for r in self.ref if r > 1)
+        return len(self.free), used, shared
