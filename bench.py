@@ -1,0 +1,410 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged decode step (copy-on-write block copies, KV append,
+paged decode attention, split-KV reduce) through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama3_8b|tiny|llama2_70b_best_of_5|long_context]
+
+Prints one JSON line. `value` is KV GB/s: the algorithmic bytes of a step
+(K and V read by attention + q read + output written + the appended K/V
+rows written) over the device time of the step, inputs resident in HBM, L2
+flushed between steps (each step timed alone with CUDA events). Sequences
+are independent, so N ranks each run their own replica of the batch
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak); seq-steps/s at 1 GPU"
+PROFILE = os.path.join(ROOT, "profiles", "paged_decode_llama3_8b.md")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b")
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def step_bytes(wl, out_bytes_per_elem=4):
+    """Algorithmic bytes of one step: every sequence's K and V for all its
+    tokens (the attention must read them), q, the output, and the appended
+    rows (written once)."""
+    kv_elem = 1 if wl.kv_dtype == "int8" else 2
+    per_tok = 2 * wl.num_kv_heads * wl.head_dim * kv_elem
+    if wl.kv_dtype == "int8":
+        per_tok += 2 * wl.num_kv_heads * 5          # fp32 scale + int8 zero point, K and V
+    kv_read = sum(wl.context_lens) * per_tok
+    nq = sum(wl.q_lens)
+    q_b = nq * wl.num_heads * wl.head_dim * 2
+    out_b = nq * wl.num_heads * wl.head_dim * out_bytes_per_elem
+    appended = nq * per_tok
+    return {"kv_read": kv_read, "q": q_b, "out": out_b, "append_write": appended,
+            "decode": kv_read + q_b + out_b, "step": kv_read + q_b + out_b + appended}
+
+
+def kernel_digest():
+    h = hashlib.sha256()
+    for f in ("paged_decode.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_154_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != kernel_digest():
+        return None
+    return float(m_b.group(1))
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 50 ms in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.samples = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                self.samples.append({"sm": float(parts[1]), "max": float(parts[2]),
+                                     "hw": parts[4], "hw_thermal": parts[5],
+                                     "sw_thermal": parts[6], "sw_power": parts[7]})
+            except ValueError:
+                pass
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sms = [s["sm"] for s in self.samples]
+        reasons = set()
+        for s in self.samples:
+            for k, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                            ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if s[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(s["max"] for s in self.samples),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def build_state(wl, device, partition_size):
+    import torch
+    from paged_kv_cache_154_gb300.engine import PagedKVCache
+    cache = PagedKVCache(wl.num_blocks, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
+                         device=device, free_order=wl.free_order)
+    names = {}
+    for ops in wl.phases:
+        cache.run_phase(ops, names)
+    si = cache.prepare_step(wl.step, names, wl.q, torch.float32, partition_size)
+    torch.cuda.synchronize()
+    return cache, si
+
+
+def launches_per_step(si, partition_size):
+    P = partition_size or 512
+    n = 1 + 1                                           # append, decode
+    if si.pairs is not None:
+        n += 1                                          # copy_blocks
+    if si.max_context_len > P:
+        n += 1                                          # split-KV reduce
+    return n
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import workloads as W
+    import paged_kv_cache_154_gb300 as pa
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    wl = W.NAMED[args.workload]()
+    cache, si = build_state(wl, device, args.partition_size)
+    nbytes = step_bytes(wl)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
+
+    def step():
+        cache.step(si, wl.scale, args.partition_size)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    time.sleep(0.15)
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush.fill_(k & 0xFF)                                   # evict the previous step from L2
+        ev[k][0].record(stream)
+        if si.pairs is not None:
+            pa.copy_blocks(cache.k, cache.v, si.pairs, cache.num_blocks, cache.k_scale,
+                           cache.v_scale, cache.k_zp, cache.v_zp)
+        pa.append_kv(si.key, si.value, cache.k, cache.v, si.slots, cache.num_blocks,
+                     cache.k_scale, cache.v_scale, cache.k_zp, cache.v_zp)
+        ev[k][1].record(stream)
+        pa.decode(si.out, si.q, cache.k, cache.v, si.block_tables, si.context_lens,
+                  si.max_context_len, wl.scale, si.query_start_loc, si.max_q_len,
+                  cache.num_blocks, cache.k_scale, cache.v_scale, cache.k_zp, cache.v_zp,
+                  args.partition_size, si.workspace)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall1 = time.perf_counter()
+    time.sleep(0.1)
+    sampler.stop()
+    assert pa.device_error() == 0
+    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
+    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    tot_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([tot_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot_ms = float(t.item())
+
+    # end to end: host (pinned) inputs copied in, result copied out, every step
+    e2e = measure_e2e(wl, cache, si, args, K_e2e=min(K, 50))
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = measured_peak()
+    dec_avg_s = statistics.mean(dec_ms) / 1e3
+    achieved = nbytes["decode"] / dec_avg_s / 1e9
+    value = world * K * nbytes["step"] / (tot_ms / 1e3) / 1e9
+    seq_steps = world * K * wl.num_seqs / (tot_ms / 1e3)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(tot_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.kv_dtype,
+        "data": "synthetic (seeded N(0,1) K/V/q, seeded lengths and block placement)",
+        "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "block_size": 16, "context_tokens": sum(wl.context_lens),
+                   "partition_size": args.partition_size or 512,
+                   "l2": "flushed between steps (2x L2 write), each step timed alone",
+                   "bytes_per_step": nbytes, "parallelism": f"replicas x{world}"},
+        "seq_steps_per_s": round(seq_steps, 1),
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "roofline": {"kernel": "pa_decode (paged_decode_kernel + split_kv_reduce_kernel)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(),
+                     "algorithmic_bytes_per_launch": nbytes["decode"],
+                     "decode_ms_avg": round(dec_avg_s * 1e3, 5),
+                     "decode_ms_p50": round(statistics.median(dec_ms), 5)},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step(si, args.partition_size) * K,
+        "clocks": sampler.summary(),
+        "wall_s_timed": round(wall1 - wall0, 3),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=12.0)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_e2e(wl, cache, si, args, K_e2e):
+    """Same metric through the public API with host buffers: per step, copy
+    q, the new K/V rows, the slots, block tables, lengths (and copy pairs)
+    from pinned host memory, run the step, copy the output back, sync."""
+    import torch
+    import paged_kv_cache_154_gb300 as pa
+    host = {}
+    for name in ("q", "key", "value", "slots", "block_tables", "context_lens", "pairs",
+                 "query_start_loc"):
+        t = getattr(si, name)
+        host[name] = None if t is None else t.cpu().pin_memory()
+    out_h = torch.empty(si.out.shape, dtype=si.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = out_h.numel() * out_h.element_size()
+    stream = torch.cuda.current_stream()
+    times = []
+    for k in range(K_e2e + 3):
+        t0 = time.perf_counter()
+        for name, t in host.items():
+            if t is not None:
+                getattr(si, name).copy_(t, non_blocking=True)
+        cache.step(si, wl.scale, args.partition_size)
+        out_h.copy_(si.out, non_blocking=True)
+        stream.synchronize()
+        if k >= 3:
+            times.append(time.perf_counter() - t0)
+    nbytes = step_bytes(wl)["step"]
+    return {"value": round(len(times) * nbytes / sum(times) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(1e3 * statistics.mean(times), 4), "steps": len(times)}
+
+
+def cpu_baseline(wl, budget_s=12.0, sample_seqs=None):
+    """The oracle (plain C, fp64, OpenMP over (sequence, kv head)) on a
+    bounded sample of the workload's sequences, same metric (GB/s of the
+    attention's algorithmic bytes for the sampled sequences)."""
+    import numpy as np
+    import oracle
+    threads = os.cpu_count() or 1
+    run = oracle.run(wl, decode=False)
+    n = wl.num_seqs if sample_seqs is None else min(sample_seqs, wl.num_seqs)
+    qsl = wl.query_start_loc[: n + 1]
+    nbytes = 0
+    kv_elem = 1 if wl.kv_dtype == "int8" else 2
+    for s in range(n):
+        nbytes += 2 * wl.context_lens[s] * wl.num_kv_heads * wl.head_dim * kv_elem
+    nq = int(qsl[-1])
+    nbytes += nq * wl.num_heads * wl.head_dim * (2 + 4)
+    reps, t_total = 0, 0.0
+    while t_total < budget_s and reps < 50:
+        t0 = time.perf_counter()
+        oracle.attend(run.q64[:nq], run.cache, run.block_tables[:n], run.context_lens[:n],
+                      qsl, wl.num_heads, wl.scale, threads=threads)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": round(reps * nbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n} of {wl.num_seqs} sequences (all heads), attention only, "
+                      f"{reps} repetitions in {t_total:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step one bounded sample of the
+    workload on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import workloads as W
+    import oracle
+    wl = W.NAMED[args.workload]()
+    threads = os.cpu_count() or 1
+    run = oracle.run(wl, decode=False)
+    # bounded sample: the first sequences whose keys add up to ~1/8 of the batch
+    target = sum(wl.context_lens) / 8
+    n, acc = 0, 0
+    while n < wl.num_seqs and acc < target:
+        acc += wl.context_lens[n]
+        n += 1
+    qsl = wl.query_start_loc[: n + 1]
+    nq = int(qsl[-1])
+    kv_elem = 1 if wl.kv_dtype == "int8" else 2
+    nbytes = sum(2 * wl.context_lens[s] * wl.num_kv_heads * wl.head_dim * kv_elem
+                 for s in range(n)) + nq * wl.num_heads * wl.head_dim * 6
+
+    def step():
+        oracle.attend(run.q64[:nq], run.cache, run.block_tables[:n], run.context_lens[:n],
+                      qsl, wl.num_heads, wl.scale, threads=threads)
+
+    for _ in range(max(3, args.warmup) if args.warmup < 3 else args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps * nbytes / dt / 1e9
+    sample = f"{n} of {wl.num_seqs} sequences (all heads) per step, attention only"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

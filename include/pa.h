@@ -1,0 +1,230 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache decode-attention library (libpa.so).
+ *
+ * Decode-phase attention over a KV cache split into fixed 16-token blocks
+ * held in one physical pool and mapped per sequence by a block table.
+ * Sources (page title, then section):
+ *   [p1] "大模型推理优化全攻略" (zhengtianqi.github.io) §2.1 why a KV cache,
+ *        §2.3 PagedAttention (16-token blocks, on-demand allocation)
+ *   [p2] "LLM推理优化深度实战" (ybb.press) §2.1 PagedAttention, copy-on-write,
+ *        best-of-N sharing; §2.2 GQA; §5.2 KV-cache quantisation
+ *   [p3] "KV Cache ... PagedAttention" (devpress.csdn.net) §二 attention
+ *        formula and KV memory formula; §七 block table and block manager
+ *   [p4] "cs336 lecture 10" notes: KV Cache workflow (decode step), GQA/MQA,
+ *        Quantization formula, speculative decoding (verify)
+ *
+ * Conventions for every call:
+ *   - Every call returns a pa_status; no C++ exception crosses the ABI.
+ *     On failure, pa_last_error() returns a message (thread-local, valid
+ *     until the next call on the same thread).
+ *   - Argument errors are detected on the host before any launch.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream). Launch failures return PA_ERR_CUDA; faults
+ *     that happen later surface at the caller's next synchronisation.
+ *   - The library allocates no device memory. Every device pointer is
+ *     caller-owned memory; the caller keeps it alive until the work on
+ *     `stream` has finished.
+ *   - Contents of device arrays (block-table entries, lengths, slots) are the
+ *     caller's contract. With the environment variable PA_VALIDATE=1 the
+ *     device calls copy them to the host first (synchronising `stream`) and
+ *     range-check them, returning PA_ERR_VALIDATION on a bad entry.
+ *
+ * Memory layout (this library's choice; the pages fix none):
+ *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim],
+ *                      element type kv_dtype (F16, BF16 or INT8 codes).
+ *                      Each (block, kv head) tile is contiguous.
+ *   k_scale, v_scale : INT8 only, fp32 [num_blocks][num_kv_heads][block_size]
+ *   k_zp, v_zp       : INT8 only, int8 [num_blocks][num_kv_heads][block_size]
+ *   slot             : phys_block * block_size + offset (int64); < 0 = skip
+ *   block_tables     : int32 [num_seqs][max_blocks_per_seq]; entry b of row s
+ *                      is the physical block holding tokens 16b .. 16b+15 of
+ *                      sequence s ([p3] §七: logical block -> physical block)
+ *   q, out           : [num_q_tokens][num_heads][head_dim], rows of sequence s
+ *                      at query_start_loc[s] .. query_start_loc[s+1]-1
+ *   GQA/MQA          : q head h reads kv head h / (num_heads / num_kv_heads)
+ *                      ([p4] GQA: heads split into contiguous groups; MQA is
+ *                      num_kv_heads == 1)
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* bad pointer, size, shape or id */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. block_size != 16) */
+    PA_ERR_OUT_OF_BLOCKS = 3, /* the pool cannot cover an append; nothing changed */
+    PA_ERR_BAD_REFCOUNT = 4,  /* refcount underflow (double free) */
+    PA_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    PA_ERR_VALIDATION = 6,    /* PA_VALIDATE found a bad device-array entry */
+    PA_ERR_DEVICE = 7         /* a kernel reported an error word (see pa_device_error) */
+} pa_status;
+
+typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2, PA_INT8 = 3 } pa_dtype;
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* pa_last_error(void);
+/* Library version string. */
+const char* pa_version(void);
+
+/* ======================================================================
+ * Host block pool ([p3] §七 KVBlockManager; refcounts and copy-on-write per
+ * [p2] §2.1). Owns host metadata only, never device memory. Not thread-safe:
+ * one pool per thread, or external locking.
+ * ==================================================================== */
+typedef struct pa_pool pa_pool;
+
+/* Create a pool of num_blocks physical blocks. The free list starts as
+ * free_order[0..num_blocks-1] (a permutation of 0..num_blocks-1) or, if
+ * free_order is NULL, as 0..num_blocks-1; blocks are taken from its END and
+ * returned to its end ([p3]'s list(range(n)) / pop() / extend()).
+ * block_size must be 16. */
+pa_status pa_pool_create(int32_t num_blocks, int32_t block_size,
+                         const int32_t* free_order, pa_pool** out);
+void pa_pool_destroy(pa_pool* pool);
+
+/* New empty sequence; ids are 0, 1, 2, ... in creation order, never reused. */
+pa_status pa_seq_create(pa_pool* pool, int32_t* seq_id);
+
+/* Child sharing every block of parent (refcount + 1 on each): best-of-N
+ * parallel sampling shares the prompt's blocks ([p2] §2.1). */
+pa_status pa_seq_fork(pa_pool* pool, int32_t parent, int32_t* child);
+
+/* Reserve n_tokens new token slots at the end of sequence `seq` and write
+ * their slots to slots_out[0..n_tokens-1]. A new block is taken exactly when
+ * the token count reaches the capacity ([p3] append_token). If the tail
+ * block is partly filled and shared (refcount > 1), it is copied first: a
+ * fresh block replaces it in this sequence's table, the old block's refcount
+ * drops by one, and the pair (old, fresh) is written to cow_pair_out[0..1]
+ * with *n_cow = 1 (else *n_cow = 0). The copy block is taken before any new
+ * tail block. The caller must run pa_copy_blocks on the returned pairs
+ * before pa_append_kv writes the slots. All-or-nothing: on
+ * PA_ERR_OUT_OF_BLOCKS nothing changes. */
+pa_status pa_seq_append_slots(pa_pool* pool, int32_t seq, int32_t n_tokens,
+                              int64_t* slots_out, int32_t* cow_pair_out,
+                              int32_t* n_cow);
+
+/* Release a sequence: refcount - 1 on each block; blocks reaching 0 go back
+ * to the end of the free list in table order ([p3] release). */
+pa_status pa_seq_free(pa_pool* pool, int32_t seq);
+
+/* Number of tokens held by a sequence. */
+pa_status pa_seq_len(pa_pool* pool, int32_t seq, int32_t* len);
+
+/* Block tables of n sequences into tables_out[n][max_blocks] (entries past a
+ * sequence's blocks are -1) and their lengths into lens_out[n] (may be NULL).
+ * PA_ERR_INVALID_ARG if a sequence holds more than max_blocks blocks. */
+pa_status pa_pool_block_tables(pa_pool* pool, const int32_t* seqs, int32_t n,
+                               int32_t max_blocks, int32_t* tables_out,
+                               int32_t* lens_out);
+
+/* free = blocks on the free list, used = refcount > 0, shared = refcount > 1
+ * (KV-cache utilisation, [p2] §7.3). Any output pointer may be NULL. */
+pa_status pa_pool_stats(pa_pool* pool, int32_t* free_blocks, int32_t* used,
+                        int32_t* shared);
+
+/* Reference count of one physical block. */
+pa_status pa_pool_refcount(pa_pool* pool, int32_t block, int32_t* ref);
+
+/* ======================================================================
+ * Device operations. Pointers are device memory unless stated.
+ * ==================================================================== */
+
+/* Copy-on-write block copies ([p2] §2.1: copy a shared block only when it
+ * is modified). For each i < n_pairs, copies physical block d_pairs[2i] to
+ * d_pairs[2i+1] in k_cache and v_cache and, for INT8, in k_scale, v_scale,
+ * k_zp, v_zp (pass NULL for those otherwise). d_pairs: device int32
+ * [n_pairs][2]. Sources and destinations must be distinct blocks, and no
+ * destination may also be a source. n_pairs == 0 is a no-op. */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, void* k_scale,
+                         void* v_scale, void* k_zp, void* v_zp,
+                         const int32_t* d_pairs, int32_t n_pairs,
+                         int32_t num_blocks, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size,
+                         pa_dtype kv_dtype, void* stream);
+
+/* Append the new tokens' K and V to the cache through slot_mapping ([p4]
+ * decode workflow: append the new K, V to the KV cache; [p3] §二 K_cache =
+ * [K1 .. Kt]). key, value: [num_tokens][num_kv_heads][head_dim] of
+ * src_dtype (F16 or BF16). For kv_dtype F16/BF16 (== src_dtype) the rows are
+ * copied bit for bit. For kv_dtype INT8 each (token, kv head) row is
+ * quantised ([p4] Quantization, x_q = round(x/scale) + zero_point): with
+ * mn = min(row, 0), mx = max(row, 0) in fp32, scale = (mx - mn)/255 (1 if
+ * 0), zp = clamp(-128 - rint(mn/scale)), code = clamp(rint(x/scale) + zp),
+ * IEEE fp32 division and round-half-to-even; scale and zp are stored per
+ * (token, kv head) ([p2] §5.2: per-head rather than global scales).
+ * slot_mapping: device int64 [num_tokens]; a negative slot skips the token. */
+pa_status pa_append_kv(const void* key, const void* value, pa_dtype src_dtype,
+                       void* k_cache, void* v_cache, pa_dtype kv_dtype,
+                       float* k_scale, float* v_scale, int8_t* k_zp,
+                       int8_t* v_zp, const int64_t* slot_mapping,
+                       int32_t num_tokens, int32_t num_blocks,
+                       int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size, void* stream);
+
+/* Bytes of workspace pa_decode needs (0 when every sequence fits one
+ * partition). partition_size 0 selects the default (512). */
+size_t pa_decode_workspace_size(int32_t num_q_tokens, int32_t num_heads,
+                                int32_t head_dim, int32_t max_context_len,
+                                int32_t partition_size);
+
+/* Decode attention ([p3] §二 softmax(Q K^T / sqrt(d)) V over the cached
+ * keys; [p4] decode workflow: score the new token's q against every cached
+ * K and take the weighted sum of the cached V).
+ *   out            [num_q_tokens][num_heads][head_dim], out_dtype F32 or
+ *                  the q dtype
+ *   q              [num_q_tokens][num_heads][head_dim], q_dtype F16/BF16;
+ *                  for F16/BF16 caches q_dtype must equal kv_dtype
+ *   context_lens   int32 [num_seqs]: tokens in each sequence INCLUDING the
+ *                  ones appended this step (append runs before attention)
+ *   query_start_loc int32 [num_seqs + 1] or NULL (then one query token per
+ *                  sequence and num_q_tokens == num_seqs). A run of r query
+ *                  tokens (speculative verify, [p4]: the target model checks
+ *                  the draft tokens in one pass) puts query i at position
+ *                  L - r + i; it sees keys 0 .. L - r + i (causal).
+ *   max_q_len      the largest r (1 when query_start_loc is NULL)
+ *   max_context_len the largest context length (host value)
+ *   scale          softmax scale, usually 1/sqrt(head_dim)
+ *   partition_size split-KV partition in tokens (multiple of 16; 0 = 512).
+ *                  Sequences longer than one partition are split; each
+ *                  partition's (o, m, l) goes to the workspace and a
+ *                  log-sum-exp reduce writes `out`.
+ *   workspace      device memory of pa_decode_workspace_size() bytes,
+ *                  256-byte aligned (NULL allowed if that size is 0). Layout,
+ *                  with P = ceil(max_context_len / partition_size):
+ *                    o_part fp32 [num_q_tokens][num_heads][P][head_dim]
+ *                    m_part fp32 [num_q_tokens][num_heads][P] (base-2 log
+ *                           domain: max of logit * log2(e))
+ *                    l_part fp32 [num_q_tokens][num_heads][P]
+ *                  each region starting on a 256-byte boundary.
+ * Requirements: head_dim 64 or 128, block_size 16, num_heads a multiple of
+ * num_kv_heads, context_lens[s] >= (query run length of s) >= 1. */
+pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
+                    pa_dtype q_dtype, const void* k_cache, const void* v_cache,
+                    pa_dtype kv_dtype, const float* k_scale,
+                    const float* v_scale, const int8_t* k_zp,
+                    const int8_t* v_zp, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    const int32_t* query_start_loc, int32_t num_seqs,
+                    int32_t num_q_tokens, int32_t max_q_len,
+                    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t block_size, int32_t num_blocks, float scale,
+                    int32_t max_context_len, int32_t partition_size,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Read and clear the device error word that kernels set instead of
+ * trapping (a bounded wait that gave up, an index a kernel refused).
+ * Synchronises `stream`. *code = 0 when no error was recorded; returns
+ * PA_ERR_DEVICE when *code != 0. */
+pa_status pa_device_error(void* stream, uint32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H_ */

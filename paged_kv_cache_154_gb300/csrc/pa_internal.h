@@ -1,0 +1,107 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// Records a formatted message for pa_last_error() and returns `s`.
+pa_status fail(pa_status s, const char* fmt, ...);
+// Maps a CUDA error to PA_ERR_CUDA with a message; PA_OK on cudaSuccess.
+pa_status cuda_status(cudaError_t e, const char* what);
+
+// Pointer to this device's error word (kernels OR codes into it instead of
+// trapping). Null if it cannot be resolved.
+unsigned int* device_error_word();
+
+// Error codes OR-ed into the device error word.
+enum : unsigned int {
+    ERR_WAIT_FULL = 1u << 0,    // consumer gave up waiting for a staged tile
+    ERR_WAIT_EMPTY = 1u << 1,   // producer gave up waiting for a free stage
+    ERR_WAIT_DRAIN = 1u << 2,   // exit drain gave up on an in-flight copy
+    ERR_BAD_BLOCK = 1u << 3,    // a block-table entry outside the pool
+    ERR_BAD_SLOT = 1u << 4,     // a slot outside the pool
+};
+
+inline int dtype_bytes(pa_dtype t) {
+    switch (t) {
+        case PA_F16: case PA_BF16: return 2;
+        case PA_F32: return 4;
+        case PA_INT8: return 1;
+    }
+    return 0;
+}
+
+bool validate_enabled();
+
+struct AppendArgs {
+    const void* key;
+    const void* value;
+    pa_dtype src_dtype;
+    void* k_cache;
+    void* v_cache;
+    pa_dtype kv_dtype;
+    float* k_scale;
+    float* v_scale;
+    int8_t* k_zp;
+    int8_t* v_zp;
+    const int64_t* slots;
+    int32_t num_tokens;
+    int32_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    cudaStream_t stream;
+};
+pa_status launch_append_kv(const AppendArgs& a);
+
+struct CopyArgs {
+    void* arrays[6];          // k, v, k_scale, v_scale, k_zp, v_zp (unused = null)
+    int64_t bytes_per_block[6];
+    const int32_t* pairs;
+    int32_t n_pairs;
+    int32_t num_blocks;
+    cudaStream_t stream;
+};
+pa_status launch_copy_blocks(const CopyArgs& a);
+
+struct DecodeArgs {
+    void* out;
+    pa_dtype out_dtype;
+    const void* q;
+    pa_dtype q_dtype;
+    const void* k_cache;
+    const void* v_cache;
+    pa_dtype kv_dtype;
+    const float* k_scale;
+    const float* v_scale;
+    const int8_t* k_zp;
+    const int8_t* v_zp;
+    const int32_t* block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t* context_lens;
+    const int32_t* query_start_loc;
+    int32_t num_seqs;
+    int32_t num_q_tokens;
+    int32_t max_q_len;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t num_blocks;
+    float scale;
+    int32_t max_context_len;
+    int32_t partition_size;
+    int32_t num_partitions;
+    float* o_part;
+    float* m_part;
+    float* l_part;
+    cudaStream_t stream;
+};
+pa_status launch_decode(const DecodeArgs& a);
+
+}  // namespace pa

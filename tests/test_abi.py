@@ -1,0 +1,142 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol include/pa.h
+declares, its host block pool agrees with the oracle's model operation by
+operation, and argument errors are caught on the host before any launch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_154_gb300 as pa
+from oracle.allocator import BlockPool, OutOfBlocks
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_154_gb300 import build
+    build.build()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_symbols()
+    assert len(names) >= 17
+    L = ctypes.CDLL(pa.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert "sm_103a" in pa.version()
+
+
+def test_pool_matches_oracle_model_on_random_ops():
+    rng = np.random.default_rng(3)
+    order = rng.permutation(300).astype(np.int32)
+    c = pa.Pool(300, 16, order)
+    m = BlockPool(300, 16, order)
+    live = []
+    for step in range(4000):
+        op = int(rng.integers(0, 4))
+        if op == 0 or not live:
+            a, b = c.seq_create(), m.create()
+            assert a == b
+            live.append(a)
+        elif op == 1:
+            p = live[int(rng.integers(len(live)))]
+            a, b = c.seq_fork(p), m.fork(p)
+            assert a == b
+            live.append(a)
+        elif op == 2:
+            s = live[int(rng.integers(len(live)))]
+            n = int(rng.integers(0, 50))
+            try:
+                ms, mp = m.append_slots(s, n)
+            except OutOfBlocks:
+                with pytest.raises(pa.PAError) as e:
+                    c.seq_append_slots(s, n)
+                assert e.value.status == 3
+                victim = live.pop(0)
+                c.seq_free(victim)
+                m.release(victim)
+                continue
+            cs, cp = c.seq_append_slots(s, n)
+            assert cs.tolist() == ms and cp == mp
+        else:
+            s = live.pop(int(rng.integers(len(live))))
+            c.seq_free(s)
+            m.release(s)
+        if step % 97 == 0 and live:
+            mb = max(1, max(len(m.block_table(s)) for s in live))
+            tables, lens = c.block_tables(live, mb)
+            for i, s in enumerate(live):
+                t = m.block_table(s)
+                assert tables[i, :len(t)].tolist() == t and (tables[i, len(t):] == -1).all()
+                assert lens[i] == m.lens[s]
+            assert c.stats() == m.stats()
+            for b in range(0, 300, 7):
+                assert c.refcount(b) == m.ref[b]
+
+
+def test_pool_errors():
+    with pytest.raises(pa.PAError) as e:
+        pa.Pool(8, 32)
+    assert e.value.status == 2                           # block size other than 16
+    with pytest.raises(pa.PAError):
+        pa.Pool(4, 16, [0, 1, 1, 2])                     # not a permutation
+    p = pa.Pool(4, 16)
+    s = p.seq_create()
+    with pytest.raises(pa.PAError) as e:
+        p.seq_append_slots(s, 65)
+    assert e.value.status == 3 and p.seq_len(s) == 0 and p.stats() == (4, 0, 0)
+    p.seq_free(s)
+    with pytest.raises(pa.PAError) as e:
+        p.seq_free(s)                                    # double free
+    assert e.value.status == 1
+    with pytest.raises(pa.PAError):
+        p.seq_fork(99)
+
+
+def test_device_calls_reject_bad_arguments_on_the_host():
+    L = pa.lib()
+    # NULL pointers, unsupported head_dim / block_size: nothing is launched
+    st = L.pa_decode(None, 2, None, 1, None, None, 1, None, None, None, None, None, 4, None,
+                     None, 2, 2, 1, 8, 2, 128, 16, 10, 0.1, 64, 0, None, 0, None)
+    assert st == 1
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.addressof(buf)
+    st = L.pa_decode(p, 2, p, 1, p, p, 1, None, None, None, None, p, 4, p, None, 2, 2, 1, 8,
+                     2, 96, 16, 10, 0.1, 64, 0, None, 0, None)
+    assert st == 2 and b"head_dim" in L.pa_last_error()
+    st = L.pa_decode(p, 2, p, 1, p, p, 1, None, None, None, None, p, 4, p, None, 2, 2, 1, 8,
+                     3, 128, 16, 10, 0.1, 64, 0, None, 0, None)
+    assert st == 1                                       # 8 heads over 3 KV heads
+    st = L.pa_decode(p, 2, p, 0, p, p, 1, None, None, None, None, p, 4, p, None, 2, 2, 1, 8,
+                     2, 128, 16, 10, 0.1, 64, 0, None, 0, None)
+    assert st == 2                                       # q fp16 against a bf16 cache
+    st = L.pa_decode(p, 2, p, 1, p, p, 1, None, None, None, None, p, 4, p, None, 2, 2, 1, 8,
+                     2, 128, 16, 10, 0.1, 4096, 0, None, 0, None)
+    assert st == 1 and b"max_blocks" in L.pa_last_error()   # table too narrow
+    st = L.pa_decode(p, 2, p, 1, p, p, 1, None, None, None, None, p, 512, p, None, 2, 2, 1, 8,
+                     2, 128, 16, 10, 0.1, 4096, 0, None, 0, None)
+    assert st == 1 and b"workspace" in L.pa_last_error()    # split-KV needs a workspace
+    st = L.pa_append_kv(p, p, 1, p, p, 0, None, None, None, None, p, 3, 10, 2, 128, 16, None)
+    assert st == 2                                       # bf16 rows into an fp16 cache
+    st = L.pa_append_kv(p, p, 1, p, p, 3, None, None, None, None, p, 3, 10, 2, 128, 16, None)
+    assert st == 1                                       # INT8 cache without scales
+    st = L.pa_copy_blocks(p, p, None, None, None, None, p, 1, 10, 2, 128, 8, 1, None)
+    assert st == 2                                       # block_size 8
+    assert L.pa_copy_blocks(None, None, None, None, None, None, None, 0, 10, 2, 128, 16, 1,
+                            None) == 0                   # nothing to copy
+
+
+def test_workspace_size():
+    assert pa.decode_workspace_size(64, 32, 128, 512, 512) == 0
+    n = pa.decode_workspace_size(4, 32, 128, 131072, 512)
+    rows = 4 * 32 * 256
+    assert n == rows * 128 * 4 + 2 * rows * 4

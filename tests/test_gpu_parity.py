@@ -1,0 +1,165 @@
+"""CUDA path vs the CPU oracle on the same seeded inputs (needs a GB300).
+
+Append and block copies must match bit for bit (the whole pool, canary
+blocks included); attention within max abs error 2e-3 for 16-bit caches
+(fp32 accumulate, fp32 output)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+import paged_kv_cache_154_gb300 as pa
+from gpu_harness import check_cache_bits, check_out, run_both, THREADS
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_154_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+SMALL = [
+    # name, lens, q_lens, H, Hkv, d, dtype, partition
+    ("gqa4_bf16_d128", [1, 15, 16, 17, 100, 513, 1000, 1500], [1] * 8, 32, 8, 128, "bf16", 0),
+    ("gqa4_bf16_p128", [1, 15, 16, 17, 100, 513, 1000, 1500], [1] * 8, 32, 8, 128, "bf16", 128),
+    ("gqa8_bf16", [300, 777, 64, 2049], [1] * 4, 64, 8, 128, "bf16", 256),
+    ("mha_f16_d64", [5, 33, 700], [1] * 3, 4, 4, 64, "f16", 0),
+    ("mqa16_f16_d64", [90, 1024, 31], [1] * 3, 16, 1, 64, "f16", 512),
+    ("verify_gqa4", [40, 5, 600, 1030, 77], [5, 5, 2, 4, 1], 16, 4, 128, "bf16", 512),
+    ("verify_gqa8_2tiles", [513, 1026, 96, 2000], [4, 3, 2, 1], 32, 4, 128, "bf16", 512),
+    ("verify_straddles_partition", [513, 514, 517], [5, 5, 5], 8, 2, 64, "bf16", 512),
+    ("max_partition", [4096, 4097, 9000], [1, 1, 1], 16, 4, 128, "bf16", 4096),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: c[0])
+def test_small_shapes(case):
+    name, lens, qlens, H, Hkv, d, dt, part = case
+    wl = W.simple(name, 100 + len(name), lens, qlens, H, Hkv, d, dt)
+    ref, cache, si, out = run_both(wl, partition_size=part)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, dt)
+
+
+def test_tiny_config():
+    wl = W.tiny()
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, "f16")
+    # and forced through the split-KV path (partitions of one block)
+    _, _, _, out2 = run_both(wl, partition_size=16, oracle_run=ref)
+    check_out(ref, out2, "f16")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16])
+def test_output_in_q_dtype(out_dtype):
+    wl = W.simple("outbf16", 7, [100, 700, 1300], [1, 2, 1], 32, 8, 128, "bf16")
+    ref, cache, si, out = run_both(wl, out_dtype=out_dtype)
+    check_out(ref, out, "bf16", out_dtype)
+
+
+def test_partials_match_oracle_partitions():
+    """Split-KV partition outputs (o normalised, m in base-2 units, l) in the
+    workspace agree with the oracle over the same key ranges."""
+    P = 256
+    wl = W.simple("partials", 9, [700, 256, 1025], [1, 3, 2], 16, 4, 128, "bf16",
+                  key_row_boost=8.0, boost_fraction=0.02)
+    ref, cache, si, out = run_both(wl, partition_size=P)
+    check_out(ref, out, "bf16")
+    nq, H, D = si.out.shape
+    nparts = (si.max_context_len + P - 1) // P
+    ws = si.workspace
+    rows = nq * H * nparts
+    o_bytes = ((rows * D * 4 + 255) // 256) * 256
+    m_bytes = ((rows * 4 + 255) // 256) * 256
+    o_part = ws[:rows * D * 4].view(torch.float32).view(nq, H, nparts, D).cpu().numpy()
+    m_part = ws[o_bytes:o_bytes + rows * 4].view(torch.float32).view(nq, H, nparts).cpu().numpy()
+    l_part = ws[o_bytes + m_bytes:o_bytes + m_bytes + rows * 4].view(torch.float32).view(
+        nq, H, nparts).cpu().numpy()
+    qsl = wl.query_start_loc
+    for p in range(nparts):
+        o, m, l = oracle.attend(ref.q64, ref.cache, ref.block_tables, ref.context_lens, qsl,
+                                wl.num_heads, wl.scale, p * P, (p + 1) * P)
+        for s, L in enumerate(wl.context_lens):
+            if L <= P or p * P >= L:
+                continue                          # single partition / partition not launched
+            rs = slice(qsl[s], qsl[s + 1])
+            seen = l[rs] > 0
+            np.testing.assert_allclose(o_part[rs, :, p][seen], o[rs][seen], rtol=0, atol=2e-3)
+            np.testing.assert_allclose(m_part[rs, :, p][seen], m[rs][seen] * np.log2(np.e),
+                                       rtol=1e-5, atol=1e-4)
+            np.testing.assert_allclose(l_part[rs, :, p][seen], l[rs][seen], rtol=1e-4)
+            assert (l_part[rs, :, p][~seen] == 0).all()
+            assert np.isneginf(m_part[rs, :, p][~seen]).all()
+
+
+def test_llama3_8b_config():
+    wl = W.llama3_8b()
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, "bf16")
+
+
+def test_best_of_5_copy_on_write_config():
+    wl = W.llama2_70b_best_of_5()
+    ref, cache, si, out = run_both(wl)
+    assert si.pairs is not None and si.pairs.shape[0] >= 8       # the step copies shared tails
+    check_cache_bits(ref, cache)
+    check_out(ref, out, "bf16")
+    free, used, shared = cache.pool.stats()
+    assert (free, used, shared) == ref.pool.stats()
+
+
+@pytest.mark.slow
+def test_long_context_split_kv_config():
+    wl = W.long_context()
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, "bf16")
+
+
+def test_bad_block_id_is_reported_not_faulted():
+    wl = W.simple("badblk", 5, [40, 70], [1, 1], 8, 2, 64, "bf16")
+    ref, cache, si, out = run_both(wl)
+    bt = si.block_tables.clone()
+    bt[1, 2] = wl.num_blocks + 1000               # outside the pool
+    pa.decode(si.out, si.q, cache.k, cache.v, bt, si.context_lens, si.max_context_len,
+              wl.scale, num_blocks=cache.num_blocks)
+    assert pa.device_error() & (1 << 3)            # ERR_BAD_BLOCK, no fault
+    assert pa.device_error() == 0                  # the word was cleared
+
+
+def test_validate_mode_rejects_bad_tables(monkeypatch):
+    wl = W.simple("validate", 6, [40, 70], [1, 1], 8, 2, 64, "bf16")
+    ref, cache, si, out = run_both(wl)
+    monkeypatch.setenv("PA_VALIDATE", "1")
+    bt = si.block_tables.clone()
+    bt[0, 0] = -5
+    with pytest.raises(pa.PAError) as e:
+        pa.decode(si.out, si.q, cache.k, cache.v, bt, si.context_lens, si.max_context_len,
+                  wl.scale, num_blocks=cache.num_blocks)
+    assert e.value.status == 6
+    bad = si.slots.clone()
+    bad[0] = cache.num_blocks * 16 + 3
+    with pytest.raises(pa.PAError) as e:
+        pa.append_kv(si.key, si.value, cache.k, cache.v, bad, cache.num_blocks)
+    assert e.value.status == 6
+    # valid inputs still pass validation
+    pa.decode(si.out, si.q, cache.k, cache.v, si.block_tables, si.context_lens,
+              si.max_context_len, wl.scale, num_blocks=cache.num_blocks)
+    torch.cuda.synchronize()
+
+
+def test_empty_inputs_are_no_ops():
+    wl = W.simple("empty", 8, [20], [1], 8, 2, 64, "bf16")
+    ref, cache, si, out = run_both(wl)
+    before = cache.k.clone()
+    pa.append_kv(si.key[:0], si.value[:0], cache.k, cache.v, si.slots[:0], cache.num_blocks)
+    pa.decode(si.out[:0], si.q[:0], cache.k, cache.v, si.block_tables[:0], si.context_lens[:0],
+              si.max_context_len, wl.scale, num_blocks=cache.num_blocks)
+    torch.cuda.synchronize()
+    assert torch.equal(before, cache.k)
