@@ -218,6 +218,46 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
                     int32_t max_context_len, int32_t partition_size,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* pa_decode without caller-provided workspace: the split-KV scratch is a
+ * built-in 16 MiB device array inside this library. The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate
+ * device memory themselves -- for example code embedded in a host
+ * application whose own allocator owns all device memory (a stray
+ * cudaMalloc would escape its accounting or fail under its memory cap), or
+ * a latency-critical decode loop that must not call cudaMalloc/cudaFree,
+ * which can synchronise the device.
+ *   - Arguments and results are exactly those of pa_decode, minus
+ *     workspace/workspace_bytes. The caller still passes (and owns) every
+ *     input and output buffer.
+ *   - If pa_decode_workspace_size() for these arguments exceeds 16 MiB
+ *     (16777216 bytes) the call returns PA_ERR_UNSUPPORTED and launches
+ *     nothing; a larger partition_size lowers the need.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *     library routine. Every GPU that loads the library holds the 16 MiB
+ *     array until the process exits.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero (each call writes every entry it
+ *     reads), but calls whose work overlaps on the GPU (different streams,
+ *     or different host threads) race on it and must be serialised. */
+pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
+                             pa_dtype q_dtype, const void* k_cache,
+                             const void* v_cache, pa_dtype kv_dtype,
+                             const float* k_scale, const float* v_scale,
+                             const int8_t* k_zp, const int8_t* v_zp,
+                             const int32_t* block_tables,
+                             int32_t max_blocks_per_seq,
+                             const int32_t* context_lens,
+                             const int32_t* query_start_loc, int32_t num_seqs,
+                             int32_t num_q_tokens, int32_t max_q_len,
+                             int32_t num_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size,
+                             int32_t num_blocks, float scale,
+                             int32_t max_context_len, int32_t partition_size,
+                             void* stream);
+
 /* Read and clear the device error word that kernels set instead of
  * trapping (a bounded wait that gave up, an index a kernel refused).
  * Synchronises `stream`. *code = 0 when no error was recorded; returns

@@ -55,6 +55,9 @@ _SIGS = {
     "pa_decode": ([_P, ctypes.c_int, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P, _P,
                    _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                    ctypes.c_float, _I32, _I32, _P, _SZ, _P], ctypes.c_int),
+    "pa_decode_no_alloc": ([_P, ctypes.c_int, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P,
+                            _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                            _I32, ctypes.c_float, _I32, _I32, _P], ctypes.c_int),
     "pa_device_error": ([_P, _P], ctypes.c_int),
 }
 
@@ -225,6 +228,27 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len
                            k_cache.shape[1], q.shape[2], k_cache.shape[2], nb, float(scale),
                            int(max_context_len), int(partition_size), _ptr(workspace), ws_bytes,
                            _stream(stream)))
+
+
+NO_ALLOC_WORKSPACE_BYTES = 16 << 20
+
+
+def decode_no_alloc(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+                    scale: float, query_start_loc=None, max_q_len: int = 1, num_blocks=None,
+                    k_scale=None, v_scale=None, k_zp=None, v_zp=None, partition_size: int = 0,
+                    stream=None) -> None:
+    """pa_decode_no_alloc: decode with the library's built-in split-KV scratch
+    (for callers that cannot allocate device memory); same arguments as
+    decode() minus the workspace."""
+    num_seqs = int(context_lens.shape[0])
+    nb = k_cache.shape[0] if num_blocks is None else num_blocks
+    _check(lib().pa_decode_no_alloc(
+        _ptr(out), _dtype_code(out), _ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache),
+        _dtype_code(k_cache), _ptr(k_scale), _ptr(v_scale), _ptr(k_zp), _ptr(v_zp),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), _ptr(query_start_loc),
+        num_seqs, int(q.shape[0]), max_q_len if query_start_loc is not None else 1, q.shape[1],
+        k_cache.shape[1], q.shape[2], k_cache.shape[2], nb, float(scale), int(max_context_len),
+        int(partition_size), _stream(stream)))
 
 
 def device_error(stream=None) -> int:

@@ -1,0 +1,72 @@
+"""pa_decode_no_alloc against pa_decode (needs a GB300).
+
+pa_decode_no_alloc serves callers that cannot allocate device memory (for
+instance code running inside a host application whose own allocator owns
+all device memory, or a decode loop that must not call cudaMalloc/cudaFree
+because they can synchronise the device): it keeps the split-KV scratch in
+a built-in 16 MiB device array instead of a caller-provided workspace.
+These tests call it through the C ABI twice in a row, on inputs that need
+the split-KV scratch, and compare each output with pa_decode's (given a
+workspace of its own) within the attention tolerance of the other GPU
+tests. The file is named to be collected last."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+import paged_kv_cache_154_gb300 as pa
+from paged_kv_cache_154_gb300.engine import PagedKVCache
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def state():
+    from paged_kv_cache_154_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    wl = W.simple("no_alloc", 4242, [600, 1500, 40, 1030], [1, 2, 1, 3], 32, 8, 128, "bf16")
+    cache = PagedKVCache(wl.num_blocks, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
+                         free_order=wl.free_order)
+    names = {}
+    for ops in wl.phases:
+        cache.run_phase(ops, names)
+    si = cache.prepare_step(wl.step, names, wl.q, torch.float32, 512)
+    cache.step(si, wl.scale, 512)              # appends the step's tokens, then attends
+    torch.cuda.synchronize()
+    assert si.workspace is not None            # these inputs need split-KV scratch
+    return wl, cache, si
+
+
+def _pair(wl, cache, si, q):
+    ref = torch.empty_like(si.out)
+    got = torch.full_like(si.out, float("nan"))
+    args = (cache.k, cache.v, si.block_tables, si.context_lens, si.max_context_len, wl.scale,
+            si.query_start_loc, si.max_q_len, cache.num_blocks)
+    pa.decode(ref, q, *args, partition_size=512, workspace=si.workspace)
+    pa.decode_no_alloc(got, q, *args, partition_size=512)
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+    return ref, got
+
+
+def test_no_alloc_matches_decode_on_two_calls_in_a_row(state):
+    wl, cache, si = state
+    q2 = (si.q.float() * -0.5).to(si.q.dtype)          # a different query for the second call
+    for q in (si.q, q2):
+        ref, got = _pair(wl, cache, si, q)
+        assert torch.isfinite(got).all()
+        err = (got.double() - ref.double()).abs().max().item()
+        assert err <= TOL, err
+
+
+def test_no_alloc_rejects_workspace_beyond_its_maximum(state):
+    wl, cache, si = state
+    big = pa.decode_workspace_size(64, 64, 128, 1 << 17, 16)
+    assert big > pa.NO_ALLOC_WORKSPACE_BYTES
+    with pytest.raises(pa.PAError) as e:
+        pa.decode_no_alloc(si.out, si.q, cache.k, cache.v, si.block_tables, si.context_lens,
+                           1 << 17, wl.scale, si.query_start_loc, si.max_q_len,
+                           cache.num_blocks, partition_size=16)
+    assert e.value.status == 2 and "16777216" in str(e.value)
