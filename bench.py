@@ -163,12 +163,11 @@ def build_state(wl, device, partition_size):
 
 
 def launches_per_step(si, partition_size):
-    P = partition_size or 512
     n = 1 + 1                                           # append, decode
     if si.pairs is not None:
         n += 1                                          # copy_blocks
-    if si.max_context_len > P:
-        n += 1                                          # split-KV reduce
+    if partition_size == 0 or si.max_context_len > partition_size:
+        n += 1                                          # partial-result reduce
     return n
 
 
@@ -264,12 +263,15 @@ def run_ours(args, rank, world, local):
         "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads,
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "block_size": 16, "context_tokens": sum(wl.context_lens),
-                   "partition_size": args.partition_size or 512,
+                   "schedule": ("balanced" if args.partition_size == 0
+                                else f"partitions of {args.partition_size}"),
                    "l2": "flushed between steps (2x L2 write), each step timed alone",
                    "bytes_per_step": nbytes, "parallelism": f"replicas x{world}"},
         "seq_steps_per_s": round(seq_steps, 1),
         "pct_of_hbm_peak": round(100 * value / peak, 2),
-        "roofline": {"kernel": "pa_decode (paged_decode_kernel + split_kv_reduce_kernel)",
+        "roofline": {"kernel": ("pa_decode (paged_decode_balanced_kernel + segment_reduce_kernel)"
+                                if args.partition_size == 0 else
+                                "pa_decode (paged_decode_kernel + split_kv_reduce_kernel)"),
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),

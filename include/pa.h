@@ -168,11 +168,16 @@ pa_status pa_append_kv(const void* key, const void* value, pa_dtype src_dtype,
                        int32_t num_kv_heads, int32_t head_dim,
                        int32_t block_size, void* stream);
 
-/* Bytes of workspace pa_decode needs (0 when every sequence fits one
- * partition). partition_size 0 selects the default (512). */
-size_t pa_decode_workspace_size(int32_t num_q_tokens, int32_t num_heads,
-                                int32_t head_dim, int32_t max_context_len,
-                                int32_t partition_size);
+/* Bytes of workspace pa_decode needs for these sizes (0 if none). With
+ * partition_size 0 (the balanced schedule) this is 2 x min(2048,
+ * num_seqs x num_kv_heads x ceil(max_context_len/16)) partial slots of
+ * 16 + 4 x R x (head_dim + 2) bytes (rounded up to 16), R = (num_heads /
+ * num_kv_heads) x max_q_len; with partition_size > 0 see pa_decode. Returns
+ * 0 for invalid sizes. Host-only: needs no GPU. */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_tokens,
+                                int32_t num_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t max_q_len,
+                                int32_t max_context_len, int32_t partition_size);
 
 /* Decode attention ([p3] §二 softmax(Q K^T / sqrt(d)) V over the cached
  * keys; [p4] decode workflow: score the new token's q against every cached
@@ -191,20 +196,31 @@ size_t pa_decode_workspace_size(int32_t num_q_tokens, int32_t num_heads,
  *   max_q_len      the largest r (1 when query_start_loc is NULL)
  *   max_context_len the largest context length (host value)
  *   scale          softmax scale, usually 1/sqrt(head_dim)
- *   partition_size split-KV partition in tokens (multiple of 16; 0 = 512).
- *                  Sequences longer than one partition are split; each
- *                  partition's (o, m, l) goes to the workspace and a
- *                  log-sum-exp reduce writes `out`.
+ *   partition_size 0 (default) selects the balanced schedule: a persistent
+ *                  grid in which every warp streams an equal contiguous share
+ *                  of all (sequence, KV head, block) work; a share that
+ *                  covers a (sequence, KV head) whole writes its output, and
+ *                  where share boundaries cut one, the pieces' partials
+ *                  (m, l, O) are merged by a log-sum-exp reduce. A multiple
+ *                  of 16 up to 4096 selects fixed split-KV partitions of that
+ *                  many tokens (one CTA per partition, KV head and sequence).
  *   workspace      device memory of pa_decode_workspace_size() bytes,
- *                  256-byte aligned (NULL allowed if that size is 0). Layout,
- *                  with P = ceil(max_context_len / partition_size):
+ *                  256-byte aligned (NULL allowed if that size is 0); its
+ *                  contents need no initialisation. Layout with
+ *                  partition_size > 0 and P = ceil(max_context_len /
+ *                  partition_size):
  *                    o_part fp32 [num_q_tokens][num_heads][P][head_dim]
+ *                           (each partition's normalised output)
  *                    m_part fp32 [num_q_tokens][num_heads][P] (base-2 log
  *                           domain: max of logit * log2(e))
  *                    l_part fp32 [num_q_tokens][num_heads][P]
- *                  each region starting on a 256-byte boundary.
+ *                  each region starting on a 256-byte boundary. With
+ *                  partition_size 0: partial slots, each int32 {sequence,
+ *                  kv head, first token, end token} then fp32 m[R], l[R]
+ *                  (base-2 units) and O[R][head_dim] (not normalised).
  * Requirements: head_dim 64 or 128, block_size 16, num_heads a multiple of
- * num_kv_heads, context_lens[s] >= (query run length of s) >= 1. */
+ * num_kv_heads, context_lens[s] >= (query run length of s) >= 1, at most
+ * 8192 sequences per call with partition_size 0. */
 pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
                     pa_dtype q_dtype, const void* k_cache, const void* v_cache,
                     pa_dtype kv_dtype, const float* k_scale,

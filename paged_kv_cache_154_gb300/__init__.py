@@ -51,7 +51,7 @@ _SIGS = {
                         ctypes.c_int, _P], ctypes.c_int),
     "pa_append_kv": ([_P, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P,
                       _I32, _I32, _I32, _I32, _I32, _P], ctypes.c_int),
-    "pa_decode_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
+    "pa_decode_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "pa_decode": ([_P, ctypes.c_int, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P, _P,
                    _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                    ctypes.c_float, _I32, _I32, _P, _SZ, _P], ctypes.c_int),
@@ -205,10 +205,12 @@ def append_kv(key, value, k_cache, v_cache, slot_mapping, num_blocks: Optional[i
                               _stream(stream)))
 
 
-def decode_workspace_size(num_q_tokens: int, num_heads: int, head_dim: int,
-                          max_context_len: int, partition_size: int = 0) -> int:
-    return int(lib().pa_decode_workspace_size(num_q_tokens, num_heads, head_dim,
-                                              max_context_len, partition_size))
+def decode_workspace_size(num_seqs: int, num_q_tokens: int, num_heads: int, num_kv_heads: int,
+                          head_dim: int, max_q_len: int, max_context_len: int,
+                          partition_size: int = 0) -> int:
+    return int(lib().pa_decode_workspace_size(num_seqs, num_q_tokens, num_heads, num_kv_heads,
+                                              head_dim, max_q_len, max_context_len,
+                                              partition_size))
 
 
 def decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,

@@ -181,21 +181,24 @@ extern "C" pa_status pa_append_kv(const void* key, const void* value, pa_dtype s
 
 namespace {
 
-int32_t effective_partition(int32_t partition_size) {
-    return partition_size > 0 ? partition_size : 512;
-}
-
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
-extern "C" size_t pa_decode_workspace_size(int32_t num_q_tokens, int32_t num_heads,
-                                           int32_t head_dim, int32_t max_context_len,
-                                           int32_t partition_size) {
-    const int32_t P = effective_partition(partition_size);
-    if (num_q_tokens <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len <= 0 || P <= 0)
+extern "C" size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_tokens,
+                                           int32_t num_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, int32_t max_q_len,
+                                           int32_t max_context_len, int32_t partition_size) {
+    if (num_seqs <= 0 || num_q_tokens <= 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || max_q_len <= 0 || max_context_len <= 0 || partition_size < 0 ||
+        num_heads % num_kv_heads != 0)
         return 0;
-    const int64_t parts = (max_context_len + (int64_t)P - 1) / P;
+    if (partition_size == 0) {
+        const int64_t workers = pa::balanced_worker_cap(num_seqs, num_kv_heads, max_context_len);
+        return (size_t)(2 * workers *
+                        pa::balanced_slot_bytes(num_heads, num_kv_heads, head_dim, max_q_len));
+    }
+    const int64_t parts = (max_context_len + (int64_t)partition_size - 1) / partition_size;
     if (parts <= 1) return 0;
     const size_t rows = (size_t)num_q_tokens * num_heads * parts;
     return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float));
@@ -243,17 +246,18 @@ extern "C" pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_
     if ((int64_t)max_blocks_per_seq * block_size < max_context_len)
         return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq %d cannot hold %d tokens",
                     max_blocks_per_seq, max_context_len);
-    const int32_t P = effective_partition(partition_size);
-    if (P % block_size != 0)
+    const int32_t P = partition_size;
+    if (P < 0 || P % block_size != 0)
         return fail(PA_ERR_INVALID_ARG, "partition_size %d is not a multiple of %d", P, block_size);
-    const int64_t parts = (max_context_len + (int64_t)P - 1) / P;
+    const int64_t parts = P > 0 ? (max_context_len + (int64_t)P - 1) / P : 1;
     if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "too many partitions (%lld)", (long long)parts);
     if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16)
         return fail(PA_ERR_INVALID_ARG, "k_cache and v_cache must be 16-byte aligned");
     if (((uintptr_t)q | (uintptr_t)out) % 16)
         return fail(PA_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
-    const size_t need = pa_decode_workspace_size(num_q_tokens, num_heads, head_dim,
-                                                 max_context_len, partition_size);
+    const size_t need = pa_decode_workspace_size(num_seqs, num_q_tokens, num_heads, num_kv_heads,
+                                                 head_dim, max_q_len, max_context_len,
+                                                 partition_size);
     if (need > 0 && (!workspace || workspace_bytes < need || (uintptr_t)workspace % 256))
         return fail(PA_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
                     need, workspace_bytes);
@@ -308,7 +312,9 @@ extern "C" pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_
     a.max_context_len = max_context_len;
     a.partition_size = P;
     a.num_partitions = (int32_t)parts;
-    if (parts > 1) {
+    if (P == 0) {
+        a.slots = workspace;
+    } else if (parts > 1) {
         const size_t rows = (size_t)num_q_tokens * num_heads * parts;
         char* w = static_cast<char*>(workspace);
         a.o_part = reinterpret_cast<float*>(w);

@@ -45,13 +45,13 @@ extern "C" pa_status pa_decode_no_alloc(
     int32_t num_seqs, int32_t num_q_tokens, int32_t max_q_len, int32_t num_heads,
     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
     float scale, int32_t max_context_len, int32_t partition_size, void* stream) {
-    const size_t need = pa_decode_workspace_size(num_q_tokens, num_heads, head_dim,
-                                                 max_context_len, partition_size);
+    const size_t need = pa_decode_workspace_size(num_seqs, num_q_tokens, num_heads, num_kv_heads,
+                                                 head_dim, max_q_len, max_context_len,
+                                                 partition_size);
     if (need > kStaticWorkspaceBytes)
         return pa::fail(PA_ERR_UNSUPPORTED,
                         "pa_decode_no_alloc: this call needs %zu bytes of split-KV workspace, "
-                        "more than the built-in %zu; use pa_decode with caller memory, or a "
-                        "larger partition_size",
+                        "more than the built-in %zu; use pa_decode with caller memory",
                         need, kStaticWorkspaceBytes);
     void* ws = nullptr;
     if (need > 0)

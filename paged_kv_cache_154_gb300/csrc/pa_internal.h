@@ -97,11 +97,29 @@ struct DecodeArgs {
     int32_t max_context_len;
     int32_t partition_size;
     int32_t num_partitions;
-    float* o_part;
+    float* o_part;           // partitioned schedule (partition_size > 0)
     float* m_part;
     float* l_part;
+    void* slots;             // balanced schedule (partition_size == 0)
     cudaStream_t stream;
 };
 pa_status launch_decode(const DecodeArgs& a);
+
+// Balanced schedule: at most this many worker warps (and partial-slot pairs),
+// and at most this many sequences per call (their prefix sums live in shared
+// memory).
+constexpr int kBalancedMaxWorkers = 2048;
+constexpr int kBalancedMaxSeqs = 8192;
+
+inline int64_t balanced_worker_cap(int num_seqs, int num_kv_heads, int max_context_len) {
+    const int64_t blocks = (int64_t)num_seqs * num_kv_heads * ((max_context_len + 15) / 16);
+    return blocks < kBalancedMaxWorkers ? blocks : kBalancedMaxWorkers;
+}
+
+// One partial slot: 16-byte header, then m, l and O of every query row of a KV head.
+inline int64_t balanced_slot_bytes(int num_heads, int num_kv_heads, int head_dim, int max_q_len) {
+    const int64_t rows = (int64_t)(num_heads / num_kv_heads) * max_q_len;
+    return (16 + 4 * rows * (head_dim + 2) + 15) / 16 * 16;
+}
 
 }  // namespace pa

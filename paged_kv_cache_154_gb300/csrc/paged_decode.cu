@@ -1,4 +1,4 @@
-// Paged decode attention for F16/BF16 caches, and the split-KV reduce.
+// Paged decode attention for F16/BF16 caches, and its partial-result merges.
 //
 // What it computes: "KV Cache ... PagedAttention" (devpress.csdn.net) §二,
 // softmax(Q K^T / sqrt(d)) V, over the keys a sequence holds in its blocks
@@ -7,23 +7,25 @@
 // weighted sum of the cached V; GQA/MQA from the same lecture: the q heads
 // of one group share one KV head, so one KV read serves the whole group.
 //
-// How (this library's design for sm_103a):
-//   * grid = (partition, kv head, sequence). A CTA owns one partition of one
-//     sequence's keys for one KV head and every query row that reads that KV
-//     head: G q heads x r query tokens (r > 1 for speculative verify runs).
-//   * One producer warp streams the partition's 16-token K and V tiles into
-//     a ring of shared-memory stages with 2-D bulk tensor copies (TMA,
-//     128-byte swizzle), one mbarrier per stage and direction.
-//   * Four consumer warps take the stages round-robin. Per 16-token block a
-//     warp computes S = Q K^T with m16n8k16 tensor-core MMAs (query rows in
-//     M, padded to 16; fp32 accumulate), applies the causal/length mask,
-//     updates an fp32 online softmax (running max and sum, base-2
-//     exponentials) and accumulates O += P V, P split as P_hi + P_lo in the
-//     16-bit type so the product keeps ~16 mantissa bits.
-//   * The four warps' (m, l, O) are merged through shared memory; a CTA
-//     whose sequence fits one partition writes the normalised output, the
-//     others write (o, m, l) partials that split_kv_reduce merges with the
-//     log-sum-exp rule.
+// Per 16-token block a warp computes S = Q K^T with m16n8k16 tensor-core
+// MMAs (the query rows of one KV head -- G q heads x r query tokens -- in M,
+// padded to 16; fp32 accumulate), applies the causal/length mask, updates an
+// fp32 online softmax (running max and sum, base-2 exponentials) and
+// accumulates O += P V with P split as P_hi + P_lo in the 16-bit type, so the
+// weights keep ~16 mantissa bits. K and V tiles reach shared memory by 2-D
+// bulk tensor copies (TMA, 128-byte swizzle) completing on mbarriers.
+//
+// Two schedules share that block step:
+//   * balanced (default, partition_size == 0): a persistent grid of warps,
+//     each an independent worker with its own TMA ring. The (sequence, kv
+//     head, block) space is cut into equal contiguous shares, one per warp,
+//     so every warp streams the same number of blocks. A (sequence, kv head)
+//     segment that a warp covers whole is written as final output; where a
+//     share boundary cuts a segment, each side writes a partial (m, l, O)
+//     and segment_reduce_kernel merges them with the log-sum-exp rule.
+//   * partitioned (partition_size > 0): grid (partition, kv head, sequence),
+//     one producer warp + four consumer warps per CTA, partitions merged by
+//     split_kv_reduce_kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -32,6 +34,7 @@
 
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pa_internal.h"
@@ -40,10 +43,665 @@
 namespace {
 
 constexpr int kBS = 16;                  // tokens per block
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 4;        // partitioned schedule
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxPartBlocks = 256;      // partition_size <= 4096 tokens
+constexpr int kWorkerWarps = 4;          // balanced schedule: warps per CTA
 constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename T>
+struct Pack;
+template <>
+struct Pack<__nv_bfloat16> {
+    static constexpr bool kBF16 = true;
+    __device__ static uint32_t pack(float lo, float hi, float& rlo, float& rhi) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        rlo = lo - __low2float(v);
+        rhi = hi - __high2float(v);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __device__ static uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __device__ static void store(void* p, float x) {
+        *static_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
+    }
+    __device__ static void store2(void* p, float a, float b) {
+        *static_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+    }
+};
+template <>
+struct Pack<__half> {
+    static constexpr bool kBF16 = false;
+    __device__ static uint32_t pack(float lo, float hi, float& rlo, float& rhi) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        rlo = lo - __low2float(v);
+        rhi = hi - __high2float(v);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __device__ static uint32_t pack(float lo, float hi) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __device__ static void store(void* p, float x) { *static_cast<__half*>(p) = __float2half_rn(x); }
+    __device__ static void store2(void* p, float a, float b) {
+        *static_cast<__half2*>(p) = __floats2half2_rn(a, b);
+    }
+};
+
+// Byte offset of the 16-byte chunk `chunk` of row `row` in a K/V tile laid
+// out by the 128B-swizzled TMA box [16 rows][64 columns] per sub-tile.
+__device__ __forceinline__ uint32_t tile_offset(int row, int chunk) {
+    const int sub = chunk >> 3, c = chunk & 7;
+    return sub * (kBS * 128) + row * 128 + ((c ^ (row & 7)) << 4);
+}
+
+// Issue the K and V copies of one (block, kv head) tile into a stage.
+template <int D>
+__device__ __forceinline__ void issue_tile(uint32_t stage, uint32_t bar, const CUtensorMap* mk,
+                                           const CUtensorMap* mv, int row, uint64_t pol) {
+    constexpr int kTile = kBS * D * 2;
+    pa::mbar_arrive_expect_tx(bar, 2 * kTile);
+#pragma unroll
+    for (int sub = 0; sub < D / 64; ++sub) {
+        pa::tma_load_2d(stage + sub * kBS * 128, mk, sub * 64, row, bar, pol);
+        pa::tma_load_2d(stage + kTile + sub * kBS * 128, mv, sub * 64, row, bar, pol);
+    }
+}
+
+// One warp's attention state over some blocks of one (sequence, kv head):
+// MT m-tiles of 16 query rows, fp32 O accumulators, running max and sum
+// (per thread: its two rows of each m-tile; l is a per-thread partial sum
+// until quad_sum()).
+template <typename T, int D, int MT>
+struct WarpAttn {
+    static constexpr int kKSteps = D / 16;
+    static constexpr int kNTiles = D / 8;
+    float o[MT][kNTiles][4];
+    float m_run[MT][2];
+    float l_run[MT][2];
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int nt = 0; nt < kNTiles; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+            m_run[mt][0] = m_run[mt][1] = -INFINITY;
+            l_run[mt][0] = l_run[mt][1] = 0.f;
+        }
+    }
+
+    // One 16-token block staged at kb (K tile) and kb + tile (V tile).
+    //   qreg   A fragments of Q (MT == 1), or qsm: smem Q tile base (MT > 1)
+    //   tok0   absolute position of the block's first token
+    //   last_q L - r: query row i sees keys <= L - r + i (row i = row / G)
+    template <int QPITCH>
+    __device__ __forceinline__ void block(uint32_t kb, const uint32_t (*qreg)[4], uint32_t qsm,
+                                          int tok0, int last_q, int L, int G, float scale_log2,
+                                          int lane) {
+        using PK = Pack<T>;
+        constexpr int kTile = kBS * D * 2;
+        const uint32_t vb = kb + kTile;
+        const int quad = lane >> 2, qc = lane & 3;
+        const int mat = lane >> 3, mrow = lane & 7;
+        const int k_tok = (mat >> 1) * 8 + mrow, k_chk = mat & 1;
+        const int v_tok = (mat & 1) * 8 + mrow, v_chk = mat >> 1;
+
+        float sacc[MT][2][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < kKSteps; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            pa::ldmatrix_x4(kb + tile_offset(k_tok, 2 * ks + k_chk), b0, b1, b2, b3);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                uint32_t a[4];
+                if constexpr (MT == 1) {
+                    a[0] = qreg[ks][0];
+                    a[1] = qreg[ks][1];
+                    a[2] = qreg[ks][2];
+                    a[3] = qreg[ks][3];
+                } else {
+                    const int arow = mt * 16 + (mat & 1) * 8 + mrow;
+                    const int achk = 2 * ks + (mat >> 1);
+                    pa::ldmatrix_x4(qsm + arow * QPITCH + achk * 16, a[0], a[1], a[2], a[3]);
+                }
+                pa::mma_16816<PK::kBF16>(sacc[mt][0], a, b0, b1);
+                pa::mma_16816<PK::kBF16>(sacc[mt][1], a, b2, b3);
+            }
+        }
+
+        const bool need_mask = tok0 + kBS - 1 > last_q;   // block reaches past some row's bound
+        uint32_t phi[MT][4], plo[MT][4];
+        float alpha[MT][2];
+        bool rescale = false;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = mt * 16 + quad + 8 * h;
+                const int bound = min(last_q + row / G, L - 1);
+                float mx = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        float v = sacc[mt][nt][2 * h + e] * scale_log2;
+                        if (need_mask && tok0 + nt * 8 + 2 * qc + e > bound) v = -INFINITY;
+                        sacc[mt][nt][2 * h + e] = v;
+                        mx = fmaxf(mx, v);
+                    }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float m_new = fmaxf(m_run[mt][h], mx);
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                alpha[mt][h] = exp2f(m_run[mt][h] - m_use);
+                m_run[mt][h] = m_new;
+                float sum = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float pv = exp2f(sacc[mt][nt][2 * h + e] - m_use);
+                        sacc[mt][nt][2 * h + e] = pv;
+                        sum += pv;
+                    }
+                l_run[mt][h] = l_run[mt][h] * alpha[mt][h] + sum;
+                rescale |= alpha[mt][h] != 1.f;
+            }
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < kNTiles; ++nt) {
+                    o[mt][nt][0] *= alpha[mt][0];
+                    o[mt][nt][1] *= alpha[mt][0];
+                    o[mt][nt][2] *= alpha[mt][1];
+                    o[mt][nt][3] *= alpha[mt][1];
+                }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            // A fragment of P (16 rows x 16 tokens) straight from the S accumulators
+            float r0, r1, r2, r3, r4, r5, r6, r7;
+            phi[mt][0] = PK::pack(sacc[mt][0][0], sacc[mt][0][1], r0, r1);
+            phi[mt][1] = PK::pack(sacc[mt][0][2], sacc[mt][0][3], r2, r3);
+            phi[mt][2] = PK::pack(sacc[mt][1][0], sacc[mt][1][1], r4, r5);
+            phi[mt][3] = PK::pack(sacc[mt][1][2], sacc[mt][1][3], r6, r7);
+            plo[mt][0] = PK::pack(r0, r1);
+            plo[mt][1] = PK::pack(r2, r3);
+            plo[mt][2] = PK::pack(r4, r5);
+            plo[mt][3] = PK::pack(r6, r7);
+        }
+
+        const int valid = L - tok0;   // tokens of this block inside the context (>= 1)
+#pragma unroll
+        for (int nd = 0; nd < D / 16; ++nd) {
+            uint32_t v0, v1, v2, v3;
+            pa::ldmatrix_x4_trans(vb + tile_offset(v_tok, 2 * nd + v_chk), v0, v1, v2, v3);
+            if (valid < kBS) {
+                // slots past the context may hold anything (even NaN patterns): zero them
+                const int t_lo = 2 * qc, t_hi = 2 * qc + 8;
+                auto keep = [&](uint32_t x, int t) -> uint32_t {
+                    const uint32_t lo = (t < valid) ? (x & 0xffffu) : 0u;
+                    const uint32_t hi = (t + 1 < valid) ? (x & 0xffff0000u) : 0u;
+                    return lo | hi;
+                };
+                v0 = keep(v0, t_lo);
+                v2 = keep(v2, t_lo);
+                v1 = keep(v1, t_hi);
+                v3 = keep(v3, t_hi);
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                pa::mma_16816<PK::kBF16>(o[mt][2 * nd], phi[mt], v0, v1);
+                pa::mma_16816<PK::kBF16>(o[mt][2 * nd], plo[mt], v0, v1);
+                pa::mma_16816<PK::kBF16>(o[mt][2 * nd + 1], phi[mt], v2, v3);
+                pa::mma_16816<PK::kBF16>(o[mt][2 * nd + 1], plo[mt], v2, v3);
+            }
+        }
+    }
+
+    __device__ __forceinline__ void quad_sum() {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                l_run[mt][h] += __shfl_xor_sync(0xffffffffu, l_run[mt][h], 1);
+                l_run[mt][h] += __shfl_xor_sync(0xffffffffu, l_run[mt][h], 2);
+            }
+    }
+};
+
+// Q fragments of one m-tile in registers (MT == 1): rows quad and quad + 8.
+template <typename T, int D>
+__device__ __forceinline__ void load_q_regs(uint32_t (*qreg)[4], const void* q, int q0, int G,
+                                            int R, int g, int num_heads, int lane) {
+    const int quad = lane >> 2, qc = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int row = quad + 8 * h;
+        const T* src = row < R ? static_cast<const T*>(q) +
+                                     ((int64_t)(q0 + row / G) * num_heads + g * G + row % G) * D
+                               : nullptr;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t lo = 0, hi = 0;
+            if (src) {
+                lo = __ldg(reinterpret_cast<const uint32_t*>(src + ks * 16 + 2 * qc));
+                hi = __ldg(reinterpret_cast<const uint32_t*>(src + ks * 16 + 8 + 2 * qc));
+            }
+            qreg[ks][h] = lo;
+            qreg[ks][2 + h] = hi;
+        }
+    }
+}
+
+// ===========================================================================
+// balanced schedule
+// ===========================================================================
+
+struct BalancedParams {
+    void* out;
+    const void* q;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* qsl;
+    uint8_t* slots;          // partial slots [2 * workers][slot_bytes]
+    unsigned int* err;
+    int max_blocks;
+    int num_heads;
+    int num_kv_heads;
+    int group;
+    int num_seqs;
+    int num_blocks;
+    int workers;
+    int slot_rows;           // rows a slot holds (q heads per kv head x max_q_len)
+    int slot_bytes;
+    float scale_log2;
+    int out_f32;
+};
+
+// A partial slot: int32 {seq, kv head, first token, end token}, then fp32
+// m[slot_rows] (base-2 units), l[slot_rows], O[slot_rows][D] (unnormalised).
+struct SlotView {
+    int32_t* hdr;
+    float* m;
+    float* l;
+    float* o;
+    __device__ SlotView(uint8_t* base, int rows) {
+        hdr = reinterpret_cast<int32_t*>(base);
+        m = reinterpret_cast<float*>(base + 16);
+        l = m + rows;
+        o = l + rows;
+    }
+};
+
+// Shared-memory layout of the balanced kernel:
+//   [barriers: kWorkerWarps x S x 8][cum: num_seqs + 1 int32] -> rounded to 1024
+//   [ring of warp 0: S stages][ring of warp 1] ...   (each stage K tile + V tile)
+//   [Q tiles of the warps, MT > 1 only]
+template <int D, int MT, int S>
+struct BalancedLayout {
+    static constexpr int kStage = 2 * kBS * D * 2;
+    static constexpr int kRing = S * kStage;
+    static constexpr int kQPitch = D * 2 + 16;
+    static constexpr int kQTile = MT > 1 ? 16 * MT * kQPitch : 0;
+    __host__ __device__ static int header_bytes(int num_seqs) {
+        return ((kWorkerWarps * S * 8 + (num_seqs + 1) * 4) + 1023) / 1024 * 1024;
+    }
+    __host__ __device__ static int smem_bytes(int num_seqs) {
+        return header_bytes(num_seqs) + kWorkerWarps * (kRing + kQTile) + 1024;
+    }
+};
+
+// Largest s with cum[s] <= f (cum non-decreasing, cum[0] = 0, f < cum[n]).
+__device__ __forceinline__ int find_seq(const int32_t* cum, int n, int64_t f) {
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid] <= f) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__host__ __device__ __forceinline__ int64_t share_start(int64_t w, int64_t B, int64_t W) {
+    return w * B / W;
+}
+
+// cum[s] = num_kv_heads * sum_{s' < s} ceil(L_s' / 16), computed by one CTA.
+__device__ void block_prefix(int32_t* cum, const int32_t* lens, int n, int hkv) {
+    __shared__ int32_t warp_tot[32];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (n + nt - 1) / nt;
+    const int a = min(n, tid * per), b = min(n, a + per);
+    int32_t local = 0;
+    for (int i = a; i < b; ++i) local += hkv * ((__ldg(lens + i) + kBS - 1) / kBS);
+    // inclusive scan of `local` over the CTA
+    const int lane = tid & 31, warp = tid >> 5;
+    int32_t x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = nt >> 5;
+        int32_t t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    int32_t run = x - local + (warp > 0 ? warp_tot[warp - 1] : 0);   // exclusive prefix
+    for (int i = a; i < b; ++i) {
+        cum[i] = run;
+        run += hkv * ((__ldg(lens + i) + kBS - 1) / kBS);
+    }
+    if (tid == nt - 1) cum[n] = run;
+    __syncthreads();
+}
+
+template <typename T, int D, int MT, int S>
+__global__ void __launch_bounds__(kWorkerWarps * 32)
+    paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                 const __grid_constant__ CUtensorMap tmap_v,
+                                 const BalancedParams p) {
+    using Lay = BalancedLayout<D, MT, S>;
+    using PK = Pack<T>;
+    constexpr int kKSteps = D / 16;
+    constexpr int kNTiles = D / 8;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = pa::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const smem = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hkv = p.num_kv_heads, G = p.group;
+    int32_t* const cum = reinterpret_cast<int32_t*>(smem + kWorkerWarps * S * 8);
+    const uint32_t bars = base + warp * S * 8;
+    const uint32_t ring = base + Lay::header_bytes(p.num_seqs) + warp * Lay::kRing;
+    const uint32_t qtile = base + Lay::header_bytes(p.num_seqs) + kWorkerWarps * Lay::kRing +
+                           warp * Lay::kQTile;
+
+    block_prefix(cum, p.context_lens, p.num_seqs, hkv);
+    const int64_t B = cum[p.num_seqs];
+    const int64_t wid = (int64_t)blockIdx.x * kWorkerWarps + warp;
+    const int64_t f0 = share_start(wid, B, p.workers);
+    const int64_t f1 = share_start(wid + 1, B, p.workers);
+    const int n = (int)(f1 - f0);
+    if (n <= 0) return;
+
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i) pa::mbar_init(bars + 8 * i, 1);
+        pa::fence_barrier_init();
+    }
+    __syncwarp();
+
+    // Producer side (all lanes run it; lane 0 issues): each lane keeps the TMA
+    // row of block (win + lane) of this share.
+    uint64_t pol = 0;
+    if (lane == 0) {
+        pa::prefetch_tensormap(&tmap_k);
+        pa::prefetch_tensormap(&tmap_v);
+        pol = pa::policy_evict_first();
+    }
+    int win = -32, my_row = 0;
+    auto refresh = [&](int wbase) {
+        win = wbase;
+        const int64_t f = f0 + wbase + lane;
+        my_row = 0;
+        if (f < f1) {
+            const int s = find_seq(cum, p.num_seqs, f);
+            const int nbs = (cum[s + 1] - cum[s]) / hkv;
+            const int local = (int)(f - cum[s]);
+            const int g = local / nbs, b = local - (local / nbs) * nbs;
+            int blk = __ldg(p.block_tables + (int64_t)s * p.max_blocks + b);
+            if (blk < 0 || blk >= p.num_blocks) {
+                if (p.err) atomicOr(p.err, pa::ERR_BAD_BLOCK);
+                blk = 0;
+            }
+            my_row = (blk * hkv + g) * kBS;
+        }
+    };
+    auto issue = [&](int k) {   // warp-uniform
+        if (k >= win + 32) refresh(k & ~31);
+        const int row = __shfl_sync(0xffffffffu, my_row, k - win);
+        if (lane == 0)
+            issue_tile<D>(ring + (k % S) * Lay::kStage, bars + 8 * (k % S), &tmap_k, &tmap_v,
+                          row, pol);
+    };
+    int issued = 0;
+    for (; issued < S && issued < n; ++issued) issue(issued);
+
+    // Consumer side: walk the share block by block, segment by segment.
+    int cs = find_seq(cum, p.num_seqs, f0);
+    int cnbs = (cum[cs + 1] - cum[cs]) / hkv;
+    int cg, cb;
+    {
+        const int local = (int)(f0 - cum[cs]);
+        cg = local / cnbs;
+        cb = local - cg * cnbs;
+    }
+    WarpAttn<T, D, MT> st;
+    uint32_t qreg[MT == 1 ? kKSteps : 1][4];
+    int L = 0, r = 1, q0 = 0, R = 0, seg_b0 = cb;
+    bool seg_first = true;
+    auto start_segment = [&]() {
+        L = __ldg(p.context_lens + cs);
+        if (p.qsl) {
+            q0 = __ldg(p.qsl + cs);
+            r = __ldg(p.qsl + cs + 1) - q0;
+        } else {
+            q0 = cs;
+            r = 1;
+        }
+        R = G * r;
+        if constexpr (MT == 1) {
+            load_q_regs<T, D>(qreg, p.q, q0, G, R, cg, p.num_heads, lane);
+        } else {
+            __syncwarp();
+            for (int e = lane; e < 16 * MT * (D / 8); e += 32) {
+                const int row = e / (D / 8), ch = e - row * (D / 8);
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (row < R) {
+                    const T* src = static_cast<const T*>(p.q) +
+                                   ((int64_t)(q0 + row / G) * p.num_heads + cg * G + row % G) * D;
+                    v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+                }
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                                 qtile + row * Lay::kQPitch + ch * 16),
+                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
+            __syncwarp();
+        }
+        st.reset();
+    };
+    auto finish_segment = [&](bool complete, int slot_idx, int tok_end) {
+        st.quad_sum();
+        const int quad = lane >> 2, qc = lane & 3;
+        if (complete) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = mt * 16 + quad + 8 * h;
+                    if (row >= R) continue;
+                    const float inv = 1.f / st.l_run[mt][h];
+                    const int64_t obase =
+                        ((int64_t)(q0 + row / G) * p.num_heads + cg * G + row % G) * D;
+#pragma unroll
+                    for (int nt = 0; nt < kNTiles; ++nt) {
+                        const float a = st.o[mt][nt][2 * h] * inv;
+                        const float b = st.o[mt][nt][2 * h + 1] * inv;
+                        const int64_t idx = obase + nt * 8 + 2 * qc;
+                        if (p.out_f32)
+                            *reinterpret_cast<float2*>(static_cast<float*>(p.out) + idx) =
+                                make_float2(a, b);
+                        else
+                            PK::store2(static_cast<T*>(p.out) + idx, a, b);
+                    }
+                }
+        } else {
+            SlotView sv(p.slots + (2 * wid + slot_idx) * (int64_t)p.slot_bytes, p.slot_rows);
+            if (lane == 0) {
+                sv.hdr[0] = cs;
+                sv.hdr[1] = cg;
+                sv.hdr[2] = seg_b0 * kBS;
+                sv.hdr[3] = tok_end;
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = mt * 16 + quad + 8 * h;
+                    if (row >= R || row >= p.slot_rows) continue;
+                    if (qc == 0) {
+                        sv.m[row] = st.m_run[mt][h];
+                        sv.l[row] = st.l_run[mt][h];
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < kNTiles; ++nt)
+                        *reinterpret_cast<float2*>(sv.o + (int64_t)row * D + nt * 8 + 2 * qc) =
+                            make_float2(st.o[mt][nt][2 * h], st.o[mt][nt][2 * h + 1]);
+                }
+        }
+    };
+    start_segment();
+
+    int consumed = 0;
+    for (int k = 0; k < n; ++k) {
+        if (!pa::mbar_wait(bars + 8 * (k % S), (k / S) & 1, p.err, pa::ERR_WAIT_FULL)) break;
+        consumed = k + 1;
+        st.template block<Lay::kQPitch>(ring + (k % S) * Lay::kStage, qreg, qtile, cb * kBS,
+                                        L - r, L, G, p.scale_log2, lane);
+        __syncwarp();
+        if (issued < n) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(issued);
+            ++issued;
+        }
+        ++cb;
+        const bool seg_done = cb == cnbs;
+        if (seg_done || k == n - 1) {
+            finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1, min(cb * kBS, L));
+            if (k == n - 1) break;
+            // next (sequence, kv head) segment
+            cb = 0;
+            if (++cg == hkv) {
+                cg = 0;
+                do {
+                    ++cs;
+                } while (cs < p.num_seqs - 1 && cum[cs + 1] == cum[cs]);
+                cnbs = (cum[cs + 1] - cum[cs]) / hkv;
+            }
+            seg_b0 = 0;
+            seg_first = false;
+            start_segment();
+        }
+    }
+    // drain: no copy of this warp may still be in flight when it exits
+    for (int k = consumed; k < issued; ++k)
+        if (!pa::mbar_wait(bars + 8 * (k % S), (k / S) & 1, p.err, pa::ERR_WAIT_DRAIN)) break;
+}
+
+// Merges the partials of every (sequence, kv head) segment that a share
+// boundary cut: out = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w over the
+// covering shares (M = max m_w), the log-sum-exp rule. One CTA per sequence.
+template <typename T, int D>
+__global__ void __launch_bounds__(128)
+    segment_reduce_kernel(const BalancedParams p) {
+    const int s = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int hkv = p.num_kv_heads, G = p.group;
+    __shared__ int64_t red[2][4];
+    // this sequence's first block in the flattened order, and the total
+    int64_t before = 0, total = 0;
+    for (int i = tid; i < p.num_seqs; i += blockDim.x) {
+        const int64_t nb = (int64_t)hkv * ((__ldg(p.context_lens + i) + kBS - 1) / kBS);
+        total += nb;
+        if (i < s) before += nb;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        total += __shfl_xor_sync(0xffffffffu, total, o);
+    }
+    if ((tid & 31) == 0) {
+        red[0][tid >> 5] = before;
+        red[1][tid >> 5] = total;
+    }
+    __syncthreads();
+    before = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+    total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+    const int L = __ldg(p.context_lens + s);
+    const int nbs = (L + kBS - 1) / kBS;
+    int q0, r;
+    if (p.qsl) {
+        q0 = __ldg(p.qsl + s);
+        r = __ldg(p.qsl + s + 1) - q0;
+    } else {
+        q0 = s;
+        r = 1;
+    }
+    const int R = G * r;
+    const int64_t W = p.workers;
+    for (int g = 0; g < hkv; ++g) {
+        const int64_t fa = before + (int64_t)g * nbs, fb = fa + nbs;
+        const int64_t wa = ((fa + 1) * W - 1) / total;     // share holding block fa
+        const int64_t wb = (fb * W - 1) / total;           // share holding block fb - 1
+        if (wa == wb) continue;                            // written whole by that share
+        for (int e = tid; e < R * D; e += blockDim.x) {
+            const int row = e / D, col = e - row * D;
+            float M = -INFINITY;
+            for (int64_t w = wa; w <= wb; ++w) {
+                const int64_t a0 = share_start(w, total, W);
+                if (a0 == share_start(w + 1, total, W)) continue;   // empty share
+                SlotView sv(p.slots + (2 * w + (a0 >= fa ? 0 : 1)) * (int64_t)p.slot_bytes,
+                            p.slot_rows);
+                M = fmaxf(M, sv.m[row]);
+            }
+            const float Mu = M == -INFINITY ? 0.f : M;
+            float num = 0.f, den = 0.f;
+            for (int64_t w = wa; w <= wb; ++w) {
+                const int64_t a0 = share_start(w, total, W);
+                if (a0 == share_start(w + 1, total, W)) continue;
+                SlotView sv(p.slots + (2 * w + (a0 >= fa ? 0 : 1)) * (int64_t)p.slot_bytes,
+                            p.slot_rows);
+                const float l = sv.l[row];
+                if (!(l > 0.f)) continue;
+                const float wt = exp2f(sv.m[row] - Mu);
+                num += wt * sv.o[(int64_t)row * D + col];
+                den += wt * l;
+            }
+            const float val = num / den;
+            const int64_t idx =
+                ((int64_t)(q0 + row / G) * p.num_heads + g * G + row % G) * D + col;
+            if (p.out_f32) static_cast<float*>(p.out)[idx] = val;
+            else Pack<T>::store(static_cast<T*>(p.out) + idx, val);
+        }
+    }
+}
+
+// ===========================================================================
+// partitioned schedule
+// ===========================================================================
 
 struct DecodeParams {
     void* out;
@@ -66,44 +724,8 @@ struct DecodeParams {
     int out_f32;
 };
 
-template <typename T>
-struct Pack;
-template <>
-struct Pack<__nv_bfloat16> {
-    static constexpr bool kBF16 = true;
-    __device__ static uint32_t pack(float lo, float hi, float& rlo, float& rhi) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        rlo = lo - __low2float(v);
-        rhi = hi - __high2float(v);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
-    __device__ static uint32_t pack(float lo, float hi) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
-    __device__ static void store(void* p, float x) {
-        *static_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
-    }
-};
-template <>
-struct Pack<__half> {
-    static constexpr bool kBF16 = false;
-    __device__ static uint32_t pack(float lo, float hi, float& rlo, float& rhi) {
-        __half2 v = __floats2half2_rn(lo, hi);
-        rlo = lo - __low2float(v);
-        rhi = hi - __high2float(v);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
-    __device__ static uint32_t pack(float lo, float hi) {
-        __half2 v = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
-    __device__ static void store(void* p, float x) { *static_cast<__half*>(p) = __float2half_rn(x); }
-};
-
 template <int D, int MT, int STAGES>
 struct Layout {
-    static constexpr int kSub = D / 64;                 // 128-byte-wide sub-tiles per tile row
     static constexpr int kTileBytes = kBS * D * 2;      // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
     static constexpr int kRingBytes = STAGES * kStageBytes;
@@ -118,14 +740,6 @@ struct Layout {
     static constexpr int kBlkOffset = kBarOffset + 2 * STAGES * 8;
     static constexpr int kSmemBytes = kBlkOffset + kMaxPartBlocks * 4 + 1024;  // + alignment slack
 };
-
-// Byte offset of the 16-byte chunk `chunk` of row `row` in a K/V tile laid
-// out by the 128B-swizzled TMA box [16 rows][64 columns] per sub-tile.
-template <int D>
-__device__ __forceinline__ uint32_t tile_offset(int row, int chunk) {
-    const int sub = chunk >> 3, c = chunk & 7;
-    return sub * (kBS * 128) + row * 128 + ((c ^ (row & 7)) << 4);
-}
 
 template <typename T, int D, int MT, int STAGES>
 __global__ void __launch_bounds__(kThreads)
@@ -213,16 +827,8 @@ __global__ void __launch_bounds__(kThreads)
                                             pa::ERR_WAIT_EMPTY))
                     break;
                 const int row = (s_blk[i] * p.num_kv_heads + g) * kBS;
-                const uint32_t kdst = base + st * Lay::kStageBytes;
-                const uint32_t vdst = kdst + Lay::kTileBytes;
-                pa::mbar_arrive_expect_tx(bar_full + 8 * st, Lay::kStageBytes);
-#pragma unroll
-                for (int sub = 0; sub < Lay::kSub; ++sub) {
-                    pa::tma_load_2d(kdst + sub * kBS * 128, &tmap_k, sub * 64, row,
-                                    bar_full + 8 * st, pol);
-                    pa::tma_load_2d(vdst + sub * kBS * 128, &tmap_v, sub * 64, row,
-                                    bar_full + 8 * st, pol);
-                }
+                issue_tile<D>(base + st * Lay::kStageBytes, bar_full + 8 * st, &tmap_k, &tmap_v,
+                              row, pol);
                 issued = i + 1;
             }
             // drain: no copy may be in flight when the CTA exits
@@ -235,185 +841,24 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ------------------------------- consumers -------------------------------
-    const int quad = lane >> 2;      // row within an 8-row half of an m-tile
-    const int qc = lane & 3;         // column pair within an n-tile
-
+    const int quad = lane >> 2;
+    const int qc = lane & 3;
     uint32_t qreg[MT == 1 ? kKSteps : 1][4];
-    if constexpr (MT == 1) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int row = quad + 8 * h;
-            const T* src = row < R ? static_cast<const T*>(p.q) +
-                                         ((int64_t)(q0 + row / G) * p.num_heads + g * G + row % G) * D
-                                   : nullptr;
-#pragma unroll
-            for (int ks = 0; ks < kKSteps; ++ks) {
-                uint32_t lo = 0, hi = 0;
-                if (src) {
-                    lo = __ldg(reinterpret_cast<const uint32_t*>(src + ks * 16 + 2 * qc));
-                    hi = __ldg(reinterpret_cast<const uint32_t*>(src + ks * 16 + 8 + 2 * qc));
-                }
-                qreg[ks][h] = lo;          // a0 / a1: k = 2qc, 2qc+1
-                qreg[ks][2 + h] = hi;      // a2 / a3: k = 8 + 2qc, ...
-            }
-        }
-    }
-
-    float o[MT][kNTiles][4];
-    float m_run[MT][2], l_run[MT][2];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-        for (int nt = 0; nt < kNTiles; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
-        m_run[mt][0] = m_run[mt][1] = -INFINITY;
-        l_run[mt][0] = l_run[mt][1] = 0.f;
-    }
-
-    // per-lane ldmatrix row addresses (before adding the stage base)
-    const int mat = lane >> 3, mrow = lane & 7;
-    const int k_tok = (mat >> 1) * 8 + mrow;   // K: m0,m1 tokens 0-7; m2,m3 tokens 8-15
-    const int k_chk = mat & 1;                 //    m0,m2 low 8 dims; m1,m3 high 8 dims
-    const int v_tok = (mat & 1) * 8 + mrow;    // V: m0,m2 tokens 0-7; m1,m3 tokens 8-15
-    const int v_chk = mat >> 1;                //    m0,m1 low 8 dims; m2,m3 high 8 dims
-    const int last_q_pos = L - r;              // query row i sees keys <= L - r + i
+    if constexpr (MT == 1) load_q_regs<T, D>(qreg, p.q, q0, G, R, g, p.num_heads, lane);
+    WarpAttn<T, D, MT> st;
+    st.reset();
 
     bool ok = true;
     for (int i = warp; i < nblk; i += kConsumerWarps) {
-        const int st = i % STAGES;
-        if (!pa::mbar_wait(bar_full + 8 * st, (i / STAGES) & 1, p.err, pa::ERR_WAIT_FULL)) {
+        const int stg = i % STAGES;
+        if (!pa::mbar_wait(bar_full + 8 * stg, (i / STAGES) & 1, p.err, pa::ERR_WAIT_FULL)) {
             ok = false;
             break;
         }
-        const uint32_t kb = base + st * Lay::kStageBytes;
-        const uint32_t vb = kb + Lay::kTileBytes;
-
-        // ---- S = Q K^T ----
-        float sacc[MT][2][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < kKSteps; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            pa::ldmatrix_x4(kb + tile_offset<D>(k_tok, 2 * ks + k_chk), b0, b1, b2, b3);
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                uint32_t a[4];
-                if constexpr (MT == 1) {
-                    a[0] = qreg[ks][0]; a[1] = qreg[ks][1]; a[2] = qreg[ks][2]; a[3] = qreg[ks][3];
-                } else {
-                    const int arow = mt * 16 + (mat & 1) * 8 + mrow;
-                    const int achk = 2 * ks + (mat >> 1);
-                    pa::ldmatrix_x4(base + Lay::kQOffset + arow * Lay::kQPitch + achk * 16, a[0],
-                                    a[1], a[2], a[3]);
-                }
-                pa::mma_16816<PK::kBF16>(sacc[mt][0], a, b0, b1);
-                pa::mma_16816<PK::kBF16>(sacc[mt][1], a, b2, b3);
-            }
-        }
-
-        // ---- mask, online softmax, P ----
-        const int tok0 = t_begin + i * kBS;                 // absolute position of token 0
-        const bool need_mask = tok0 + kBS - 1 > last_q_pos;  // block reaches past some row's bound
-        uint32_t phi[MT][4], plo[MT][4];
-        float alpha[MT][2];
-        bool rescale = false;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = mt * 16 + quad + 8 * h;
-                const int bound = min(last_q_pos + row / G, L - 1);
-                float mx = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        float v = sacc[mt][nt][2 * h + e] * p.scale_log2;
-                        if (need_mask && tok0 + nt * 8 + 2 * qc + e > bound) v = -INFINITY;
-                        sacc[mt][nt][2 * h + e] = v;
-                        mx = fmaxf(mx, v);
-                    }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m_run[mt][h], mx);
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                alpha[mt][h] = exp2f(m_run[mt][h] - m_use);
-                m_run[mt][h] = m_new;
-                float sum = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float pv = exp2f(sacc[mt][nt][2 * h + e] - m_use);
-                        sacc[mt][nt][2 * h + e] = pv;
-                        sum += pv;
-                    }
-                l_run[mt][h] = l_run[mt][h] * alpha[mt][h] + sum;
-                if (alpha[mt][h] != 1.f) rescale = true;
-            }
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const float a0 = alpha[mt][0], a1 = alpha[mt][1];
-#pragma unroll
-                for (int nt = 0; nt < kNTiles; ++nt) {
-                    o[mt][nt][0] *= a0;
-                    o[mt][nt][1] *= a0;
-                    o[mt][nt][2] *= a1;
-                    o[mt][nt][3] *= a1;
-                }
-            }
-        }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            // A fragment of P (16 rows x 16 tokens) straight from the S accumulators
-            float r0, r1, r2, r3, r4, r5, r6, r7;
-            phi[mt][0] = PK::pack(sacc[mt][0][0], sacc[mt][0][1], r0, r1);
-            phi[mt][1] = PK::pack(sacc[mt][0][2], sacc[mt][0][3], r2, r3);
-            phi[mt][2] = PK::pack(sacc[mt][1][0], sacc[mt][1][1], r4, r5);
-            phi[mt][3] = PK::pack(sacc[mt][1][2], sacc[mt][1][3], r6, r7);
-            plo[mt][0] = PK::pack(r0, r1);
-            plo[mt][1] = PK::pack(r2, r3);
-            plo[mt][2] = PK::pack(r4, r5);
-            plo[mt][3] = PK::pack(r6, r7);
-        }
-
-        // ---- O += P V ----
-        const int valid = L - tok0;   // tokens of this block inside the context (>= 1)
-#pragma unroll
-        for (int nd = 0; nd < D / 16; ++nd) {
-            uint32_t v0, v1, v2, v3;
-            pa::ldmatrix_x4_trans(vb + tile_offset<D>(v_tok, 2 * nd + v_chk), v0, v1, v2, v3);
-            if (valid < kBS) {
-                // slots past the context may hold anything (even NaN patterns): zero them
-                const int t_lo = 2 * qc, t_hi = 2 * qc + 8;
-                auto keep = [&](uint32_t x, int t) -> uint32_t {
-                    uint32_t lo = (t < valid) ? (x & 0xffffu) : 0u;
-                    uint32_t hi = (t + 1 < valid) ? (x & 0xffff0000u) : 0u;
-                    return lo | hi;
-                };
-                v0 = keep(v0, t_lo);
-                v2 = keep(v2, t_lo);
-                v1 = keep(v1, t_hi);
-                v3 = keep(v3, t_hi);
-            }
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                pa::mma_16816<PK::kBF16>(o[mt][2 * nd], phi[mt], v0, v1);
-                pa::mma_16816<PK::kBF16>(o[mt][2 * nd], plo[mt], v0, v1);
-                pa::mma_16816<PK::kBF16>(o[mt][2 * nd + 1], phi[mt], v2, v3);
-                pa::mma_16816<PK::kBF16>(o[mt][2 * nd + 1], plo[mt], v2, v3);
-            }
-        }
+        st.template block<Lay::kQPitch>(base + stg * Lay::kStageBytes, qreg, base + Lay::kQOffset,
+                                        t_begin + i * kBS, L - r, L, G, p.scale_log2, lane);
         __syncwarp();
-        if (lane == 0) pa::mbar_arrive(bar_empty + 8 * st);
+        if (lane == 0) pa::mbar_arrive(bar_empty + 8 * stg);
     }
 
     // ---- merge the consumer warps through shared memory (the ring is free now) ----
@@ -422,21 +867,19 @@ __global__ void __launch_bounds__(kThreads)
     float* const m_sh = reinterpret_cast<float*>(smem);                        // [W][kRows]
     float* const l_sh = m_sh + kConsumerWarps * kRows;                         // [W][kRows]
     float* const o_sh = l_sh + kConsumerWarps * kRows;                         // [W][kRows][D]
+    st.quad_sum();
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float l = l_run[mt][h];
-            l += __shfl_xor_sync(0xffffffffu, l, 1);
-            l += __shfl_xor_sync(0xffffffffu, l, 2);
             const int row = mt * 16 + quad + 8 * h;
             if (qc == 0) {
-                m_sh[warp * kRows + row] = ok ? m_run[mt][h] : -INFINITY;
-                l_sh[warp * kRows + row] = ok ? l : 0.f;
+                m_sh[warp * kRows + row] = ok ? st.m_run[mt][h] : -INFINITY;
+                l_sh[warp * kRows + row] = ok ? st.l_run[mt][h] : 0.f;
             }
 #pragma unroll
             for (int nt = 0; nt < kNTiles; ++nt) {
-                float2 v = make_float2(o[mt][nt][2 * h], o[mt][nt][2 * h + 1]);
+                float2 v = make_float2(st.o[mt][nt][2 * h], st.o[mt][nt][2 * h + 1]);
                 *reinterpret_cast<float2*>(o_sh + ((size_t)warp * kRows + row) * D + nt * 8 +
                                            2 * qc) = v;
             }
@@ -612,9 +1055,11 @@ struct MapCache {
 };
 MapCache g_maps;
 
+constexpr int kBalancedStages = 2;
+
 template <typename T, int D, int MT>
-pa_status launch_typed(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const DecodeParams& prm) {
+pa_status launch_partitioned(const pa::DecodeArgs& a, const CUtensorMap& mk,
+                             const CUtensorMap& mv, const DecodeParams& prm) {
     constexpr int STAGES = 8;
     using Lay = Layout<D, MT, STAGES>;
     auto kern = paged_decode_kernel<T, D, MT, STAGES>;
@@ -640,15 +1085,88 @@ pa_status launch_typed(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUt
     return PA_OK;
 }
 
+// Resident CTAs per SM for a kernel and shared-memory size, and the SM count, per device.
+struct Residency {
+    std::mutex mu;
+    struct E {
+        const void* fn;
+        int smem, device, ctas, sms;
+    } e[64];
+    int n = 0;
+    pa_status get(const void* fn, int smem, int* ctas, int* sms) {
+        int dev = 0;
+        if (pa_status s = pa::cuda_status(cudaGetDevice(&dev), "cudaGetDevice")) return s;
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n; ++i)
+            if (e[i].fn == fn && e[i].smem == smem && e[i].device == dev) {
+                *ctas = e[i].ctas;
+                *sms = e[i].sms;
+                return PA_OK;
+            }
+        int c = 0, m = 0;
+        if (pa_status s = pa::cuda_status(
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, fn, kWorkerWarps * 32, smem),
+                "occupancy query"))
+            return s;
+        if (pa_status s = pa::cuda_status(
+                cudaDeviceGetAttribute(&m, cudaDevAttrMultiProcessorCount, dev), "SM count"))
+            return s;
+        if (n < 64) e[n++] = E{fn, smem, dev, c, m};
+        *ctas = c;
+        *sms = m;
+        return PA_OK;
+    }
+};
+Residency g_residency;
+
+template <typename T, int D, int MT>
+pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                          BalancedParams prm) {
+    constexpr int S = kBalancedStages;
+    using Lay = BalancedLayout<D, MT, S>;
+    auto kern = paged_decode_balanced_kernel<T, D, MT, S>;
+    const int smem = Lay::smem_bytes(a.num_seqs);
+    static bool attr_set = false;   // per instantiation and process; benign race (idempotent)
+    if (!attr_set) {
+        // the largest size any call of this instantiation can ask for
+        if (pa_status s = pa::cuda_status(
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Lay::smem_bytes(pa::kBalancedMaxSeqs)),
+                "decode: set shared memory size"))
+            return s;
+        attr_set = true;
+    }
+    int ctas = 0, sms = 0;
+    if (pa_status s = g_residency.get(reinterpret_cast<const void*>(kern), smem, &ctas, &sms))
+        return s;
+    if (ctas < 1) return pa::fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
+    const int64_t workers = std::min<int64_t>((int64_t)ctas * sms * kWorkerWarps,
+                                              pa::balanced_worker_cap(a.num_seqs, a.num_kv_heads,
+                                                                      a.max_context_len));
+    prm.workers = (int)workers;
+    const int grid = (int)((workers + kWorkerWarps - 1) / kWorkerWarps);
+    kern<<<grid, kWorkerWarps * 32, smem, a.stream>>>(mk, mv, prm);
+    if (pa_status s = pa::cuda_status(cudaGetLastError(), "decode launch")) return s;
+    segment_reduce_kernel<T, D><<<a.num_seqs, 128, 0, a.stream>>>(prm);
+    return pa::cuda_status(cudaGetLastError(), "segment reduce launch");
+}
+
 template <typename T>
 pa_status launch_dtype(const pa::DecodeArgs& a, int mt, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const DecodeParams& prm) {
-    if (a.head_dim == 128) {
-        if (mt == 1) return launch_typed<T, 128, 1>(a, mk, mv, prm);
-        return launch_typed<T, 128, 2>(a, mk, mv, prm);
+                       const CUtensorMap& mv, const DecodeParams& prm,
+                       const BalancedParams& bprm) {
+    if (a.partition_size == 0) {
+        if (a.head_dim == 128)
+            return mt == 1 ? launch_balanced<T, 128, 1>(a, mk, mv, bprm)
+                           : launch_balanced<T, 128, 2>(a, mk, mv, bprm);
+        return mt == 1 ? launch_balanced<T, 64, 1>(a, mk, mv, bprm)
+                       : launch_balanced<T, 64, 2>(a, mk, mv, bprm);
     }
-    if (mt == 1) return launch_typed<T, 64, 1>(a, mk, mv, prm);
-    return launch_typed<T, 64, 2>(a, mk, mv, prm);
+    if (a.head_dim == 128)
+        return mt == 1 ? launch_partitioned<T, 128, 1>(a, mk, mv, prm)
+                       : launch_partitioned<T, 128, 2>(a, mk, mv, prm);
+    return mt == 1 ? launch_partitioned<T, 64, 1>(a, mk, mv, prm)
+                   : launch_partitioned<T, 64, 2>(a, mk, mv, prm);
 }
 
 }  // namespace
@@ -669,6 +1187,9 @@ pa_status launch_decode(const DecodeArgs& a) {
         return fail(PA_ERR_UNSUPPORTED,
                     "%lld query rows per KV head (q heads per KV head x max_q_len) > 32 for a "
                     "16-bit cache", (long long)rows);
+    if (a.partition_size == 0 && a.num_seqs > kBalancedMaxSeqs)
+        return fail(PA_ERR_UNSUPPORTED, "more than %d sequences in one balanced decode call",
+                    kBalancedMaxSeqs);
     CUtensorMap mk, mv;
     if (pa_status s = g_maps.get(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim)) return s;
     if (pa_status s = g_maps.get(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim)) return s;
@@ -691,8 +1212,26 @@ pa_status launch_decode(const DecodeArgs& a) {
     prm.num_blocks = a.num_blocks;
     prm.scale_log2 = a.scale * kLog2e;
     prm.out_f32 = a.out_dtype == PA_F32;
-    if (a.kv_dtype == PA_BF16) return launch_dtype<__nv_bfloat16>(a, mt, mk, mv, prm);
-    return launch_dtype<__half>(a, mt, mk, mv, prm);
+    BalancedParams b{};
+    b.out = a.out;
+    b.q = a.q;
+    b.block_tables = a.block_tables;
+    b.context_lens = a.context_lens;
+    b.qsl = a.query_start_loc;
+    b.slots = static_cast<uint8_t*>(a.slots);
+    b.err = prm.err;
+    b.max_blocks = a.max_blocks_per_seq;
+    b.num_heads = a.num_heads;
+    b.num_kv_heads = a.num_kv_heads;
+    b.group = G;
+    b.num_seqs = a.num_seqs;
+    b.num_blocks = a.num_blocks;
+    b.slot_rows = (int)rows;
+    b.slot_bytes = (int)balanced_slot_bytes(a.num_heads, a.num_kv_heads, a.head_dim, a.max_q_len);
+    b.scale_log2 = prm.scale_log2;
+    b.out_f32 = prm.out_f32;
+    if (a.kv_dtype == PA_BF16) return launch_dtype<__nv_bfloat16>(a, mt, mk, mv, prm, b);
+    return launch_dtype<__half>(a, mt, mk, mv, prm, b);
 }
 
 }  // namespace pa

@@ -121,7 +121,8 @@ class PagedKVCache:
         multi = max(q_lens) > 1
         qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
         nq = int(qsl[-1])
-        ws_bytes = decode_workspace_size(nq, q.shape[1], q.shape[2], max(lens), partition_size)
+        ws_bytes = decode_workspace_size(len(seqs), nq, q.shape[1], self.num_kv_heads, q.shape[2],
+                                         max(q_lens), max(lens), partition_size)
         return StepInputs(
             key=torch.cat(ks).to(dev), value=torch.cat(vs).to(dev),
             slots=torch.from_numpy(np.ascontiguousarray(slots)).to(dev),

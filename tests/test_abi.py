@@ -124,7 +124,10 @@ def test_device_calls_reject_bad_arguments_on_the_host():
     assert st == 1 and b"max_blocks" in L.pa_last_error()   # table too narrow
     st = L.pa_decode(p, 2, p, 1, p, p, 1, None, None, None, None, p, 512, p, None, 2, 2, 1, 8,
                      2, 128, 16, 10, 0.1, 4096, 0, None, 0, None)
-    assert st == 1 and b"workspace" in L.pa_last_error()    # split-KV needs a workspace
+    assert st == 1 and b"workspace" in L.pa_last_error()    # balanced schedule needs one
+    st = L.pa_decode(p, 2, p, 1, p, p, 1, None, None, None, None, p, 512, p, None, 2, 2, 1, 8,
+                     2, 128, 16, 10, 0.1, 4096, 24, None, 0, None)
+    assert st == 1 and b"partition_size" in L.pa_last_error()   # not a multiple of 16
     st = L.pa_append_kv(p, p, 1, p, p, 0, None, None, None, None, p, 3, 10, 2, 128, 16, None)
     assert st == 2                                       # bf16 rows into an fp16 cache
     st = L.pa_append_kv(p, p, 1, p, p, 3, None, None, None, None, p, 3, 10, 2, 128, 16, None)
@@ -136,7 +139,13 @@ def test_device_calls_reject_bad_arguments_on_the_host():
 
 
 def test_workspace_size():
-    assert pa.decode_workspace_size(64, 32, 128, 512, 512) == 0
-    n = pa.decode_workspace_size(4, 32, 128, 131072, 512)
+    # partitioned schedule: o, m, l per (q token, head, partition)
+    assert pa.decode_workspace_size(64, 64, 32, 8, 128, 1, 512, 512) == 0
+    n = pa.decode_workspace_size(4, 4, 32, 8, 128, 1, 131072, 512)
     rows = 4 * 32 * 256
     assert n == rows * 128 * 4 + 2 * rows * 4
+    # balanced schedule: 2 slots per worker, workers capped at 2048
+    slot = 16 + 4 * (4 * 1) * (128 + 2)
+    assert pa.decode_workspace_size(64, 64, 32, 8, 128, 1, 4096, 0) == 2 * 2048 * slot
+    assert pa.decode_workspace_size(1, 1, 8, 2, 64, 1, 17, 0) == 2 * (2 * 2) * (16 + 4 * 4 * 66)
+    assert pa.decode_workspace_size(1, 1, 8, 3, 64, 1, 17, 0) == 0      # heads not a multiple

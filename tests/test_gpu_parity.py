@@ -128,7 +128,7 @@ def test_bad_block_id_is_reported_not_faulted():
     bt = si.block_tables.clone()
     bt[1, 2] = wl.num_blocks + 1000               # outside the pool
     pa.decode(si.out, si.q, cache.k, cache.v, bt, si.context_lens, si.max_context_len,
-              wl.scale, num_blocks=cache.num_blocks)
+              wl.scale, num_blocks=cache.num_blocks, workspace=si.workspace)
     assert pa.device_error() & (1 << 3)            # ERR_BAD_BLOCK, no fault
     assert pa.device_error() == 0                  # the word was cleared
 
@@ -141,7 +141,7 @@ def test_validate_mode_rejects_bad_tables(monkeypatch):
     bt[0, 0] = -5
     with pytest.raises(pa.PAError) as e:
         pa.decode(si.out, si.q, cache.k, cache.v, bt, si.context_lens, si.max_context_len,
-                  wl.scale, num_blocks=cache.num_blocks)
+                  wl.scale, num_blocks=cache.num_blocks, workspace=si.workspace)
     assert e.value.status == 6
     bad = si.slots.clone()
     bad[0] = cache.num_blocks * 16 + 3
@@ -150,7 +150,7 @@ def test_validate_mode_rejects_bad_tables(monkeypatch):
     assert e.value.status == 6
     # valid inputs still pass validation
     pa.decode(si.out, si.q, cache.k, cache.v, si.block_tables, si.context_lens,
-              si.max_context_len, wl.scale, num_blocks=cache.num_blocks)
+              si.max_context_len, wl.scale, num_blocks=cache.num_blocks, workspace=si.workspace)
     torch.cuda.synchronize()
 
 
@@ -163,3 +163,66 @@ def test_empty_inputs_are_no_ops():
               si.max_context_len, wl.scale, num_blocks=cache.num_blocks)
     torch.cuda.synchronize()
     assert torch.equal(before, cache.k)
+
+
+def _written_slots(ws: torch.Tensor, wl, max_q_len: int):
+    """Partial slots of the balanced schedule that the last call wrote (the
+    workspace was filled with 0xFF first, so unwritten headers read -1)."""
+    rows = (wl.num_heads // wl.num_kv_heads) * max_q_len
+    slot_bytes = (16 + 4 * rows * (wl.head_dim + 2) + 15) // 16 * 16
+    raw = ws.cpu().numpy()
+    out = []
+    for i in range(raw.size // slot_bytes):
+        b = raw[i * slot_bytes:(i + 1) * slot_bytes]
+        hdr = b[:16].view(np.int32)
+        if hdr[0] < 0:
+            continue
+        f = b[16:16 + 4 * rows * (2 + wl.head_dim)].view(np.float32)
+        m, l, o = f[:rows], f[rows:2 * rows], f[2 * rows:].reshape(rows, wl.head_dim)
+        out.append((tuple(int(x) for x in hdr), m, l, o))
+    return out
+
+
+@pytest.mark.parametrize("case", [
+    # many short sequences: a share covers several (sequence, kv head) segments
+    ("many_short", [1, 2, 3, 17, 31, 33, 5, 64, 100, 7] * 6, [1] * 60, 16, 4, 128),
+    # one long sequence and MQA: far more shares than segments, most cut
+    ("one_long", [20000], [1], 8, 1, 128),
+    # verify runs and GQA 8, partial slots with 2 m-tiles of rows
+    ("verify_long", [3000, 777, 4100], [4, 1, 3], 32, 4, 128),
+])
+def test_balanced_partials_match_oracle(case):
+    name, lens, qlens, H, Hkv, d = case
+    wl = W.simple(name, 300 + len(lens), lens, qlens, H, Hkv, d, "bf16")
+    ref = oracle.run(wl, threads=THREADS, canary_blocks=W.CANARY_BLOCKS,
+                     canary_byte=W.CANARY_BYTE)
+    from paged_kv_cache_154_gb300.engine import PagedKVCache
+    cache = PagedKVCache(wl.num_blocks, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
+                         free_order=wl.free_order)
+    names = {}
+    for ops in wl.phases:
+        cache.run_phase(ops, names)
+    si = cache.prepare_step(wl.step, names, wl.q, torch.float32, 0)
+    si.workspace.fill_(0xFF)
+    cache.step(si, wl.scale, 0)
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+    check_out(ref, si.out, "bf16")
+    slots = _written_slots(si.workspace, wl, si.max_q_len)
+    assert slots, "expected at least one cut segment"
+    G = wl.num_heads // wl.num_kv_heads
+    qsl = wl.query_start_loc
+    for (s, g, t0, t1), m, l, o in slots:
+        L = wl.context_lens[s]
+        assert 0 <= t0 < t1 <= L and t0 % 16 == 0
+        om, mm, lm = oracle.attend(ref.q64, ref.cache, ref.block_tables, ref.context_lens, qsl,
+                                   wl.num_heads, wl.scale, t0, t1)
+        r = qsl[s + 1] - qsl[s]
+        for row in range(G * r):
+            qi, h = qsl[s] + row // G, g * G + row % G
+            if lm[qi, h] == 0:
+                assert l[row] == 0 and np.isneginf(m[row])
+                continue
+            np.testing.assert_allclose(m[row], mm[qi, h] * np.log2(np.e), rtol=1e-5, atol=1e-4)
+            np.testing.assert_allclose(l[row], lm[qi, h], rtol=1e-4)
+            np.testing.assert_allclose(o[row] / l[row], om[qi, h], rtol=0, atol=2e-3)
