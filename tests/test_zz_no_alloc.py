@@ -63,7 +63,8 @@ def test_no_alloc_matches_decode_on_two_calls_in_a_row(state):
 
 def test_no_alloc_rejects_workspace_beyond_its_maximum(state):
     wl, cache, si = state
-    big = pa.decode_workspace_size(64, 64, 128, 1 << 17, 16)
+    big = pa.decode_workspace_size(si.context_lens.shape[0], si.q.shape[0], wl.num_heads,
+                                   wl.num_kv_heads, wl.head_dim, si.max_q_len, 1 << 17, 16)
     assert big > pa.NO_ALLOC_WORKSPACE_BYTES
     with pytest.raises(pa.PAError) as e:
         pa.decode_no_alloc(si.out, si.q, cache.k, cache.v, si.block_tables, si.context_lens,
