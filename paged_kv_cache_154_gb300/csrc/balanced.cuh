@@ -1,0 +1,258 @@
+// The balanced decode schedule, shared by the 16-bit and the INT8 kernels.
+//
+// Work space. Each sequence s has nb_s = ceil(L_s / 16) blocks and R_s = G *
+// r_s query rows per KV head (G q heads per KV head, r_s query tokens). Rows
+// are served in tiles of RT (16 or 32); a sequence has C_s = ceil(R_s / RT)
+// row chunks. A *segment* is (sequence, kv head, chunk); segments are laid
+// out in order s, then kv head, then chunk, each as nb_s consecutive
+// "virtual blocks". Chunks of one (sequence, kv head) read the same KV, and
+// sit next to each other, so the workers that stream them do so at about
+// the same time and the repeated reads mostly hit L2.
+//
+// Shares. The B virtual blocks are cut into W equal contiguous shares, one
+// per worker warp: share w = [w*B/W, (w+1)*B/W). A segment that a share holds
+// whole is written as final output by that warp. Where share boundaries cut
+// a segment, every piece is written as a partial (m, l, O) to a slot -- slot
+// 2w for the first segment of share w, 2w+1 for its last -- and the reduce
+// kernel merges the pieces with the log-sum-exp rule.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace sched {
+
+constexpr int kBS = 16;            // tokens per block
+constexpr int kWorkerWarps = 4;    // warps per CTA
+
+struct Params {
+    void* out;
+    const void* q;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* qsl;            // may be null: one query token per sequence
+    int32_t* cum_out;              // workspace copy of the prefix sums [num_seqs + 1]
+    uint8_t* slots;                // partial slots [2 * workers][slot_bytes]
+    unsigned int* err;
+    int max_blocks;
+    int num_heads;
+    int num_kv_heads;
+    int group;                     // q heads per kv head
+    int num_seqs;
+    int num_blocks;
+    int workers;
+    int rows_per_tile;             // RT
+    int slot_bytes;
+    float scale_log2;              // softmax scale * log2(e)
+    int out_f32;
+};
+
+// A partial slot: int32 {seq, kv head, chunk, first token, end token, 0, 0, 0},
+// then fp32 m[RT] (base-2 units), l[RT], O[RT][D] (not normalised). Row j of a
+// slot is query row chunk*RT + j of the (sequence, kv head).
+struct Slot {
+    int32_t* hdr;
+    float* m;
+    float* l;
+    float* o;
+    __device__ __forceinline__ Slot(uint8_t* base, int rt) {
+        hdr = reinterpret_cast<int32_t*>(base);
+        m = reinterpret_cast<float*>(base + 32);
+        l = m + rt;
+        o = l + rt;
+    }
+};
+
+__host__ __device__ __forceinline__ int64_t slot_bytes(int rt, int d) {
+    return (32 + 4 * (int64_t)rt * (d + 2) + 15) / 16 * 16;
+}
+
+__device__ __forceinline__ int query_run(const int32_t* qsl, int s, int* q0) {
+    if (!qsl) {
+        *q0 = s;
+        return 1;
+    }
+    *q0 = __ldg(qsl + s);
+    return __ldg(qsl + s + 1) - *q0;
+}
+
+__device__ __forceinline__ int chunks_of(const Params& p, int s) {
+    int q0;
+    const int r = query_run(p.qsl, s, &q0);
+    return (p.group * r + p.rows_per_tile - 1) / p.rows_per_tile;
+}
+
+__host__ __device__ __forceinline__ int64_t share_start(int64_t w, int64_t B, int64_t W) {
+    return w * B / W;
+}
+
+// Shared-memory header of a balanced kernel: per-warp mbarriers, then
+// cum[num_seqs + 1] (virtual blocks before each sequence) and chunks[num_seqs].
+__host__ __device__ __forceinline__ int header_bytes(int num_seqs, int stages) {
+    return ((kWorkerWarps * stages * 8 + (num_seqs + 1) * 4 + num_seqs) + 1023) / 1024 * 1024;
+}
+
+// cum[s] = num_kv_heads * sum_{s' < s} C_s' * nb_s' and chunks[s] = C_s, by one
+// CTA; CTA 0 also copies cum to the workspace for the reduce kernel.
+__device__ void build_prefix(int32_t* cum, uint8_t* chunks, const Params& p) {
+    __shared__ int32_t warp_tot[32];
+    const int n = p.num_seqs;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (n + nt - 1) / nt;
+    const int a = min(n, tid * per), b = min(n, a + per);
+    int32_t local = 0;
+    for (int i = a; i < b; ++i) {
+        const int c = chunks_of(p, i);
+        chunks[i] = (uint8_t)c;
+        local += p.num_kv_heads * c * ((__ldg(p.context_lens + i) + kBS - 1) / kBS);
+    }
+    const int lane = tid & 31, warp = tid >> 5;
+    int32_t x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = nt >> 5;
+        int32_t t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    int32_t run = x - local + (warp > 0 ? warp_tot[warp - 1] : 0);
+    for (int i = a; i < b; ++i) {
+        cum[i] = run;
+        run += p.num_kv_heads * chunks[i] * ((__ldg(p.context_lens + i) + kBS - 1) / kBS);
+    }
+    if (tid == nt - 1) cum[n] = run;
+    __syncthreads();
+    if (blockIdx.x == 0 && p.cum_out)
+        for (int i = tid; i <= n; i += nt) p.cum_out[i] = cum[i];
+}
+
+// Position of virtual block f: sequence, kv head, chunk, block.
+struct Pos {
+    int s, g, c, b, nbs, C;
+};
+
+__device__ __forceinline__ Pos locate(const int32_t* cum, const uint8_t* chunks, int n, int hkv,
+                                      int64_t f) {
+    int lo = 0, hi = n;   // largest s with cum[s] <= f
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid] <= f) lo = mid;
+        else hi = mid;
+    }
+    Pos q;
+    q.s = lo;
+    q.C = chunks[lo];
+    q.nbs = (cum[lo + 1] - cum[lo]) / (hkv * q.C);
+    const int local = (int)(f - cum[lo]);
+    const int seg = local / q.nbs;
+    q.b = local - seg * q.nbs;
+    q.g = seg / q.C;
+    q.c = seg - q.g * q.C;
+    return q;
+}
+
+// The next segment after (s, g, c).
+__device__ __forceinline__ void next_segment(Pos& q, const int32_t* cum, const uint8_t* chunks,
+                                             int n, int hkv) {
+    q.b = 0;
+    if (++q.c < q.C) return;
+    q.c = 0;
+    if (++q.g < hkv) return;
+    q.g = 0;
+    do {
+        ++q.s;
+    } while (q.s < n - 1 && cum[q.s + 1] == cum[q.s]);
+    q.C = chunks[q.s];
+    q.nbs = (cum[q.s + 1] - cum[q.s]) / (hkv * q.C);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int out_f32) {
+    if (out_f32) static_cast<float*>(out)[idx] = v;
+    else if constexpr (sizeof(T) == 2) {
+        if constexpr (std::is_same<T, __half>::value)
+            static_cast<__half*>(out)[idx] = __float2half_rn(v);
+        else
+            static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+    }
+}
+
+// Merges the pieces of every cut segment. grid = (num_kv_heads * max chunks,
+// num_seqs), 128 threads; warp w takes query rows w, w + 4, ...; a lane owns
+// D / 32 columns. Online log-sum-exp over the pieces: out = sum 2^(m - M) O /
+// sum 2^(m - M) l.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p) {
+    constexpr int EPL = D / 32;
+    const int s = blockIdx.y;
+    const int C = chunks_of(p, s);
+    const int g = blockIdx.x / C, c = blockIdx.x - (blockIdx.x / C) * C;
+    if (g >= p.num_kv_heads) return;
+    const int L = __ldg(p.context_lens + s);
+    const int nbs = (L + kBS - 1) / kBS;
+    const int64_t B = p.cum_out[p.num_seqs];
+    const int64_t W = p.workers;
+    const int64_t fa = p.cum_out[s] + (int64_t)(g * C + c) * nbs;
+    const int64_t fb = fa + nbs;
+    const int64_t wa = ((fa + 1) * W - 1) / B;     // share holding virtual block fa
+    const int64_t wb = (fb * W - 1) / B;           // share holding virtual block fb - 1
+    if (wa == wb) return;                          // written whole by that share
+    int q0;
+    const int r = query_run(p.qsl, s, &q0);
+    const int G = p.group, RT = p.rows_per_tile;
+    const int rows = min(RT, G * r - c * RT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int row = warp; row < rows; row += 4) {
+        float M = -INFINITY, den = 0.f, acc[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
+        for (int64_t w = wa; w <= wb; ++w) {
+            const int64_t a0 = share_start(w, B, W);
+            if (a0 == share_start(w + 1, B, W)) continue;   // empty share
+            Slot sl(p.slots + (2 * w + (a0 >= fa ? 0 : 1)) * (int64_t)p.slot_bytes, RT);
+            const float l = __ldg(sl.l + row);
+            if (!(l > 0.f)) continue;                      // piece saw no key of this row
+            const float m = __ldg(sl.m + row);
+            const float* src = sl.o + (int64_t)row * D + lane * EPL;
+            float v[EPL];
+            if constexpr (EPL == 4) {
+                const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+                v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+            } else {
+                const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+                v[0] = t.x; v[1] = t.y;
+            }
+            const float Mn = fmaxf(M, m);
+            const float a = exp2f(M - Mn), b = exp2f(m - Mn);
+            den = den * a + l * b;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * a + v[e] * b;
+            M = Mn;
+        }
+        const int grow = c * RT + row;
+        const int64_t base =
+            ((int64_t)(q0 + grow / G) * p.num_heads + g * G + grow % G) * D + lane * EPL;
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) store_out<T>(p.out, base + e, acc[e] * inv, p.out_f32);
+    }
+}
+
+}  // namespace sched
+}  // namespace pa

@@ -193,11 +193,10 @@ extern "C" size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_token
         head_dim <= 0 || max_q_len <= 0 || max_context_len <= 0 || partition_size < 0 ||
         num_heads % num_kv_heads != 0)
         return 0;
-    if (partition_size == 0) {
-        const int64_t workers = pa::balanced_worker_cap(num_seqs, num_kv_heads, max_context_len);
-        return (size_t)(2 * workers *
-                        pa::balanced_slot_bytes(num_heads, num_kv_heads, head_dim, max_q_len));
-    }
+    if (partition_size == 0)
+        return (size_t)pa::balanced_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_q_len,
+                                          max_context_len)
+            .workspace_bytes;
     const int64_t parts = (max_context_len + (int64_t)partition_size - 1) / partition_size;
     if (parts <= 1) return 0;
     const size_t rows = (size_t)num_q_tokens * num_heads * parts;

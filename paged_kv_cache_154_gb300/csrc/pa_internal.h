@@ -105,21 +105,47 @@ struct DecodeArgs {
 };
 pa_status launch_decode(const DecodeArgs& a);
 
-// Balanced schedule: at most this many worker warps (and partial-slot pairs),
-// and at most this many sequences per call (their prefix sums live in shared
-// memory).
+// Balanced schedule (partition_size == 0): at most this many worker warps
+// (and partial-slot pairs), and at most this many sequences per call (their
+// prefix sums live in shared memory).
 constexpr int kBalancedMaxWorkers = 2048;
 constexpr int kBalancedMaxSeqs = 8192;
 
-inline int64_t balanced_worker_cap(int num_seqs, int num_kv_heads, int max_context_len) {
-    const int64_t blocks = (int64_t)num_seqs * num_kv_heads * ((max_context_len + 15) / 16);
-    return blocks < kBalancedMaxWorkers ? blocks : kBalancedMaxWorkers;
+struct BalancedShape {
+    int rows_per_tile;       // query rows per worker tile (16 or 32)
+    int64_t max_chunks;      // row tiles per (sequence, kv head), at most
+    int64_t workers;         // cap on worker warps
+    int64_t cum_bytes;       // workspace prefix sums, 256-byte aligned
+    int64_t slot_bytes;      // one partial slot
+    int64_t virtual_blocks;  // upper bound of the schedule's work units
+    int64_t workspace_bytes;
+};
+
+inline BalancedShape balanced_shape(int num_seqs, int num_heads, int num_kv_heads,
+                                    int head_dim, int max_q_len, int max_context_len) {
+    BalancedShape b{};
+    const int64_t rows = (int64_t)(num_heads / num_kv_heads) * max_q_len;
+    b.rows_per_tile = rows <= 16 ? 16 : 32;
+    b.max_chunks = (rows + b.rows_per_tile - 1) / b.rows_per_tile;
+    b.virtual_blocks =
+        (int64_t)num_seqs * num_kv_heads * b.max_chunks * ((max_context_len + 15) / 16);
+    b.workers = b.virtual_blocks < kBalancedMaxWorkers ? b.virtual_blocks : kBalancedMaxWorkers;
+    b.cum_bytes = ((int64_t)4 * (num_seqs + 1) + 255) / 256 * 256;
+    b.slot_bytes = (32 + 4 * (int64_t)b.rows_per_tile * (head_dim + 2) + 15) / 16 * 16;
+    b.workspace_bytes = b.cum_bytes + 2 * b.workers * b.slot_bytes;
+    return b;
 }
 
-// One partial slot: 16-byte header, then m, l and O of every query row of a KV head.
-inline int64_t balanced_slot_bytes(int num_heads, int num_kv_heads, int head_dim, int max_q_len) {
-    const int64_t rows = (int64_t)(num_heads / num_kv_heads) * max_q_len;
-    return (16 + 4 * rows * (head_dim + 2) + 15) / 16 * 16;
+// Limits of the balanced schedule that the host can check.
+inline pa_status balanced_check(const DecodeArgs& a) {
+    if (a.num_seqs > kBalancedMaxSeqs)
+        return fail(PA_ERR_UNSUPPORTED, "more than %d sequences in one call with partition_size 0",
+                    kBalancedMaxSeqs);
+    const BalancedShape b = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim,
+                                           a.max_q_len, a.max_context_len);
+    if (b.max_chunks > 255 || b.virtual_blocks > 0x7fffffffll)
+        return fail(PA_ERR_UNSUPPORTED, "decode call too large for one balanced launch");
+    return PA_OK;
 }
 
 }  // namespace pa

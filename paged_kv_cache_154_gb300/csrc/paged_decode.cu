@@ -37,6 +37,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "balanced.cuh"
 #include "pa_internal.h"
 #include "ptx.cuh"
 
@@ -138,10 +139,11 @@ struct WarpAttn {
     //   qreg   A fragments of Q (MT == 1), or qsm: smem Q tile base (MT > 1)
     //   tok0   absolute position of the block's first token
     //   last_q L - r: query row i sees keys <= L - r + i (row i = row / G)
+    //   row_off index of this tile's first query row among the KV head's rows
     template <int QPITCH>
     __device__ __forceinline__ void block(uint32_t kb, const uint32_t (*qreg)[4], uint32_t qsm,
-                                          int tok0, int last_q, int L, int G, float scale_log2,
-                                          int lane) {
+                                          int tok0, int last_q, int row_off, int L, int G,
+                                          float scale_log2, int lane) {
         using PK = Pack<T>;
         constexpr int kTile = kBS * D * 2;
         const uint32_t vb = kb + kTile;
@@ -188,7 +190,7 @@ struct WarpAttn {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int row = mt * 16 + quad + 8 * h;
-                const int bound = min(last_q + row / G, L - 1);
+                const int bound = min(last_q + (row_off + row) / G, L - 1);
                 float mx = -INFINITY;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
@@ -282,17 +284,19 @@ struct WarpAttn {
     }
 };
 
-// Q fragments of one m-tile in registers (MT == 1): rows quad and quad + 8.
+// Q fragments of one m-tile in registers (MT == 1): tile rows quad and quad + 8,
+// i.e. query rows row_lo + quad (+ 8) of kv head g, zero at or past row_hi.
 template <typename T, int D>
 __device__ __forceinline__ void load_q_regs(uint32_t (*qreg)[4], const void* q, int q0, int G,
-                                            int R, int g, int num_heads, int lane) {
+                                            int row_lo, int row_hi, int g, int num_heads,
+                                            int lane) {
     const int quad = lane >> 2, qc = lane & 3;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const int row = quad + 8 * h;
-        const T* src = row < R ? static_cast<const T*>(q) +
-                                     ((int64_t)(q0 + row / G) * num_heads + g * G + row % G) * D
-                               : nullptr;
+        const int row = row_lo + quad + 8 * h;
+        const T* src = row < row_hi ? static_cast<const T*>(q) +
+                                          ((int64_t)(q0 + row / G) * num_heads + g * G + row % G) * D
+                                    : nullptr;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             uint32_t lo = 0, hi = 0;
@@ -307,140 +311,47 @@ __device__ __forceinline__ void load_q_regs(uint32_t (*qreg)[4], const void* q, 
 }
 
 // ===========================================================================
-// balanced schedule
+// balanced schedule (see balanced.cuh)
 // ===========================================================================
 
-struct BalancedParams {
-    void* out;
-    const void* q;
-    const int32_t* block_tables;
-    const int32_t* context_lens;
-    const int32_t* qsl;
-    uint8_t* slots;          // partial slots [2 * workers][slot_bytes]
-    unsigned int* err;
-    int max_blocks;
-    int num_heads;
-    int num_kv_heads;
-    int group;
-    int num_seqs;
-    int num_blocks;
-    int workers;
-    int slot_rows;           // rows a slot holds (q heads per kv head x max_q_len)
-    int slot_bytes;
-    float scale_log2;
-    int out_f32;
-};
-
-// A partial slot: int32 {seq, kv head, first token, end token}, then fp32
-// m[slot_rows] (base-2 units), l[slot_rows], O[slot_rows][D] (unnormalised).
-struct SlotView {
-    int32_t* hdr;
-    float* m;
-    float* l;
-    float* o;
-    __device__ SlotView(uint8_t* base, int rows) {
-        hdr = reinterpret_cast<int32_t*>(base);
-        m = reinterpret_cast<float*>(base + 16);
-        l = m + rows;
-        o = l + rows;
-    }
-};
-
-// Shared-memory layout of the balanced kernel:
-//   [barriers: kWorkerWarps x S x 8][cum: num_seqs + 1 int32] -> rounded to 1024
-//   [ring of warp 0: S stages][ring of warp 1] ...   (each stage K tile + V tile)
-//   [Q tiles of the warps, MT > 1 only]
 template <int D, int MT, int S>
 struct BalancedLayout {
     static constexpr int kStage = 2 * kBS * D * 2;
     static constexpr int kRing = S * kStage;
     static constexpr int kQPitch = D * 2 + 16;
     static constexpr int kQTile = MT > 1 ? 16 * MT * kQPitch : 0;
-    __host__ __device__ static int header_bytes(int num_seqs) {
-        return ((kWorkerWarps * S * 8 + (num_seqs + 1) * 4) + 1023) / 1024 * 1024;
-    }
     __host__ __device__ static int smem_bytes(int num_seqs) {
-        return header_bytes(num_seqs) + kWorkerWarps * (kRing + kQTile) + 1024;
+        return pa::sched::header_bytes(num_seqs, S) + kWorkerWarps * (kRing + kQTile) + 1024;
     }
 };
-
-// Largest s with cum[s] <= f (cum non-decreasing, cum[0] = 0, f < cum[n]).
-__device__ __forceinline__ int find_seq(const int32_t* cum, int n, int64_t f) {
-    int lo = 0, hi = n;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cum[mid] <= f) lo = mid;
-        else hi = mid;
-    }
-    return lo;
-}
-
-__host__ __device__ __forceinline__ int64_t share_start(int64_t w, int64_t B, int64_t W) {
-    return w * B / W;
-}
-
-// cum[s] = num_kv_heads * sum_{s' < s} ceil(L_s' / 16), computed by one CTA.
-__device__ void block_prefix(int32_t* cum, const int32_t* lens, int n, int hkv) {
-    __shared__ int32_t warp_tot[32];
-    const int tid = threadIdx.x, nt = blockDim.x;
-    const int per = (n + nt - 1) / nt;
-    const int a = min(n, tid * per), b = min(n, a + per);
-    int32_t local = 0;
-    for (int i = a; i < b; ++i) local += hkv * ((__ldg(lens + i) + kBS - 1) / kBS);
-    // inclusive scan of `local` over the CTA
-    const int lane = tid & 31, warp = tid >> 5;
-    int32_t x = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_tot[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        const int nw = nt >> 5;
-        int32_t t = lane < nw ? warp_tot[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
-            if (lane >= o) t += y;
-        }
-        if (lane < nw) warp_tot[lane] = t;
-    }
-    __syncthreads();
-    int32_t run = x - local + (warp > 0 ? warp_tot[warp - 1] : 0);   // exclusive prefix
-    for (int i = a; i < b; ++i) {
-        cum[i] = run;
-        run += hkv * ((__ldg(lens + i) + kBS - 1) / kBS);
-    }
-    if (tid == nt - 1) cum[n] = run;
-    __syncthreads();
-}
 
 template <typename T, int D, int MT, int S>
 __global__ void __launch_bounds__(kWorkerWarps * 32)
     paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                  const __grid_constant__ CUtensorMap tmap_v,
-                                 const BalancedParams p) {
+                                 const pa::sched::Params p) {
+    using namespace pa::sched;
     using Lay = BalancedLayout<D, MT, S>;
     using PK = Pack<T>;
     constexpr int kKSteps = D / 16;
     constexpr int kNTiles = D / 8;
+    constexpr int RT = 16 * MT;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = pa::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const smem = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hkv = p.num_kv_heads, G = p.group;
+    const int hkv = p.num_kv_heads, G = p.group, n_seqs = p.num_seqs;
     int32_t* const cum = reinterpret_cast<int32_t*>(smem + kWorkerWarps * S * 8);
+    uint8_t* const chunks = reinterpret_cast<uint8_t*>(cum + n_seqs + 1);
     const uint32_t bars = base + warp * S * 8;
-    const uint32_t ring = base + Lay::header_bytes(p.num_seqs) + warp * Lay::kRing;
-    const uint32_t qtile = base + Lay::header_bytes(p.num_seqs) + kWorkerWarps * Lay::kRing +
-                           warp * Lay::kQTile;
+    const int hdr = header_bytes(n_seqs, S);
+    const uint32_t ring = base + hdr + warp * Lay::kRing;
+    const uint32_t qtile = base + hdr + kWorkerWarps * Lay::kRing + warp * Lay::kQTile;
 
-    block_prefix(cum, p.context_lens, p.num_seqs, hkv);
-    const int64_t B = cum[p.num_seqs];
+    build_prefix(cum, chunks, p);
+    const int64_t B = cum[n_seqs];
     const int64_t wid = (int64_t)blockIdx.x * kWorkerWarps + warp;
     const int64_t f0 = share_start(wid, B, p.workers);
     const int64_t f1 = share_start(wid + 1, B, p.workers);
@@ -454,7 +365,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     __syncwarp();
 
     // Producer side (all lanes run it; lane 0 issues): each lane keeps the TMA
-    // row of block (win + lane) of this share.
+    // row of virtual block (win + lane) of this share.
     uint64_t pol = 0;
     if (lane == 0) {
         pa::prefetch_tensormap(&tmap_k);
@@ -467,16 +378,13 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         const int64_t f = f0 + wbase + lane;
         my_row = 0;
         if (f < f1) {
-            const int s = find_seq(cum, p.num_seqs, f);
-            const int nbs = (cum[s + 1] - cum[s]) / hkv;
-            const int local = (int)(f - cum[s]);
-            const int g = local / nbs, b = local - (local / nbs) * nbs;
-            int blk = __ldg(p.block_tables + (int64_t)s * p.max_blocks + b);
+            const Pos q = locate(cum, chunks, n_seqs, hkv, f);
+            int blk = __ldg(p.block_tables + (int64_t)q.s * p.max_blocks + q.b);
             if (blk < 0 || blk >= p.num_blocks) {
                 if (p.err) atomicOr(p.err, pa::ERR_BAD_BLOCK);
                 blk = 0;
             }
-            my_row = (blk * hkv + g) * kBS;
+            my_row = (blk * hkv + q.g) * kBS;
         }
     };
     auto issue = [&](int k) {   // warp-uniform
@@ -490,38 +398,27 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     for (; issued < S && issued < n; ++issued) issue(issued);
 
     // Consumer side: walk the share block by block, segment by segment.
-    int cs = find_seq(cum, p.num_seqs, f0);
-    int cnbs = (cum[cs + 1] - cum[cs]) / hkv;
-    int cg, cb;
-    {
-        const int local = (int)(f0 - cum[cs]);
-        cg = local / cnbs;
-        cb = local - cg * cnbs;
-    }
+    Pos cur = locate(cum, chunks, n_seqs, hkv, f0);
     WarpAttn<T, D, MT> st;
     uint32_t qreg[MT == 1 ? kKSteps : 1][4];
-    int L = 0, r = 1, q0 = 0, R = 0, seg_b0 = cb;
+    int L = 0, r = 1, q0 = 0, rows = 0, row_off = 0, seg_b0 = cur.b;
     bool seg_first = true;
     auto start_segment = [&]() {
-        L = __ldg(p.context_lens + cs);
-        if (p.qsl) {
-            q0 = __ldg(p.qsl + cs);
-            r = __ldg(p.qsl + cs + 1) - q0;
-        } else {
-            q0 = cs;
-            r = 1;
-        }
-        R = G * r;
+        L = __ldg(p.context_lens + cur.s);
+        r = query_run(p.qsl, cur.s, &q0);
+        row_off = cur.c * RT;
+        rows = min(RT, G * r - row_off);
         if constexpr (MT == 1) {
-            load_q_regs<T, D>(qreg, p.q, q0, G, R, cg, p.num_heads, lane);
+            load_q_regs<T, D>(qreg, p.q, q0, G, row_off, row_off + rows, cur.g, p.num_heads, lane);
         } else {
             __syncwarp();
-            for (int e = lane; e < 16 * MT * (D / 8); e += 32) {
+            for (int e = lane; e < RT * (D / 8); e += 32) {
                 const int row = e / (D / 8), ch = e - row * (D / 8);
                 uint4 v = make_uint4(0, 0, 0, 0);
-                if (row < R) {
+                if (row < rows) {
+                    const int gr = row_off + row;
                     const T* src = static_cast<const T*>(p.q) +
-                                   ((int64_t)(q0 + row / G) * p.num_heads + cg * G + row % G) * D;
+                                   ((int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G) * D;
                     v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
                 }
                 asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
@@ -542,10 +439,11 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int row = mt * 16 + quad + 8 * h;
-                    if (row >= R) continue;
+                    if (row >= rows) continue;
+                    const int gr = row_off + row;
                     const float inv = 1.f / st.l_run[mt][h];
                     const int64_t obase =
-                        ((int64_t)(q0 + row / G) * p.num_heads + cg * G + row % G) * D;
+                        ((int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G) * D;
 #pragma unroll
                     for (int nt = 0; nt < kNTiles; ++nt) {
                         const float a = st.o[mt][nt][2 * h] * inv;
@@ -559,26 +457,27 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
                     }
                 }
         } else {
-            SlotView sv(p.slots + (2 * wid + slot_idx) * (int64_t)p.slot_bytes, p.slot_rows);
+            Slot sl(p.slots + (2 * wid + slot_idx) * (int64_t)p.slot_bytes, RT);
             if (lane == 0) {
-                sv.hdr[0] = cs;
-                sv.hdr[1] = cg;
-                sv.hdr[2] = seg_b0 * kBS;
-                sv.hdr[3] = tok_end;
+                sl.hdr[0] = cur.s;
+                sl.hdr[1] = cur.g;
+                sl.hdr[2] = cur.c;
+                sl.hdr[3] = seg_b0 * kBS;
+                sl.hdr[4] = tok_end;
             }
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int row = mt * 16 + quad + 8 * h;
-                    if (row >= R || row >= p.slot_rows) continue;
+                    if (row >= rows) continue;
                     if (qc == 0) {
-                        sv.m[row] = st.m_run[mt][h];
-                        sv.l[row] = st.l_run[mt][h];
+                        sl.m[row] = st.m_run[mt][h];
+                        sl.l[row] = st.l_run[mt][h];
                     }
 #pragma unroll
                     for (int nt = 0; nt < kNTiles; ++nt)
-                        *reinterpret_cast<float2*>(sv.o + (int64_t)row * D + nt * 8 + 2 * qc) =
+                        *reinterpret_cast<float2*>(sl.o + (int64_t)row * D + nt * 8 + 2 * qc) =
                             make_float2(st.o[mt][nt][2 * h], st.o[mt][nt][2 * h + 1]);
                 }
         }
@@ -589,28 +488,20 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     for (int k = 0; k < n; ++k) {
         if (!pa::mbar_wait(bars + 8 * (k % S), (k / S) & 1, p.err, pa::ERR_WAIT_FULL)) break;
         consumed = k + 1;
-        st.template block<Lay::kQPitch>(ring + (k % S) * Lay::kStage, qreg, qtile, cb * kBS,
-                                        L - r, L, G, p.scale_log2, lane);
+        st.template block<Lay::kQPitch>(ring + (k % S) * Lay::kStage, qreg, qtile, cur.b * kBS,
+                                        L - r, row_off, L, G, p.scale_log2, lane);
         __syncwarp();
         if (issued < n) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(issued);
             ++issued;
         }
-        ++cb;
-        const bool seg_done = cb == cnbs;
+        ++cur.b;
+        const bool seg_done = cur.b == cur.nbs;
         if (seg_done || k == n - 1) {
-            finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1, min(cb * kBS, L));
+            finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1, min(cur.b * kBS, L));
             if (k == n - 1) break;
-            // next (sequence, kv head) segment
-            cb = 0;
-            if (++cg == hkv) {
-                cg = 0;
-                do {
-                    ++cs;
-                } while (cs < p.num_seqs - 1 && cum[cs + 1] == cum[cs]);
-                cnbs = (cum[cs + 1] - cum[cs]) / hkv;
-            }
+            next_segment(cur, cum, chunks, n_seqs, hkv);
             seg_b0 = 0;
             seg_first = false;
             start_segment();
@@ -619,84 +510,6 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     // drain: no copy of this warp may still be in flight when it exits
     for (int k = consumed; k < issued; ++k)
         if (!pa::mbar_wait(bars + 8 * (k % S), (k / S) & 1, p.err, pa::ERR_WAIT_DRAIN)) break;
-}
-
-// Merges the partials of every (sequence, kv head) segment that a share
-// boundary cut: out = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w over the
-// covering shares (M = max m_w), the log-sum-exp rule. One CTA per sequence.
-template <typename T, int D>
-__global__ void __launch_bounds__(128)
-    segment_reduce_kernel(const BalancedParams p) {
-    const int s = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int hkv = p.num_kv_heads, G = p.group;
-    __shared__ int64_t red[2][4];
-    // this sequence's first block in the flattened order, and the total
-    int64_t before = 0, total = 0;
-    for (int i = tid; i < p.num_seqs; i += blockDim.x) {
-        const int64_t nb = (int64_t)hkv * ((__ldg(p.context_lens + i) + kBS - 1) / kBS);
-        total += nb;
-        if (i < s) before += nb;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        before += __shfl_xor_sync(0xffffffffu, before, o);
-        total += __shfl_xor_sync(0xffffffffu, total, o);
-    }
-    if ((tid & 31) == 0) {
-        red[0][tid >> 5] = before;
-        red[1][tid >> 5] = total;
-    }
-    __syncthreads();
-    before = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-    total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-    const int L = __ldg(p.context_lens + s);
-    const int nbs = (L + kBS - 1) / kBS;
-    int q0, r;
-    if (p.qsl) {
-        q0 = __ldg(p.qsl + s);
-        r = __ldg(p.qsl + s + 1) - q0;
-    } else {
-        q0 = s;
-        r = 1;
-    }
-    const int R = G * r;
-    const int64_t W = p.workers;
-    for (int g = 0; g < hkv; ++g) {
-        const int64_t fa = before + (int64_t)g * nbs, fb = fa + nbs;
-        const int64_t wa = ((fa + 1) * W - 1) / total;     // share holding block fa
-        const int64_t wb = (fb * W - 1) / total;           // share holding block fb - 1
-        if (wa == wb) continue;                            // written whole by that share
-        for (int e = tid; e < R * D; e += blockDim.x) {
-            const int row = e / D, col = e - row * D;
-            float M = -INFINITY;
-            for (int64_t w = wa; w <= wb; ++w) {
-                const int64_t a0 = share_start(w, total, W);
-                if (a0 == share_start(w + 1, total, W)) continue;   // empty share
-                SlotView sv(p.slots + (2 * w + (a0 >= fa ? 0 : 1)) * (int64_t)p.slot_bytes,
-                            p.slot_rows);
-                M = fmaxf(M, sv.m[row]);
-            }
-            const float Mu = M == -INFINITY ? 0.f : M;
-            float num = 0.f, den = 0.f;
-            for (int64_t w = wa; w <= wb; ++w) {
-                const int64_t a0 = share_start(w, total, W);
-                if (a0 == share_start(w + 1, total, W)) continue;
-                SlotView sv(p.slots + (2 * w + (a0 >= fa ? 0 : 1)) * (int64_t)p.slot_bytes,
-                            p.slot_rows);
-                const float l = sv.l[row];
-                if (!(l > 0.f)) continue;
-                const float wt = exp2f(sv.m[row] - Mu);
-                num += wt * sv.o[(int64_t)row * D + col];
-                den += wt * l;
-            }
-            const float val = num / den;
-            const int64_t idx =
-                ((int64_t)(q0 + row / G) * p.num_heads + g * G + row % G) * D + col;
-            if (p.out_f32) static_cast<float*>(p.out)[idx] = val;
-            else Pack<T>::store(static_cast<T*>(p.out) + idx, val);
-        }
-    }
 }
 
 // ===========================================================================
@@ -844,7 +657,7 @@ __global__ void __launch_bounds__(kThreads)
     const int quad = lane >> 2;
     const int qc = lane & 3;
     uint32_t qreg[MT == 1 ? kKSteps : 1][4];
-    if constexpr (MT == 1) load_q_regs<T, D>(qreg, p.q, q0, G, R, g, p.num_heads, lane);
+    if constexpr (MT == 1) load_q_regs<T, D>(qreg, p.q, q0, G, 0, R, g, p.num_heads, lane);
     WarpAttn<T, D, MT> st;
     st.reset();
 
@@ -856,7 +669,7 @@ __global__ void __launch_bounds__(kThreads)
             break;
         }
         st.template block<Lay::kQPitch>(base + stg * Lay::kStageBytes, qreg, base + Lay::kQOffset,
-                                        t_begin + i * kBS, L - r, L, G, p.scale_log2, lane);
+                                        t_begin + i * kBS, L - r, 0, L, G, p.scale_log2, lane);
         __syncwarp();
         if (lane == 0) pa::mbar_arrive(bar_empty + 8 * stg);
     }
@@ -1121,7 +934,7 @@ Residency g_residency;
 
 template <typename T, int D, int MT>
 pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
-                          BalancedParams prm) {
+                          pa::sched::Params prm) {
     constexpr int S = kBalancedStages;
     using Lay = BalancedLayout<D, MT, S>;
     auto kern = paged_decode_balanced_kernel<T, D, MT, S>;
@@ -1140,21 +953,22 @@ pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const 
     if (pa_status s = g_residency.get(reinterpret_cast<const void*>(kern), smem, &ctas, &sms))
         return s;
     if (ctas < 1) return pa::fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
-    const int64_t workers = std::min<int64_t>((int64_t)ctas * sms * kWorkerWarps,
-                                              pa::balanced_worker_cap(a.num_seqs, a.num_kv_heads,
-                                                                      a.max_context_len));
+    const pa::BalancedShape shape = pa::balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
+                                                       a.head_dim, a.max_q_len, a.max_context_len);
+    const int64_t workers = std::min<int64_t>((int64_t)ctas * sms * kWorkerWarps, shape.workers);
     prm.workers = (int)workers;
     const int grid = (int)((workers + kWorkerWarps - 1) / kWorkerWarps);
     kern<<<grid, kWorkerWarps * 32, smem, a.stream>>>(mk, mv, prm);
     if (pa_status s = pa::cuda_status(cudaGetLastError(), "decode launch")) return s;
-    segment_reduce_kernel<T, D><<<a.num_seqs, 128, 0, a.stream>>>(prm);
+    dim3 rgrid((unsigned)(a.num_kv_heads * shape.max_chunks), a.num_seqs);
+    pa::sched::segment_reduce_kernel<T, D><<<rgrid, 128, 0, a.stream>>>(prm);
     return pa::cuda_status(cudaGetLastError(), "segment reduce launch");
 }
 
 template <typename T>
 pa_status launch_dtype(const pa::DecodeArgs& a, int mt, const CUtensorMap& mk,
                        const CUtensorMap& mv, const DecodeParams& prm,
-                       const BalancedParams& bprm) {
+                       const pa::sched::Params& bprm) {
     if (a.partition_size == 0) {
         if (a.head_dim == 128)
             return mt == 1 ? launch_balanced<T, 128, 1>(a, mk, mv, bprm)
@@ -1182,14 +996,16 @@ pa_status launch_decode(const DecodeArgs& a) {
                     kMaxPartBlocks * kBS);
     const int G = a.num_heads / a.num_kv_heads;
     const int64_t rows = (int64_t)G * a.max_q_len;
-    const int mt = (int)((rows + 15) / 16);
-    if (mt > 2)
+    int mt = rows > 16 ? 2 : 1;
+    if (a.partition_size > 0 && rows > 32)
         return fail(PA_ERR_UNSUPPORTED,
-                    "%lld query rows per KV head (q heads per KV head x max_q_len) > 32 for a "
-                    "16-bit cache", (long long)rows);
-    if (a.partition_size == 0 && a.num_seqs > kBalancedMaxSeqs)
-        return fail(PA_ERR_UNSUPPORTED, "more than %d sequences in one balanced decode call",
-                    kBalancedMaxSeqs);
+                    "%lld query rows per KV head (q heads per KV head x max_q_len) > 32 with "
+                    "fixed partitions; use partition_size 0", (long long)rows);
+    if (a.partition_size == 0) {
+        if (pa_status s = balanced_check(a)) return s;
+        mt = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim, a.max_q_len,
+                            a.max_context_len).rows_per_tile / 16;
+    }
     CUtensorMap mk, mv;
     if (pa_status s = g_maps.get(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim)) return s;
     if (pa_status s = g_maps.get(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim)) return s;
@@ -1212,13 +1028,16 @@ pa_status launch_decode(const DecodeArgs& a) {
     prm.num_blocks = a.num_blocks;
     prm.scale_log2 = a.scale * kLog2e;
     prm.out_f32 = a.out_dtype == PA_F32;
-    BalancedParams b{};
+    const BalancedShape shape = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
+                                               a.head_dim, a.max_q_len, a.max_context_len);
+    pa::sched::Params b{};
     b.out = a.out;
     b.q = a.q;
     b.block_tables = a.block_tables;
     b.context_lens = a.context_lens;
     b.qsl = a.query_start_loc;
-    b.slots = static_cast<uint8_t*>(a.slots);
+    b.cum_out = static_cast<int32_t*>(a.slots);
+    b.slots = static_cast<uint8_t*>(a.slots) + shape.cum_bytes;
     b.err = prm.err;
     b.max_blocks = a.max_blocks_per_seq;
     b.num_heads = a.num_heads;
@@ -1226,8 +1045,8 @@ pa_status launch_decode(const DecodeArgs& a) {
     b.group = G;
     b.num_seqs = a.num_seqs;
     b.num_blocks = a.num_blocks;
-    b.slot_rows = (int)rows;
-    b.slot_bytes = (int)balanced_slot_bytes(a.num_heads, a.num_kv_heads, a.head_dim, a.max_q_len);
+    b.rows_per_tile = shape.rows_per_tile;
+    b.slot_bytes = (int)shape.slot_bytes;
     b.scale_log2 = prm.scale_log2;
     b.out_f32 = prm.out_f32;
     if (a.kv_dtype == PA_BF16) return launch_dtype<__nv_bfloat16>(a, mt, mk, mv, prm, b);

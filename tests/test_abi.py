@@ -144,8 +144,14 @@ def test_workspace_size():
     n = pa.decode_workspace_size(4, 4, 32, 8, 128, 1, 131072, 512)
     rows = 4 * 32 * 256
     assert n == rows * 128 * 4 + 2 * rows * 4
-    # balanced schedule: 2 slots per worker, workers capped at 2048
-    slot = 16 + 4 * (4 * 1) * (128 + 2)
-    assert pa.decode_workspace_size(64, 64, 32, 8, 128, 1, 4096, 0) == 2 * 2048 * slot
-    assert pa.decode_workspace_size(1, 1, 8, 2, 64, 1, 17, 0) == 2 * (2 * 2) * (16 + 4 * 4 * 66)
+    # balanced schedule: prefix sums, then 2 slots per worker (workers capped at 2048);
+    # a slot is a 32-byte header + m, l, O for a tile of 16 (or 32) query rows
+    slot = 32 + 4 * 16 * (128 + 2)
+    assert pa.decode_workspace_size(64, 64, 32, 8, 128, 1, 4096, 0) == 512 + 2 * 2048 * slot
+    slot64 = 32 + 4 * 16 * 66
+    assert pa.decode_workspace_size(1, 1, 8, 2, 64, 1, 17, 0) == 256 + 2 * (2 * 2) * slot64
+    # 32 q heads on one KV head with verify runs of 5: tiles of 32 rows, 5 chunks
+    slot32 = 32 + 4 * 32 * 130
+    assert pa.decode_workspace_size(256, 400, 32, 1, 128, 5, 16384, 0) == \
+        1280 + 2 * 2048 * slot32
     assert pa.decode_workspace_size(1, 1, 8, 3, 64, 1, 17, 0) == 0      # heads not a multiple

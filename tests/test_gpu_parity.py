@@ -167,19 +167,24 @@ def test_empty_inputs_are_no_ops():
 
 def _written_slots(ws: torch.Tensor, wl, max_q_len: int):
     """Partial slots of the balanced schedule that the last call wrote (the
-    workspace was filled with 0xFF first, so unwritten headers read -1)."""
-    rows = (wl.num_heads // wl.num_kv_heads) * max_q_len
-    slot_bytes = (16 + 4 * rows * (wl.head_dim + 2) + 15) // 16 * 16
-    raw = ws.cpu().numpy()
+    workspace was filled with 0xFF first, so unwritten headers read -1).
+    Layout: prefix sums (num_seqs + 1 int32, 256-byte aligned), then slots of
+    a 32-byte header {seq, kv head, chunk, first token, end token} and fp32
+    m[RT], l[RT], O[RT][d]."""
+    G = wl.num_heads // wl.num_kv_heads
+    rt = 16 if G * max_q_len <= 16 else 32
+    slot_bytes = (32 + 4 * rt * (wl.head_dim + 2) + 15) // 16 * 16
+    cum_bytes = (4 * (wl.num_seqs + 1) + 255) // 256 * 256
+    raw = ws.cpu().numpy()[cum_bytes:]
     out = []
     for i in range(raw.size // slot_bytes):
         b = raw[i * slot_bytes:(i + 1) * slot_bytes]
-        hdr = b[:16].view(np.int32)
+        hdr = b[:32].view(np.int32)
         if hdr[0] < 0:
             continue
-        f = b[16:16 + 4 * rows * (2 + wl.head_dim)].view(np.float32)
-        m, l, o = f[:rows], f[rows:2 * rows], f[2 * rows:].reshape(rows, wl.head_dim)
-        out.append((tuple(int(x) for x in hdr), m, l, o))
+        f = b[32:32 + 4 * rt * (2 + wl.head_dim)].view(np.float32)
+        m, l, o = f[:rt], f[rt:2 * rt], f[2 * rt:].reshape(rt, wl.head_dim)
+        out.append((tuple(int(x) for x in hdr[:5]), rt, m, l, o))
     return out
 
 
@@ -190,6 +195,8 @@ def _written_slots(ws: torch.Tensor, wl, max_q_len: int):
     ("one_long", [20000], [1], 8, 1, 128),
     # verify runs and GQA 8, partial slots with 2 m-tiles of rows
     ("verify_long", [3000, 777, 4100], [4, 1, 3], 32, 4, 128),
+    # 64 query rows per KV head: two row chunks per (sequence, kv head)
+    ("chunked_rows", [2500, 900], [2, 1], 32, 1, 128),
 ])
 def test_balanced_partials_match_oracle(case):
     name, lens, qlens, H, Hkv, d = case
@@ -212,17 +219,29 @@ def test_balanced_partials_match_oracle(case):
     assert slots, "expected at least one cut segment"
     G = wl.num_heads // wl.num_kv_heads
     qsl = wl.query_start_loc
-    for (s, g, t0, t1), m, l, o in slots:
+    for (s, g, c, t0, t1), rt, m, l, o in slots:
         L = wl.context_lens[s]
         assert 0 <= t0 < t1 <= L and t0 % 16 == 0
         om, mm, lm = oracle.attend(ref.q64, ref.cache, ref.block_tables, ref.context_lens, qsl,
                                    wl.num_heads, wl.scale, t0, t1)
         r = qsl[s + 1] - qsl[s]
-        for row in range(G * r):
+        for j in range(min(rt, G * r - c * rt)):
+            row = c * rt + j
             qi, h = qsl[s] + row // G, g * G + row % G
             if lm[qi, h] == 0:
-                assert l[row] == 0 and np.isneginf(m[row])
+                assert l[j] == 0 and np.isneginf(m[j])
                 continue
-            np.testing.assert_allclose(m[row], mm[qi, h] * np.log2(np.e), rtol=1e-5, atol=1e-4)
-            np.testing.assert_allclose(l[row], lm[qi, h], rtol=1e-4)
-            np.testing.assert_allclose(o[row] / l[row], om[qi, h], rtol=0, atol=2e-3)
+            np.testing.assert_allclose(m[j], mm[qi, h] * np.log2(np.e), rtol=1e-5, atol=1e-4)
+            np.testing.assert_allclose(l[j], lm[qi, h], rtol=1e-4)
+            np.testing.assert_allclose(o[j] / l[j], om[qi, h], rtol=0, atol=2e-3)
+
+
+def test_many_query_rows_per_kv_head_use_row_chunks():
+    """MQA with 32 q heads and verify runs of up to 5 tokens: up to 160 query
+    rows per KV head, served as row tiles of 32 (five chunks re-reading the
+    same KV), checked against the oracle."""
+    wl = W.simple("mqa_rows160", 71, [300, 1000, 77, 2600, 16, 5], [5, 1, 3, 4, 2, 5], 32, 1,
+                  128, "bf16")
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, "bf16")
