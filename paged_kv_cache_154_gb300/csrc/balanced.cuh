@@ -22,6 +22,7 @@
 #include <stdint.h>
 
 #include "pa_internal.h"
+#include "ptx.cuh"
 
 namespace pa {
 namespace sched {
@@ -98,8 +99,10 @@ __host__ __device__ __forceinline__ int header_bytes(int num_seqs, int stages) {
 
 // cum[s] = num_kv_heads * sum_{s' < s} C_s' * nb_s' and chunks[s] = C_s, by one
 // CTA; CTA 0 also copies cum to the workspace for the reduce kernel.
-__device__ void build_prefix(int32_t* cum, uint8_t* chunks, const Params& p) {
+static __device__ void build_prefix(int32_t* cum, uint8_t* chunks, const Params& p) {
     __shared__ int32_t warp_tot[32];
+    pa::grid_dependents_launch();   // the reduce kernel may be scheduled early
+    pa::grid_dependency_wait();     // inputs written by the previous kernel are visible
     const int n = p.num_seqs;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int per = (n + nt - 1) / nt;
@@ -194,24 +197,31 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int o
 
 // Merges the pieces of every cut segment. grid = (num_kv_heads * max chunks,
 // num_seqs), 128 threads; warp w takes query rows w, w + 4, ...; a lane owns
-// D / 32 columns. Online log-sum-exp over the pieces: out = sum 2^(m - M) O /
-// sum 2^(m - M) l.
+// D / 32 columns. Pieces are read eight at a time (independent loads), then
+// folded into an online log-sum-exp: out = sum 2^(m - M) O / sum 2^(m - M) l.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p) {
     constexpr int EPL = D / 32;
+    constexpr int kBatch = 8;
+    pa::grid_dependency_wait();     // the decode kernel's partials must be complete
     const int s = blockIdx.y;
     const int C = chunks_of(p, s);
     const int g = blockIdx.x / C, c = blockIdx.x - (blockIdx.x / C) * C;
     if (g >= p.num_kv_heads) return;
     const int L = __ldg(p.context_lens + s);
     const int nbs = (L + kBS - 1) / kBS;
-    const int64_t B = p.cum_out[p.num_seqs];
+    const int64_t B = __ldg(p.cum_out + p.num_seqs);
     const int64_t W = p.workers;
-    const int64_t fa = p.cum_out[s] + (int64_t)(g * C + c) * nbs;
+    const int64_t fa = __ldg(p.cum_out + s) + (int64_t)(g * C + c) * nbs;
     const int64_t fb = fa + nbs;
     const int64_t wa = ((fa + 1) * W - 1) / B;     // share holding virtual block fa
     const int64_t wb = (fb * W - 1) / B;           // share holding virtual block fb - 1
     if (wa == wb) return;                          // written whole by that share
+    // share wa holds the segment's first piece in its second slot unless the
+    // segment starts exactly where the share does; later shares hold their
+    // piece in their first slot (they start inside the segment)
+    const int first_slot = share_start(wa, B, W) < fa ? 1 : 0;
+    const bool may_be_empty = B < W;               // only then can a share hold no block
     int q0;
     const int r = query_run(p.qsl, s, &q0);
     const int G = p.group, RT = p.rows_per_tile;
@@ -221,29 +231,50 @@ __global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p) {
         float M = -INFINITY, den = 0.f, acc[EPL];
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-#pragma unroll 4
-        for (int64_t w = wa; w <= wb; ++w) {
-            const int64_t a0 = share_start(w, B, W);
-            if (a0 == share_start(w + 1, B, W)) continue;   // empty share
-            Slot sl(p.slots + (2 * w + (a0 >= fa ? 0 : 1)) * (int64_t)p.slot_bytes, RT);
-            const float l = __ldg(sl.l + row);
-            if (!(l > 0.f)) continue;                      // piece saw no key of this row
-            const float m = __ldg(sl.m + row);
-            const float* src = sl.o + (int64_t)row * D + lane * EPL;
-            float v[EPL];
-            if constexpr (EPL == 4) {
-                const float4 t = __ldg(reinterpret_cast<const float4*>(src));
-                v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-            } else {
-                const float2 t = __ldg(reinterpret_cast<const float2*>(src));
-                v[0] = t.x; v[1] = t.y;
-            }
-            const float Mn = fmaxf(M, m);
-            const float a = exp2f(M - Mn), b = exp2f(m - Mn);
-            den = den * a + l * b;
+        for (int64_t w0 = wa; w0 <= wb; w0 += kBatch) {
+            float lv[kBatch], mv[kBatch], ov[kBatch][EPL];
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * a + v[e] * b;
-            M = Mn;
+            for (int j = 0; j < kBatch; ++j) {
+                const int64_t w = w0 + j;
+                bool ok = w <= wb;
+                if (ok && may_be_empty)
+                    ok = share_start(w, B, W) != share_start(w + 1, B, W);
+                lv[j] = 0.f;
+                mv[j] = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) ov[j][e] = 0.f;
+                if (ok) {
+                    const int slot = w == wa ? first_slot : 0;
+                    Slot sl(p.slots + (2 * w + slot) * (int64_t)p.slot_bytes, RT);
+                    lv[j] = __ldg(sl.l + row);
+                    mv[j] = __ldg(sl.m + row);
+                    const float* src = sl.o + (int64_t)row * D + lane * EPL;
+                    if constexpr (EPL == 4) {
+                        const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+                        ov[j][0] = t.x; ov[j][1] = t.y; ov[j][2] = t.z; ov[j][3] = t.w;
+                    } else {
+                        const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+                        ov[j][0] = t.x; ov[j][1] = t.y;
+                    }
+                }
+            }
+            float Mb = M;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (lv[j] > 0.f) Mb = fmaxf(Mb, mv[j]);
+            if (Mb == -INFINITY) continue;                 // no piece of this batch saw a key
+            const float a = exp2f(M - Mb);
+            den *= a;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] *= a;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const float wgt = lv[j] > 0.f ? exp2f(mv[j] - Mb) : 0.f;
+                den += wgt * lv[j];
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] += wgt * ov[j][e];
+            }
+            M = Mb;
         }
         const int grow = c * RT + row;
         const int64_t base =

@@ -38,6 +38,25 @@ inline int dtype_bytes(pa_dtype t) {
 
 bool validate_enabled();
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel in the stream finishes; it must call
+// grid_dependency_wait() (ptx.cuh) before touching memory that kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 struct AppendArgs {
     const void* key;
     const void* value;

@@ -566,6 +566,8 @@ __global__ void __launch_bounds__(kThreads)
     const int part = blockIdx.x;
     const int g = blockIdx.y;
     const int s = blockIdx.z;
+    pa::grid_dependents_launch();
+    pa::grid_dependency_wait();
     const int L = __ldg(p.context_lens + s);
     const int t_begin = part * p.partition_size;
     if (t_begin >= L) return;
@@ -742,6 +744,7 @@ __global__ void __launch_bounds__(128)
                            const int32_t* __restrict__ qsl, int num_heads, int num_partitions,
                            int partition_size) {
     constexpr int EPL = D / 32;
+    pa::grid_dependency_wait();
     const int s = blockIdx.y;
     const int h = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -886,14 +889,19 @@ pa_status launch_partitioned(const pa::DecodeArgs& a, const CUtensorMap& mk,
         attr_set = true;
     }
     dim3 grid(a.num_partitions, a.num_kv_heads, a.num_seqs);
-    kern<<<grid, kThreads, Lay::kSmemBytes, a.stream>>>(mk, mv, prm);
-    if (pa_status s = pa::cuda_status(cudaGetLastError(), "decode launch")) return s;
+    if (pa_status s = pa::cuda_status(
+            pa::launch_pdl(kern, grid, dim3(kThreads), Lay::kSmemBytes, a.stream, mk, mv, prm),
+            "decode launch"))
+        return s;
     if (a.num_partitions > 1) {
         dim3 rgrid((a.num_heads + 3) / 4, a.num_seqs);
-        split_kv_reduce_kernel<T, D><<<rgrid, 128, 0, a.stream>>>(
-            a.out, a.out_dtype == PA_F32, a.o_part, a.m_part, a.l_part, a.context_lens,
-            a.query_start_loc, a.num_heads, a.num_partitions, a.partition_size);
-        if (pa_status s = pa::cuda_status(cudaGetLastError(), "split-KV reduce launch")) return s;
+        if (pa_status s = pa::cuda_status(
+                pa::launch_pdl(split_kv_reduce_kernel<T, D>, rgrid, dim3(128), 0, a.stream,
+                               a.out, (int)(a.out_dtype == PA_F32), a.o_part, a.m_part, a.l_part,
+                               a.context_lens, a.query_start_loc, a.num_heads, a.num_partitions,
+                               a.partition_size),
+                "split-KV reduce launch"))
+            return s;
     }
     return PA_OK;
 }
@@ -958,11 +966,14 @@ pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const 
     const int64_t workers = std::min<int64_t>((int64_t)ctas * sms * kWorkerWarps, shape.workers);
     prm.workers = (int)workers;
     const int grid = (int)((workers + kWorkerWarps - 1) / kWorkerWarps);
-    kern<<<grid, kWorkerWarps * 32, smem, a.stream>>>(mk, mv, prm);
-    if (pa_status s = pa::cuda_status(cudaGetLastError(), "decode launch")) return s;
+    if (pa_status s = pa::cuda_status(
+            pa::launch_pdl(kern, dim3(grid), dim3(kWorkerWarps * 32), smem, a.stream, mk, mv, prm),
+            "decode launch"))
+        return s;
     dim3 rgrid((unsigned)(a.num_kv_heads * shape.max_chunks), a.num_seqs);
-    pa::sched::segment_reduce_kernel<T, D><<<rgrid, 128, 0, a.stream>>>(prm);
-    return pa::cuda_status(cudaGetLastError(), "segment reduce launch");
+    return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<T, D>, rgrid,
+                                          dim3(128), 0, a.stream, prm),
+                           "segment reduce launch");
 }
 
 template <typename T>

@@ -245,3 +245,57 @@ def test_many_query_rows_per_kv_head_use_row_chunks():
     ref, cache, si, out = run_both(wl)
     check_cache_bits(ref, cache)
     check_out(ref, out, "bf16")
+
+
+INT8_SMALL = [
+    # name, lens, q_lens, H, Hkv, d, q dtype
+    ("int8_gqa4", [1, 15, 16, 17, 100, 513, 1500], [1] * 7, 32, 8, 128, torch.bfloat16),
+    ("int8_mqa_verify", [5, 40, 300, 1025, 2000, 77], [5, 2, 1, 4, 3, 5], 32, 1, 128,
+     torch.bfloat16),
+    ("int8_d64_f16q", [33, 700, 64, 129], [1, 2, 1, 3], 8, 2, 64, torch.float16),
+    ("int8_mha", [200, 31], [1, 1], 4, 4, 128, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("case", INT8_SMALL, ids=lambda c: c[0])
+def test_int8_small_shapes(case):
+    """INT8 KV: codes, scales and zero points bit-identical to the oracle's
+    quantiser; attention over the dequantised values within 1e-2."""
+    name, lens, qlens, H, Hkv, d, qdt = case
+    wl = W.simple(name, 500 + len(name), lens, qlens, H, Hkv, d, "int8", q_dtype=qdt,
+                  key_row_boost=4.0, boost_fraction=0.02)
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, "int8")
+
+
+def test_int8_output_in_q_dtype():
+    wl = W.simple("int8_out16", 77, [300, 1000], [2, 1], 32, 1, 128, "int8",
+                  q_dtype=torch.bfloat16)
+    ref, cache, si, out = run_both(wl, out_dtype=torch.bfloat16)
+    check_out(ref, out, "int8", torch.bfloat16)
+
+
+def test_mixed_int8_config():
+    """256 ragged sequences, MQA 32/1, INT8 KV, 20% with verify runs of 2-5."""
+    wl = W.mixed_int8()
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, "int8")
+
+
+def test_int8_wide_value_range():
+    """Values spanning many binades (x 2^-6 .. 2^6 per row) keep the exact
+    dequantisation path accurate: the running power-of-two V reference and the
+    per-row q scaling must not lose the small rows."""
+    wl = W.simple("int8_range", 91, [800, 1200, 50], [1, 3, 1], 16, 2, 128, "int8",
+                  q_dtype=torch.bfloat16)
+    rng = np.random.default_rng(0)
+    for op in wl.phases[0] + wl.step:
+        if isinstance(op, W.Append):
+            f = torch.from_numpy(2.0 ** rng.integers(-6, 7, size=op.k.shape[:2])).float()
+            op.k[:] = (op.k.float() * f[..., None]).to(op.k.dtype)
+            op.v[:] = (op.v.float() * f[..., None]).to(op.v.dtype)
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, "int8")
