@@ -98,17 +98,29 @@ __device__ __forceinline__ uint32_t tile8_offset(int row, int chunk) {
     else return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);                        // 64B swizzle
 }
 
+// Shared memory after the schedule header: the four warps' rings (each a
+// multiple of 1024 bytes, so every stage starts on a 1024-byte boundary as
+// TMA and the swizzle need), then per warp its stage scale areas, its Q tile
+// and its row factors.
 template <int D, int MT>
 struct Q8Layout {
     static constexpr int RT = 16 * MT;
     static constexpr int kTile = kBS * D;                         // codes of one K (or V) tile
     static constexpr int kStage = ((2 * kTile) + 1023) / 1024 * 1024;
     static constexpr int kRing = kStages * kStage;
+    static constexpr int kScales = kStages * kScaleBytes;
     static constexpr int kQPitch = D * 2 + 16;
     static constexpr int kQTile = RT * kQPitch;
-    static constexpr int kPerWarp = kRing + kStages * kScaleBytes + kQTile + RT * 4;
+    static constexpr int kRowMul = RT * 4;
+    static_assert(kRing % 1024 == 0, "rings must keep 1024-byte alignment");
+    static_assert(kScales % 16 == 0 && kQTile % 16 == 0, "16-byte alignment");
+    static constexpr int kRings = kWorkerWarps * kRing;
+    static constexpr int kScalesAt = kRings;
+    static constexpr int kQAt = kScalesAt + kWorkerWarps * kScales;
+    static constexpr int kRowMulAt = kQAt + kWorkerWarps * kQTile;
+    static constexpr int kBody = kRowMulAt + kWorkerWarps * kRowMul;
     __host__ __device__ static int smem_bytes(int num_seqs) {
-        return pa::sched::header_bytes(num_seqs, kStages) + kWorkerWarps * kPerWarp + 1024;
+        return pa::sched::header_bytes(num_seqs, kStages) + kBody + 1024;
     }
 };
 
@@ -141,13 +153,13 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     int32_t* const cum = reinterpret_cast<int32_t*>(smem + kWorkerWarps * S * 8);
     uint8_t* const chunks = reinterpret_cast<uint8_t*>(cum + n_seqs + 1);
     const uint32_t bars = base + warp * S * 8;
-    const int hdr = header_bytes(n_seqs, S);
-    const uint32_t wbase = base + hdr + warp * Lay::kPerWarp;
-    const uint32_t ring = wbase;
-    const uint32_t scl = wbase + Lay::kRing;                     // S x 160 bytes
-    const uint32_t qtile = scl + S * kScaleBytes;
-    uint8_t* const scl_p = smem + hdr + warp * Lay::kPerWarp + Lay::kRing;
-    float* const rowmul_p = reinterpret_cast<float*>(scl_p + S * kScaleBytes + Lay::kQTile);
+    const int hdr = header_bytes(n_seqs, S);            // a multiple of 1024
+    const uint32_t ring = base + hdr + warp * Lay::kRing;
+    const uint32_t scl = base + hdr + Lay::kScalesAt + warp * Lay::kScales;   // S x 160 bytes
+    const uint32_t qtile = base + hdr + Lay::kQAt + warp * Lay::kQTile;
+    uint8_t* const scl_p = smem + hdr + Lay::kScalesAt + warp * Lay::kScales;
+    float* const rowmul_p =
+        reinterpret_cast<float*>(smem + hdr + Lay::kRowMulAt + warp * Lay::kRowMul);
 
     build_prefix(cum, chunks, p);
     const int64_t B = cum[n_seqs];
