@@ -196,11 +196,11 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int o
 }
 
 // Merges the pieces of every cut segment. grid = (num_kv_heads * max chunks,
-// num_seqs), 128 threads; warp w takes query rows w, w + 4, ...; a lane owns
-// D / 32 columns. Pieces are read eight at a time (independent loads), then
-// folded into an online log-sum-exp: out = sum 2^(m - M) O / sum 2^(m - M) l.
+// num_seqs), one warp per query row of the row tile (at most 16 warps); a lane
+// owns D / 32 columns. Pieces are read eight at a time (independent loads),
+// then folded into an online log-sum-exp: out = sum 2^(m - M) O / sum 2^(m - M) l.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p) {
+__global__ void __launch_bounds__(512, 1) segment_reduce_kernel(const Params p) {
     constexpr int EPL = D / 32;
     constexpr int kBatch = 8;
     pa::grid_dependency_wait();     // the decode kernel's partials must be complete
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p) {
     const int G = p.group, RT = p.rows_per_tile;
     const int rows = min(RT, G * r - c * RT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int row = warp; row < rows; row += 4) {
+    for (int row = warp; row < rows; row += blockDim.x >> 5) {
         float M = -INFINITY, den = 0.f, acc[EPL];
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] = 0.f;

@@ -205,14 +205,14 @@ struct WarpAttn {
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                 const float m_new = fmaxf(m_run[mt][h], mx);
                 const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                alpha[mt][h] = exp2f(m_run[mt][h] - m_use);
+                alpha[mt][h] = pa::ex2(m_run[mt][h] - m_use);
                 m_run[mt][h] = m_new;
                 float sum = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const float pv = exp2f(sacc[mt][nt][2 * h + e] - m_use);
+                        const float pv = pa::ex2(sacc[mt][nt][2 * h + e] - m_use);
                         sacc[mt][nt][2 * h + e] = pv;
                         sum += pv;
                     }
@@ -972,7 +972,7 @@ pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const 
         return s;
     dim3 rgrid((unsigned)(a.num_kv_heads * shape.max_chunks), a.num_seqs);
     return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<T, D>, rgrid,
-                                          dim3(128), 0, a.stream, prm),
+                                          dim3(32 * std::min(shape.rows_per_tile, 16)), 0, a.stream, prm),
                            "segment reduce launch");
 }
 

@@ -228,54 +228,70 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         row_off = cur.c * RT;
         rows = min(RT, G * r - row_off);
         __syncwarp();
-        // Q tile: fp16, scaled by 2^(14 - e_row), dims in the MMA's k order
-        for (int row = 0; row < RT; ++row) {
-            float v[D / 32];
-            float mx = 0.f;
-            if (row < rows) {
-                const int gr = row_off + row;
-                const TQ* src = static_cast<const TQ*>(p.q) +
-                                ((int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G) * D +
-                                lane * (D / 32);
+        // Q tile: fp16, scaled by 2^(14 - e_row), dims in the MMA's k order.
+        // Eight rows' loads are issued together, then reduced and stored.
+        constexpr int EPL = D / 32;
+        for (int r0 = 0; r0 < RT; r0 += 8) {
+            float v[8][EPL];
 #pragma unroll
-                for (int e = 0; e < D / 32; ++e) {
-                    if constexpr (std::is_same<TQ, __half>::value) v[e] = __half2float(src[e]);
-                    else v[e] = __bfloat162float(src[e]);
-                    mx = fmaxf(mx, fabsf(v[e]));
+            for (int j = 0; j < 8; ++j) {
+                const int row = r0 + j;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) v[j][e] = 0.f;
+                if (row < rows) {
+                    const int gr = row_off + row;
+                    const TQ* src = static_cast<const TQ*>(p.q) +
+                                    ((int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G) *
+                                        D +
+                                    lane * EPL;
+                    if constexpr (EPL == 4) {
+                        const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+                        const TQ* t = reinterpret_cast<const TQ*>(&u);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) v[j][e] = (float)t[e];
+                    } else {
+                        const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
+                        const TQ* t = reinterpret_cast<const TQ*>(&u);
+                        v[j][0] = (float)t[0];
+                        v[j][1] = (float)t[1];
+                    }
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < D / 32; ++e) v[e] = 0.f;
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            int ex = 0;
-            if (mx > 0.f) {
-                ex = (int)((__float_as_uint(mx) >> 23) & 0xff) - 127;   // floor(log2(max|q|))
-                ex = max(-100, min(100, ex));
-            }
-            const float up = exp2i(14 - ex);
+            for (int j = 0; j < 8; ++j) {
+                const int row = r0 + j;
+                float mx = 0.f;
 #pragma unroll
-            for (int e = 0; e < D / 32; ++e) v[e] *= up;
-            const uint32_t rowb = qtile + row * Lay::kQPitch;
-            if constexpr (D == 128) {
-                // lane holds dims 4*lane .. +3: chunk lane/4, a = lane%4 -> k 2a, 2a+1, 8+2a, 9+2a
-                const int ch = lane >> 2, a = lane & 3;
-                const __half2 lo = __floats2half2_rn(v[0], v[1]);
-                const __half2 hi = __floats2half2_rn(v[2], v[3]);
-                asm volatile("st.shared.b32 [%0], %1;" ::"r"(rowb + (ch * 16 + 2 * a) * 2),
-                             "r"(*reinterpret_cast<const uint32_t*>(&lo)) : "memory");
-                asm volatile("st.shared.b32 [%0], %1;" ::"r"(rowb + (ch * 16 + 8 + 2 * a) * 2),
-                             "r"(*reinterpret_cast<const uint32_t*>(&hi)) : "memory");
-            } else {
-                // lane holds dims 2*lane, +1: chunk lane/8, a = (lane%8)/2, b = 2*(lane%2)
-                const int ch = lane >> 3, a = (lane & 7) >> 1, b = lane & 1;
-                const __half2 h = __floats2half2_rn(v[0], v[1]);
-                asm volatile("st.shared.b32 [%0], %1;" ::"r"(rowb + (ch * 16 + 8 * b + 2 * a) * 2),
-                             "r"(*reinterpret_cast<const uint32_t*>(&h)) : "memory");
+                for (int e = 0; e < EPL; ++e) mx = fmaxf(mx, fabsf(v[j][e]));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                int ex = 0;
+                if (mx > 0.f) {
+                    ex = (int)((__float_as_uint(mx) >> 23) & 0xff) - 127;   // floor(log2 max|q|)
+                    ex = max(-100, min(100, ex));
+                }
+                const float up = exp2i(14 - ex);
+                const uint32_t rowb = qtile + row * Lay::kQPitch;
+                if constexpr (D == 128) {
+                    // lane holds dims 4*lane .. +3: chunk lane/4, a = lane%4 -> k 2a, 2a+1, 8+2a, 9+2a
+                    const int ch = lane >> 2, a = lane & 3;
+                    const __half2 lo = __floats2half2_rn(v[j][0] * up, v[j][1] * up);
+                    const __half2 hi = __floats2half2_rn(v[j][2] * up, v[j][3] * up);
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(rowb + (ch * 16 + 2 * a) * 2),
+                                 "r"(*reinterpret_cast<const uint32_t*>(&lo)) : "memory");
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(rowb + (ch * 16 + 8 + 2 * a) * 2),
+                                 "r"(*reinterpret_cast<const uint32_t*>(&hi)) : "memory");
+                } else {
+                    // lane holds dims 2*lane, +1: chunk lane/8, a = (lane%8)/2, b = lane%2
+                    const int ch = lane >> 3, a = (lane & 7) >> 1, b = lane & 1;
+                    const __half2 h = __floats2half2_rn(v[j][0] * up, v[j][1] * up);
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(
+                                     rowb + (ch * 16 + 8 * b + 2 * a) * 2),
+                                 "r"(*reinterpret_cast<const uint32_t*>(&h)) : "memory");
+                }
+                if (lane == 0) rowmul_p[row] = row < rows ? p.scale_log2 * exp2i(ex - 14) : 0.f;
             }
-            if (lane == 0) rowmul_p[row] = row < rows ? p.scale_log2 * exp2i(ex - 14) : 0.f;
         }
         __syncwarp();
 #pragma unroll
@@ -452,14 +468,14 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                 const float m_new = fmaxf(m_run[mt][h], mx);
                 const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                const float al = exp2f(m_run[mt][h] - m_use);
+                const float al = pa::ex2(m_run[mt][h] - m_use);
                 m_run[mt][h] = m_new;
                 float sum = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const float pv = exp2f(sacc[mt][nt][2 * h + e] - m_use);
+                        const float pv = pa::ex2(sacc[mt][nt][2 * h + e] - m_use);
                         sum += pv;
                         sacc[mt][nt][2 * h + e] = pv * vs4[nt][e] * inv_vref;
                     }
@@ -643,7 +659,7 @@ pa_status launch8(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensor
         return s;
     dim3 rgrid((unsigned)(a.num_kv_heads * shape.max_chunks), a.num_seqs);
     return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<TQ, D>, rgrid,
-                                          dim3(128), 0, a.stream, prm),
+                                          dim3(32 * std::min(shape.rows_per_tile, 16)), 0, a.stream, prm),
                            "segment reduce launch");
 }
 

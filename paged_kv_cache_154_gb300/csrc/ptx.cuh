@@ -135,6 +135,14 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
     }
 }
 
+// 2^x with the hardware approximation (max relative error ~2^-22; results
+// below 2^-126 flush to 0; 2^-inf = 0), for softmax weights.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialization attribute may start before the previous kernel in the
 // stream has finished; grid_dependency_wait() blocks until that kernel has
