@@ -208,6 +208,12 @@ __global__ void __launch_bounds__(512, 1) segment_reduce_kernel(const Params p) 
     const int C = chunks_of(p, s);
     const int g = blockIdx.x / C, c = blockIdx.x - (blockIdx.x / C) * C;
     if (g >= p.num_kv_heads) return;
+    int q0;
+    const int r = query_run(p.qsl, s, &q0);
+    const int G = p.group, RT = p.rows_per_tile;
+    const int rows = min(RT, G * r - c * RT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= rows) return;                      // before any 64-bit division
     const int L = __ldg(p.context_lens + s);
     const int nbs = (L + kBS - 1) / kBS;
     const int64_t B = __ldg(p.cum_out + p.num_seqs);
@@ -222,11 +228,6 @@ __global__ void __launch_bounds__(512, 1) segment_reduce_kernel(const Params p) 
     // piece in their first slot (they start inside the segment)
     const int first_slot = share_start(wa, B, W) < fa ? 1 : 0;
     const bool may_be_empty = B < W;               // only then can a share hold no block
-    int q0;
-    const int r = query_run(p.qsl, s, &q0);
-    const int G = p.group, RT = p.rows_per_tile;
-    const int rows = min(RT, G * r - c * RT);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int row = warp; row < rows; row += blockDim.x >> 5) {
         float M = -INFINITY, den = 0.f, acc[EPL];
 #pragma unroll

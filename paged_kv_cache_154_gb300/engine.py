@@ -136,17 +136,39 @@ class PagedKVCache:
             workspace=(torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
                        if ws_bytes else None))
 
-    def step(self, si: StepInputs, scale: float, partition_size: int = 0,
-             write: bool = True) -> torch.Tensor:
-        """One decode step on device-resident inputs: copies, append, attend."""
-        if write:
-            if si.pairs is not None:
-                copy_blocks(self.k, self.v, si.pairs, self.num_blocks, self.k_scale,
-                            self.v_scale, self.k_zp, self.v_zp)
-            append_kv(si.key, si.value, self.k, self.v, si.slots, self.num_blocks,
-                      self.k_scale, self.v_scale, self.k_zp, self.v_zp)
+    def write_step(self, si: StepInputs) -> None:
+        """The step's cache writes: copy-on-write block copies, then the append."""
+        if si.pairs is not None:
+            copy_blocks(self.k, self.v, si.pairs, self.num_blocks, self.k_scale,
+                        self.v_scale, self.k_zp, self.v_zp)
+        append_kv(si.key, si.value, self.k, self.v, si.slots, self.num_blocks,
+                  self.k_scale, self.v_scale, self.k_zp, self.v_zp)
+
+    def attend_step(self, si: StepInputs, scale: float, partition_size: int = 0) -> torch.Tensor:
+        """The step's attention over the cache (decode kernel + partial merge)."""
         decode(si.out, si.q, self.k, self.v, si.block_tables, si.context_lens,
                si.max_context_len, scale, si.query_start_loc, si.max_q_len, self.num_blocks,
                self.k_scale, self.v_scale, self.k_zp, self.v_zp, partition_size,
                si.workspace)
         return si.out
+
+    def step(self, si: StepInputs, scale: float, partition_size: int = 0,
+             write: bool = True) -> torch.Tensor:
+        """One decode step on device-resident inputs: copies, append, attend."""
+        if write:
+            self.write_step(si)
+        return self.attend_step(si, scale, partition_size)
+
+    def capture(self, fn, *args) -> "torch.cuda.CUDAGraph":
+        """Record fn(*args) (e.g. write_step or attend_step) in a CUDA graph;
+        graph.replay() then runs the same kernels on the same buffers with no
+        per-launch host work. fn runs once eagerly first, so the library's
+        one-time set-up (tensor maps, kernel attributes) happens outside the
+        capture."""
+        fn(*args)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(*args)
+        torch.cuda.synchronize()
+        return g

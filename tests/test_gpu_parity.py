@@ -304,3 +304,21 @@ def test_int8_wide_value_range():
     ref, cache, si, out = run_both(wl)
     check_cache_bits(ref, cache)
     check_out(ref, out, "int8")
+
+
+def test_graph_replay_matches_eager():
+    """A step captured in CUDA graphs (writes; attention, with programmatic
+    dependent launches) replays to the same bits as the eager calls."""
+    wl = W.simple("graph", 17, [700, 2300, 90, 1500], [1, 3, 1, 2], 32, 8, 128, "bf16")
+    ref, cache, si, out = run_both(wl)
+    eager = out.clone()
+    g_write = cache.capture(cache.write_step, si)
+    g_attend = cache.capture(cache.attend_step, si, wl.scale, 0)
+    si.out.zero_()
+    for _ in range(3):
+        g_write.replay()
+        g_attend.replay()
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+    assert torch.equal(si.out, eager)
+    check_cache_bits(ref, cache)
