@@ -195,25 +195,32 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int o
     }
 }
 
-// Merges the pieces of every cut segment. grid = (num_kv_heads * max chunks,
-// num_seqs), one warp per query row of the row tile (at most 16 warps); a lane
-// owns D / 32 columns. Pieces are read eight at a time (independent loads),
-// then folded into an online log-sum-exp: out = sum 2^(m - M) O / sum 2^(m - M) l.
+// Merges the pieces of every cut segment. One warp per (sequence, kv head,
+// chunk, query row) -- a flat grid of 4-warp CTAs over num_seqs x num_kv_heads
+// x max_chunks x row_slots items (row_slots = the most rows a chunk can have)
+// -- so the items that exist run in about one wave. A lane owns D / 32
+// columns. Pieces are read eight at a time (independent loads), then folded
+// into an online log-sum-exp: out = sum 2^(m - M) O / sum 2^(m - M) l.
 template <typename T, int D>
-__global__ void __launch_bounds__(512, 1) segment_reduce_kernel(const Params p) {
+__global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p, int max_chunks,
+                                                             int row_slots) {
     constexpr int EPL = D / 32;
     constexpr int kBatch = 8;
     pa::grid_dependency_wait();     // the decode kernel's partials must be complete
-    const int s = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    int64_t item = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int row = (int)(item % row_slots);
+    item /= row_slots;
+    const int gc = (int)(item % (p.num_kv_heads * max_chunks));
+    const int s = (int)(item / (p.num_kv_heads * max_chunks));
+    if (s >= p.num_seqs) return;
     const int C = chunks_of(p, s);
-    const int g = blockIdx.x / C, c = blockIdx.x - (blockIdx.x / C) * C;
+    const int g = gc / C, c = gc - (gc / C) * C;
     if (g >= p.num_kv_heads) return;
     int q0;
     const int r = query_run(p.qsl, s, &q0);
     const int G = p.group, RT = p.rows_per_tile;
-    const int rows = min(RT, G * r - c * RT);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp >= rows) return;                      // before any 64-bit division
+    if (row >= min(RT, G * r - c * RT)) return;    // before any 64-bit division
     const int L = __ldg(p.context_lens + s);
     const int nbs = (L + kBS - 1) / kBS;
     const int64_t B = __ldg(p.cum_out + p.num_seqs);
@@ -228,62 +235,71 @@ __global__ void __launch_bounds__(512, 1) segment_reduce_kernel(const Params p) 
     // piece in their first slot (they start inside the segment)
     const int first_slot = share_start(wa, B, W) < fa ? 1 : 0;
     const bool may_be_empty = B < W;               // only then can a share hold no block
-    for (int row = warp; row < rows; row += blockDim.x >> 5) {
-        float M = -INFINITY, den = 0.f, acc[EPL];
+    float M = -INFINITY, den = 0.f, acc[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-        for (int64_t w0 = wa; w0 <= wb; w0 += kBatch) {
-            float lv[kBatch], mv[kBatch], ov[kBatch][EPL];
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    for (int64_t w0 = wa; w0 <= wb; w0 += kBatch) {
+        float lv[kBatch], mv[kBatch], ov[kBatch][EPL];
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int64_t w = w0 + j;
-                bool ok = w <= wb;
-                if (ok && may_be_empty)
-                    ok = share_start(w, B, W) != share_start(w + 1, B, W);
-                lv[j] = 0.f;
-                mv[j] = -INFINITY;
+        for (int j = 0; j < kBatch; ++j) {
+            const int64_t w = w0 + j;
+            bool ok = w <= wb;
+            if (ok && may_be_empty) ok = share_start(w, B, W) != share_start(w + 1, B, W);
+            lv[j] = 0.f;
+            mv[j] = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) ov[j][e] = 0.f;
-                if (ok) {
-                    const int slot = w == wa ? first_slot : 0;
-                    Slot sl(p.slots + (2 * w + slot) * (int64_t)p.slot_bytes, RT);
-                    lv[j] = __ldg(sl.l + row);
-                    mv[j] = __ldg(sl.m + row);
-                    const float* src = sl.o + (int64_t)row * D + lane * EPL;
-                    if constexpr (EPL == 4) {
-                        const float4 t = __ldg(reinterpret_cast<const float4*>(src));
-                        ov[j][0] = t.x; ov[j][1] = t.y; ov[j][2] = t.z; ov[j][3] = t.w;
-                    } else {
-                        const float2 t = __ldg(reinterpret_cast<const float2*>(src));
-                        ov[j][0] = t.x; ov[j][1] = t.y;
-                    }
+            for (int e = 0; e < EPL; ++e) ov[j][e] = 0.f;
+            if (ok) {
+                const int slot = w == wa ? first_slot : 0;
+                Slot sl(p.slots + (2 * w + slot) * (int64_t)p.slot_bytes, RT);
+                lv[j] = __ldg(sl.l + row);
+                mv[j] = __ldg(sl.m + row);
+                const float* src = sl.o + (int64_t)row * D + lane * EPL;
+                if constexpr (EPL == 4) {
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+                    ov[j][0] = t.x; ov[j][1] = t.y; ov[j][2] = t.z; ov[j][3] = t.w;
+                } else {
+                    const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+                    ov[j][0] = t.x; ov[j][1] = t.y;
                 }
             }
-            float Mb = M;
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j)
-                if (lv[j] > 0.f) Mb = fmaxf(Mb, mv[j]);
-            if (Mb == -INFINITY) continue;                 // no piece of this batch saw a key
-            const float a = exp2f(M - Mb);
-            den *= a;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[e] *= a;
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const float wgt = lv[j] > 0.f ? exp2f(mv[j] - Mb) : 0.f;
-                den += wgt * lv[j];
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[e] += wgt * ov[j][e];
-            }
-            M = Mb;
         }
-        const int grow = c * RT + row;
-        const int64_t base =
-            ((int64_t)(q0 + grow / G) * p.num_heads + g * G + grow % G) * D + lane * EPL;
-        const float inv = 1.f / den;
+        float Mb = M;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) store_out<T>(p.out, base + e, acc[e] * inv, p.out_f32);
+        for (int j = 0; j < kBatch; ++j)
+            if (lv[j] > 0.f) Mb = fmaxf(Mb, mv[j]);
+        if (Mb == -INFINITY) continue;                 // no piece of this batch saw a key
+        const float a = exp2f(M - Mb);
+        den *= a;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] *= a;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const float wgt = lv[j] > 0.f ? exp2f(mv[j] - Mb) : 0.f;
+            den += wgt * lv[j];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] += wgt * ov[j][e];
+        }
+        M = Mb;
     }
+    const int grow = c * RT + row;
+    const int64_t base =
+        ((int64_t)(q0 + grow / G) * p.num_heads + g * G + grow % G) * D + lane * EPL;
+    const float inv = 1.f / den;
+    if constexpr (EPL == 4) {
+        if (p.out_f32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + base) =
+                make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+            return;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) store_out<T>(p.out, base + e, acc[e] * inv, p.out_f32);
+}
+
+// Grid of segment_reduce_kernel for a call: (items + 3) / 4 CTAs of 128 threads.
+inline int64_t reduce_ctas(int num_seqs, int num_kv_heads, int64_t max_chunks, int row_slots) {
+    return ((int64_t)num_seqs * num_kv_heads * max_chunks * row_slots + 3) / 4;
 }
 
 }  // namespace sched

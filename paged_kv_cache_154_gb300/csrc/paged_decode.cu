@@ -970,9 +970,16 @@ pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const 
             pa::launch_pdl(kern, dim3(grid), dim3(kWorkerWarps * 32), smem, a.stream, mk, mv, prm),
             "decode launch"))
         return s;
-    dim3 rgrid((unsigned)(a.num_kv_heads * shape.max_chunks), a.num_seqs);
-    return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<T, D>, rgrid,
-                                          dim3(32 * std::min(shape.rows_per_tile, 16)), 0, a.stream, prm),
+    // query rows a chunk can have: all its G * max_q_len rows, up to one tile
+    const int row_slots = (int)std::min<int64_t>(shape.rows_per_tile,
+                                                 (int64_t)(a.num_heads / a.num_kv_heads) *
+                                                     a.max_q_len);
+    const int64_t rctas = pa::sched::reduce_ctas(a.num_seqs, a.num_kv_heads, shape.max_chunks,
+                                                 row_slots);
+    if (rctas > 0x7fffffff) return pa::fail(PA_ERR_UNSUPPORTED, "reduce grid too large");
+    return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<T, D>,
+                                          dim3((unsigned)rctas), dim3(128), 0, a.stream, prm,
+                                          (int)shape.max_chunks, row_slots),
                            "segment reduce launch");
 }
 
