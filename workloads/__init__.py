@@ -272,45 +272,54 @@ def best_of_n(name: str, seed: int, num_groups: int, n_forks: int,
 # The five named workloads (sizes as stated in their docstrings).
 # --------------------------------------------------------------------------
 
-def tiny() -> Workload:
+# Shard r of a workload (one per rank when several GPUs each take their own
+# batch of independent sequences) draws from seed + SHARD_STRIDE * r; shard 0
+# is the workload itself.
+SHARD_STRIDE = 1000
+
+
+def tiny(shard: int = 0) -> Workload:
     """4 sequences, post-append lengths {17, 33, 64, 100}; 8 q / 2 KV heads,
     head_dim 64, fp16, a 64-block pool placed by a seeded permutation."""
-    return simple("tiny", SEED_BASE + 1, [17, 33, 64, 100], [1, 1, 1, 1],
-                  num_heads=8, num_kv_heads=2, head_dim=64, kv_dtype="f16",
+    return simple("tiny", SEED_BASE + 1 + SHARD_STRIDE * shard, [17, 33, 64, 100],
+                  [1, 1, 1, 1], num_heads=8, num_kv_heads=2, head_dim=64, kv_dtype="f16",
                   pool_factor=0.0, min_pool_blocks=64)
 
 
-def llama3_8b(batch: int = 64, lo: int = 512, hi: int = 4096) -> Workload:
+def llama3_8b(batch: int = 64, lo: int = 512, hi: int = 4096, shard: int = 0) -> Workload:
     """Llama-3-8B-shaped decode step: 64 sequences, lengths U[512, 4096],
     32 q / 8 KV heads, head_dim 128, bf16, pool 1.2x the blocks needed."""
-    rng = np.random.default_rng(SEED_BASE + 2)
+    seed = SEED_BASE + 2 + SHARD_STRIDE * shard
+    rng = np.random.default_rng(seed)
     lens = rng.integers(lo, hi + 1, size=batch)
-    return simple("llama3_8b_decode", SEED_BASE + 2, lens, [1] * batch,
+    return simple("llama3_8b_decode", seed, lens, [1] * batch,
                   num_heads=32, num_kv_heads=8, head_dim=128, kv_dtype="bf16")
 
 
-def llama2_70b_best_of_5(num_groups: int = 8, prompt_len: int = 4096) -> Workload:
+def llama2_70b_best_of_5(num_groups: int = 8, prompt_len: int = 4096,
+                         shard: int = 0) -> Workload:
     """Llama-2-70B-shaped best-of-5: 8 prompts of 4096 (+1..15 shared) tokens,
     forked 5 ways, 0-256 private tokens per fork, 64 q / 8 KV heads, bf16."""
-    return best_of_n("llama2_70b_best_of_5", SEED_BASE + 3, num_groups, 5,
-                     prompt_len, 15, 256, num_heads=64, num_kv_heads=8,
+    return best_of_n("llama2_70b_best_of_5", SEED_BASE + 3 + SHARD_STRIDE * shard,
+                     num_groups, 5, prompt_len, 15, 256, num_heads=64, num_kv_heads=8,
                      head_dim=128)
 
 
-def long_context(lens=(32768, 65536, 100000, 131072)) -> Workload:
+def long_context(lens=(32768, 65536, 100000, 131072), shard: int = 0) -> Workload:
     """Long-context split-KV decode: 4 sequences up to 131072 tokens, 32 q /
     8 KV heads, head_dim 128, bf16, 1% of key rows scaled by 8."""
-    return simple("long_context_split_kv", SEED_BASE + 4, list(lens),
+    return simple("long_context_split_kv", SEED_BASE + 4 + SHARD_STRIDE * shard, list(lens),
                   [1] * len(lens), num_heads=32, num_kv_heads=8, head_dim=128,
                   kv_dtype="bf16", pool_factor=1.05, key_row_boost=8.0)
 
 
 def mixed_int8(batch: int = 256, median: int = 1024, cap: int = 16384,
-               verify_fraction: float = 0.2) -> Workload:
+               verify_fraction: float = 0.2, shard: int = 0) -> Workload:
     """Continuous-batching mixed step: 256 sequences with lognormal lengths
     (median 1024, sigma 1, capped at 16384), MQA 32 q / 1 KV head, head_dim
     128, INT8 KV; 20% of sequences carry a verify run of 2-5 query tokens."""
-    rng = np.random.default_rng(SEED_BASE + 5)
+    seed = SEED_BASE + 5 + SHARD_STRIDE * shard
+    rng = np.random.default_rng(seed)
     raw = rng.lognormal(mean=math.log(median), sigma=1.0, size=batch)
     q_lens = np.ones(batch, dtype=np.int64)
     nver = int(round(verify_fraction * batch))
@@ -318,7 +327,7 @@ def mixed_int8(batch: int = 256, median: int = 1024, cap: int = 16384,
     q_lens[ver] = rng.integers(2, 6, size=nver)
     lens = np.minimum(np.rint(raw), cap).astype(np.int64)
     lens = np.maximum(lens, q_lens)
-    return simple("mixed_mqa_int8_verify", SEED_BASE + 5, lens, q_lens,
+    return simple("mixed_mqa_int8_verify", seed, lens, q_lens,
                   num_heads=32, num_kv_heads=1, head_dim=128, kv_dtype="int8",
                   q_dtype=torch.bfloat16)
 
