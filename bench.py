@@ -28,7 +28,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak); seq-steps/s at 1 GPU"
-PROFILE = os.path.join(ROOT, "profiles", "paged_decode_llama3_8b.md")
+# Committed ncu summary per decode kernel family: the summary file and the
+# sources whose digest it records (traffic is reported only while they match).
+PROFILES = {
+    "16bit": ("paged_decode_llama3_8b.md", ("paged_decode.cu", "balanced.cuh", "ptx.cuh")),
+    "int8": ("paged_decode_int8_mixed.md", ("paged_decode_int8.cu", "balanced.cuh", "ptx.cuh")),
+}
 
 
 def parse():
@@ -95,24 +100,28 @@ def step_bytes(wl, out_bytes_per_elem=4):
             "decode": kv_read + q_b + out_b, "step": kv_read + q_b + out_b + appended}
 
 
-def kernel_digest():
+def kernel_family(kv_dtype: str) -> str:
+    return "int8" if kv_dtype == "int8" else "16bit"
+
+
+def kernel_digest(family: str = "16bit"):
     h = hashlib.sha256()
-    for f in ("paged_decode.cu", "balanced.cuh", "ptx.cuh"):
+    for f in PROFILES[family][1]:
         with open(os.path.join(ROOT, "paged_kv_cache_154_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
+def recorded_traffic(family: str = "16bit"):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
     try:
-        text = open(PROFILE).read()
+        text = open(os.path.join(ROOT, "profiles", PROFILES[family][0])).read()
     except OSError:
         return None
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_b or m_sha.group(1) != kernel_digest():
+    if not m_sha or not m_b or m_sha.group(1) != kernel_digest(family):
         return None
     return float(m_b.group(1))
 
@@ -301,13 +310,16 @@ def run_ours(args, rank, world, local):
                                    if world > 1 else "1 GPU")},
         "seq_steps_per_s": round(seq_steps, 1),
         "pct_of_hbm_peak": round(100 * value / peak, 2),
-        "roofline": {"kernel": ("pa_decode (paged_decode_balanced_kernel + segment_reduce_kernel)"
+        "roofline": {"kernel": ("pa_decode (paged_decode_int8_kernel + segment_reduce_kernel)"
+                                if wl.kv_dtype == "int8" else
+                                "pa_decode (paged_decode_balanced_kernel + segment_reduce_kernel)"
                                 if args.partition_size == 0 else
                                 "pa_decode (paged_decode_kernel + split_kv_reduce_kernel)"),
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(),
+                     "traffic": (recorded_traffic(kernel_family(wl.kv_dtype))
+                                 if args.partition_size == 0 else None),
                      "algorithmic_bytes_per_launch": nbytes["decode"],
                      "decode_ms_avg": round(dec_avg_s * 1e3, 5),
                      "decode_ms_p50": round(statistics.median(dec_ms), 5)},
