@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="read-once decode: fork groups read their shared blocks once")
     return ap.parse_args()
 
 
@@ -186,7 +188,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
-def build_state(wl, device, partition_size):
+def build_state(wl, device, partition_size, shared_prefix=False):
     import torch
     from paged_kv_cache_154_gb300.engine import PagedKVCache
     cache = PagedKVCache(wl.num_blocks, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
@@ -194,15 +196,31 @@ def build_state(wl, device, partition_size):
     names = {}
     for ops in wl.phases:
         cache.run_phase(ops, names)
-    si = cache.prepare_step(wl.step, names, wl.q, torch.float32, partition_size)
+    si = cache.prepare_step(wl.step, names, wl.q, torch.float32, partition_size,
+                            shared_prefix=shared_prefix)
     torch.cuda.synchronize()
     return cache, si
 
 
+def unique_kv_bytes(wl, group_start, prefix_len):
+    """KV bytes read-once decode must read: each group's shared prefix once,
+    every sequence's tokens after it once."""
+    per_tok = 2 * wl.num_kv_heads * wl.head_dim * (1 if wl.kv_dtype == "int8" else 2)
+    toks = 0
+    for g in range(len(prefix_len)):
+        toks += int(prefix_len[g])
+        for s in range(int(group_start[g]), int(group_start[g + 1])):
+            toks += wl.context_lens[s] - int(prefix_len[g])
+    return toks * per_tok
+
+
 def launches_per_step(si, partition_size):
-    n = 1 + 1                                           # append, decode
+    n = 1                                               # append
     if si.pairs is not None:
         n += 1                                          # copy_blocks
+    if si.shared is not None:
+        return n + 6                                    # prep, 2 x (decode + reduce), merge
+    n += 1                                              # decode
     if partition_size == 0 or si.max_context_len > partition_size:
         n += 1                                          # partial-result reduce
     return n
@@ -219,8 +237,14 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     wl = rank_workload(args.workload, rank)
-    cache, si = build_state(wl, device, args.partition_size)
+    if args.shared_prefix and args.partition_size:
+        raise SystemExit("--shared-prefix uses the balanced schedule (partition size 0)")
+    cache, si = build_state(wl, device, args.partition_size, args.shared_prefix)
     nbytes = step_bytes(wl)
+    if si.shared is not None:
+        nbytes["kv_read_unique"] = unique_kv_bytes(wl, si.shared.group_start_host,
+                                                   si.shared.prefix_len_host)
+        nbytes["decode_unique"] = nbytes["kv_read_unique"] + nbytes["q"] + nbytes["out"]
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
@@ -281,7 +305,9 @@ def run_ours(args, rank, world, local):
         return
     peak, peak_kind = measured_peak()
     dec_avg_s = statistics.mean(dec_ms) / 1e3
-    achieved = nbytes["decode"] / dec_avg_s / 1e9
+    # the method's own algorithmic bytes: read-once decode reads shared blocks once
+    alg_bytes = nbytes.get("decode_unique", nbytes["decode"])
+    achieved = alg_bytes / dec_avg_s / 1e9
     value = K * job_bytes / (tot_ms / 1e3) / 1e9
     seq_steps = K * job_seqs / (tot_ms / 1e3)
     line = {
@@ -300,7 +326,10 @@ def run_ours(args, rank, world, local):
         "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads,
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "block_size": 16, "context_tokens": sum(wl.context_lens),
-                   "schedule": ("balanced" if args.partition_size == 0
+                   "schedule": ("balanced, read-once shared prefixes "
+                                f"({len(si.shared.prefix_len_host)} fork groups)"
+                                if si.shared is not None else
+                                "balanced" if args.partition_size == 0
                                 else f"partitions of {args.partition_size}"),
                    "l2": "flushed between steps (2x L2 write, then a 2x L2 read so no dirty "
                          "line is left), each step timed alone",
@@ -310,7 +339,11 @@ def run_ours(args, rank, world, local):
                                    if world > 1 else "1 GPU")},
         "seq_steps_per_s": round(seq_steps, 1),
         "pct_of_hbm_peak": round(100 * value / peak, 2),
-        "roofline": {"kernel": ("pa_decode (paged_decode_int8_kernel + segment_reduce_kernel)"
+        "roofline": {"kernel": ("pa_decode_shared_prefix (prefix_prep_kernel, "
+                                "paged_decode_balanced_kernel + segment_reduce_kernel for the "
+                                "prefixes and for the suffixes, prefix_merge_kernel)"
+                                if si.shared is not None else
+                                "pa_decode (paged_decode_int8_kernel + segment_reduce_kernel)"
                                 if wl.kv_dtype == "int8" else
                                 "pa_decode (paged_decode_balanced_kernel + segment_reduce_kernel)"
                                 if args.partition_size == 0 else
@@ -319,8 +352,8 @@ def run_ours(args, rank, world, local):
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": (recorded_traffic(kernel_family(wl.kv_dtype))
-                                 if args.partition_size == 0 else None),
-                     "algorithmic_bytes_per_launch": nbytes["decode"],
+                                 if args.partition_size == 0 and si.shared is None else None),
+                     "algorithmic_bytes_per_launch": alg_bytes,
                      "decode_ms_avg": round(dec_avg_s * 1e3, 5),
                      "decode_ms_p50": round(statistics.median(dec_ms), 5)},
         "e2e": e2e,
@@ -341,21 +374,24 @@ def measure_e2e(wl, cache, si, args, graphs, K_e2e):
     from pinned host memory, run the step, copy the output back, sync."""
     import torch
     import paged_kv_cache_154_gb300 as pa
-    host = {}
+    pairs = []                                   # (device input, pinned host copy)
     for name in ("q", "key", "value", "slots", "block_tables", "context_lens", "pairs",
                  "query_start_loc"):
         t = getattr(si, name)
-        host[name] = None if t is None else t.cpu().pin_memory()
+        if t is not None:
+            pairs.append((t, t.cpu().pin_memory()))
+    if si.shared is not None:                    # the step's fork groups are inputs too
+        for t in (si.shared.group_start, si.shared.prefix_len):
+            pairs.append((t, t.cpu().pin_memory()))
     out_h = torch.empty(si.out.shape, dtype=si.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
     d2h = out_h.numel() * out_h.element_size()
     stream = torch.cuda.current_stream()
     times = []
     for k in range(K_e2e + 3):
         t0 = time.perf_counter()
-        for name, t in host.items():
-            if t is not None:
-                getattr(si, name).copy_(t, non_blocking=True)
+        for d, h in pairs:
+            d.copy_(h, non_blocking=True)
         for g in graphs:
             g.replay()
         out_h.copy_(si.out, non_blocking=True)

@@ -132,6 +132,24 @@ pa_status pa_pool_stats(pa_pool* pool, int32_t* free_blocks, int32_t* used,
 /* Reference count of one physical block. */
 pa_status pa_pool_refcount(pa_pool* pool, int32_t block, int32_t* ref);
 
+/* Fork groups for pa_decode_shared_prefix ([p2] §2.1: best-of-N forks share
+ * the prompt's blocks by reference count). Walks seqs[0..n) in order; a run
+ * of adjacent sequences whose first physical block is the same forms one
+ * group. prefix_len_out[g] is the number of leading tokens that every member
+ * holds in the same physical blocks and that come before every member's
+ * first query: whole 16-token blocks only, at most (L - r + 1) / 16 blocks
+ * for a member with L tokens and a query run of r (q_lens[i], or 1 when
+ * q_lens is NULL). A group of one sequence gets prefix 0.
+ *   group_start_out  host int32 [n + 1]: group g is seqs[group_start[g] ..
+ *                    group_start[g + 1])
+ *   prefix_len_out   host int32 [n]
+ *   num_groups_out   number of groups written
+ * PA_ERR_INVALID_ARG for an unknown sequence or a query run outside
+ * [1, L]. Forks that are not adjacent in seqs land in different groups. */
+pa_status pa_pool_prefix_groups(pa_pool* pool, const int32_t* seqs, int32_t n,
+                                const int32_t* q_lens, int32_t* group_start_out,
+                                int32_t* prefix_len_out, int32_t* num_groups_out);
+
 /* ======================================================================
  * Device operations. Pointers are device memory unless stated.
  * ==================================================================== */
@@ -273,6 +291,54 @@ pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
                              int32_t num_blocks, float scale,
                              int32_t max_context_len, int32_t partition_size,
                              void* stream);
+
+/* Workspace bytes of pa_decode_shared_prefix for these sizes (0 for invalid
+ * sizes). */
+size_t pa_decode_shared_prefix_workspace_size(
+    int32_t num_seqs, int32_t num_q_tokens, int32_t num_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t max_q_len,
+    int32_t max_context_len, int32_t num_groups, int32_t max_group_q_len,
+    int32_t max_prefix_len, int32_t max_blocks_per_seq);
+
+/* Decode attention with read-once shared prefixes (copy-on-write forks,
+ * [p2] §2.1). The result is that of pa_decode with partition_size 0 on the
+ * same arguments (16-bit caches only); the difference is that the blocks a
+ * group of forks shares are read once per group and KV head instead of once
+ * per fork:
+ *   1. each group's first prefix_len[g] tokens are attended by all of the
+ *      group's query rows together (no causal mask is needed: every prefix
+ *      token precedes every query of the group),
+ *   2. every sequence attends its own tokens [prefix_len, L) with the usual
+ *      causal offset for query runs,
+ *   3. each output row merges the two results by their log-sum-exp (the
+ *      rule of the split-KV reduce).
+ *   group_start   device int32 [num_groups + 1]: group g is sequences
+ *                 group_start[g] .. group_start[g + 1] - 1; groups cover
+ *                 0 .. num_seqs in order, none empty
+ *   prefix_len    device int32 [num_groups]: a multiple of 16, at most
+ *                 max_prefix_len and at most L - r + 1 for every member;
+ *                 every member's block table holds the same physical ids
+ *                 for the first prefix_len / 16 blocks (pa_pool_prefix_groups
+ *                 computes both arrays). 0 means no shared prefix.
+ *   max_group_q_len host: the largest number of query tokens in one group
+ *   max_prefix_len  host: the largest prefix_len
+ *   workspace     pa_decode_shared_prefix_workspace_size() bytes, 256-byte
+ *                 aligned, no initialisation needed.
+ * Other arguments as pa_decode. Under PA_VALIDATE=1 the group arrays are
+ * also checked against the block tables (PA_ERR_VALIDATION). INT8 caches
+ * return PA_ERR_UNSUPPORTED. */
+pa_status pa_decode_shared_prefix(
+    void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+    const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+    const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, const int32_t* query_start_loc,
+    int32_t num_seqs, int32_t num_q_tokens, int32_t max_q_len,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int32_t num_blocks, float scale,
+    int32_t max_context_len, const int32_t* group_start,
+    const int32_t* prefix_len, int32_t num_groups, int32_t max_group_q_len,
+    int32_t max_prefix_len, void* workspace, size_t workspace_bytes,
+    void* stream);
 
 /* Read and clear the device error word that kernels set instead of
  * trapping (a bounded wait that gave up, an index a kernel refused).

@@ -132,3 +132,48 @@ class BlockPool:
         used = sum(1 for r in self.ref if r > 0)
         shared = sum(1 for r in self.ref if r > 1)
         return len(self.free), used, shared
+
+    def prefix_groups(self, seqs: Sequence[int],
+                      q_lens: Optional[Sequence[int]] = None) -> Tuple[List[int], List[int]]:
+        """Fork groups for read-once shared-prefix decode: runs of adjacent
+        sequences (in the given order) whose first physical block is the same
+        -- forks of one prompt (page 2 §2.1, best-of-N) -- and, per group, the
+        tokens at the front that every member holds in the same physical
+        blocks and that precede every member's first query: whole blocks
+        only, at most (L - r + 1) // block_size of them for a member with L
+        tokens and a query run of r. A group of one gets prefix 0.
+        Returns (group_start [G + 1], prefix_len [G])."""
+        bs = self.block_size
+        seqs = [int(s) for s in seqs]
+        rs = [1] * len(seqs) if q_lens is None else [int(r) for r in q_lens]
+        for s, r in zip(seqs, rs):
+            self._get(s)
+            if not 1 <= r <= self.lens[s]:
+                raise ValueError(f"sequence {s}: query run {r}")
+        starts, prefixes = [], []
+        i = 0
+        while i < len(seqs):
+            first = self.tables[seqs[i]]
+            j = i + 1
+            while (j < len(seqs) and first and self.tables[seqs[j]]
+                   and self.tables[seqs[j]][0] == first[0]):
+                j += 1
+            k = 0
+            if j - i > 1:
+                members = range(i, j)
+                # longest run of leading entries equal in every member's table
+                k = min(len(self.tables[seqs[m]]) for m in members)
+                for m in members:
+                    t = self.tables[seqs[m]]
+                    c = 0
+                    while c < k and t[c] == first[c]:
+                        c += 1
+                    k = c
+                # no prefix token may reach a member's first query
+                k = min([k] + [(self.lens[seqs[m]] - rs[m] + 1) // bs for m in members])
+            starts.append(i)
+            prefixes.append(k * bs)
+            i = j
+        starts.append(len(seqs))
+        return starts, prefixes
+

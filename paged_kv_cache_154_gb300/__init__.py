@@ -59,6 +59,12 @@ _SIGS = {
                             _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                             _I32, ctypes.c_float, _I32, _I32, _P], ctypes.c_int),
     "pa_device_error": ([_P, _P], ctypes.c_int),
+    "pa_pool_prefix_groups": ([_P, _P, _I32, _P, _P, _P, _P], ctypes.c_int),
+    "pa_decode_shared_prefix_workspace_size": ([_I32] * 11, _SZ),
+    "pa_decode_shared_prefix": ([_P, ctypes.c_int, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P,
+                                 _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                                 ctypes.c_float, _I32, _P, _P, _I32, _I32, _I32, _P, _SZ, _P],
+                                ctypes.c_int),
 }
 
 
@@ -175,6 +181,21 @@ class Pool:
         _check(lib().pa_pool_refcount(self._h, block, ctypes.addressof(out)))
         return out.value
 
+    def prefix_groups(self, seqs: Sequence[int],
+                      q_lens: Optional[Sequence[int]] = None) -> Tuple[np.ndarray, np.ndarray]:
+        """pa_pool_prefix_groups: (group_start [G + 1], prefix_len [G]) for the
+        sequences in this order (adjacent forks of one prompt form a group)."""
+        s = np.ascontiguousarray(seqs, dtype=np.int32)
+        ql = None if q_lens is None else np.ascontiguousarray(q_lens, dtype=np.int32)
+        gs = np.zeros(len(s) + 1, np.int32)
+        pl = np.zeros(max(1, len(s)), np.int32)
+        ng = _I32()
+        _check(lib().pa_pool_prefix_groups(self._h, s.ctypes.data, len(s),
+                                           None if ql is None else ql.ctypes.data,
+                                           gs.ctypes.data, pl.ctypes.data,
+                                           ctypes.addressof(ng)))
+        return gs[:ng.value + 1].copy(), pl[:ng.value].copy()
+
 
 # ---------------------------------------------------------------------------
 # device operations (torch tensors in, nothing allocated)
@@ -230,6 +251,36 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len
                            k_cache.shape[1], q.shape[2], k_cache.shape[2], nb, float(scale),
                            int(max_context_len), int(partition_size), _ptr(workspace), ws_bytes,
                            _stream(stream)))
+
+
+def decode_shared_prefix_workspace_size(num_seqs: int, num_q_tokens: int, num_heads: int,
+                                        num_kv_heads: int, head_dim: int, max_q_len: int,
+                                        max_context_len: int, num_groups: int,
+                                        max_group_q_len: int, max_prefix_len: int,
+                                        max_blocks_per_seq: int) -> int:
+    return int(lib().pa_decode_shared_prefix_workspace_size(
+        num_seqs, num_q_tokens, num_heads, num_kv_heads, head_dim, max_q_len, max_context_len,
+        num_groups, max_group_q_len, max_prefix_len, max_blocks_per_seq))
+
+
+def decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
+                         max_context_len: int, scale: float, group_start, prefix_len,
+                         max_group_q_len: int, max_prefix_len: int, query_start_loc=None,
+                         max_q_len: int = 1, num_blocks=None, workspace=None,
+                         stream=None) -> None:
+    """pa_decode_shared_prefix; group_start / prefix_len: device int32 (see
+    Pool.prefix_groups); other arguments as decode()."""
+    num_seqs = int(context_lens.shape[0])
+    nb = k_cache.shape[0] if num_blocks is None else num_blocks
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_shared_prefix(
+        _ptr(out), _dtype_code(out), _ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache),
+        _dtype_code(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        _ptr(query_start_loc), num_seqs, int(q.shape[0]),
+        max_q_len if query_start_loc is not None else 1, q.shape[1], k_cache.shape[1],
+        q.shape[2], k_cache.shape[2], nb, float(scale), int(max_context_len), _ptr(group_start),
+        _ptr(prefix_len), int(prefix_len.shape[0]), int(max_group_q_len), int(max_prefix_len),
+        _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 NO_ALLOC_WORKSPACE_BYTES = 16 << 20

@@ -50,7 +50,22 @@ struct Params {
     int slot_bytes;
     float scale_log2;              // softmax scale * log2(e)
     int out_f32;
+    const int32_t* ctx_start;      // may be null; else sequence s attends tokens [ctx_start[s], L)
+                                   // (a multiple of 16)
+    float* lse_out;                // may be null; else [num_q_tokens][num_heads] base-2 log-sum-exp
+                                   // of each output row, in scale * log2(e) units
+    int unmasked;                  // 1: every query row sees every key < L (no causal offset)
 };
+
+// First block a sequence attends (0 unless ctx_start is given).
+__device__ __forceinline__ int first_block(const Params& p, int s) {
+    return p.ctx_start ? __ldg(p.ctx_start + s) / kBS : 0;
+}
+
+// Blocks a sequence attends: from first_block to the last block holding a token.
+__device__ __forceinline__ int blocks_of(const Params& p, int s) {
+    return max(0, (__ldg(p.context_lens + s) + kBS - 1) / kBS - first_block(p, s));
+}
 
 // A partial slot: int32 {seq, kv head, chunk, first token, end token, 0, 0, 0},
 // then fp32 m[RT] (base-2 units), l[RT], O[RT][D] (not normalised). Row j of a
@@ -111,7 +126,7 @@ static __device__ void build_prefix(int32_t* cum, uint8_t* chunks, const Params&
     for (int i = a; i < b; ++i) {
         const int c = chunks_of(p, i);
         chunks[i] = (uint8_t)c;
-        local += p.num_kv_heads * c * ((__ldg(p.context_lens + i) + kBS - 1) / kBS);
+        local += p.num_kv_heads * c * blocks_of(p, i);
     }
     const int lane = tid & 31, warp = tid >> 5;
     int32_t x = local;
@@ -136,7 +151,7 @@ static __device__ void build_prefix(int32_t* cum, uint8_t* chunks, const Params&
     int32_t run = x - local + (warp > 0 ? warp_tot[warp - 1] : 0);
     for (int i = a; i < b; ++i) {
         cum[i] = run;
-        run += p.num_kv_heads * chunks[i] * ((__ldg(p.context_lens + i) + kBS - 1) / kBS);
+        run += p.num_kv_heads * chunks[i] * blocks_of(p, i);
     }
     if (tid == nt - 1) cum[n] = run;
     __syncthreads();
@@ -221,8 +236,8 @@ __global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p, int
     const int r = query_run(p.qsl, s, &q0);
     const int G = p.group, RT = p.rows_per_tile;
     if (row >= min(RT, G * r - c * RT)) return;    // before any 64-bit division
-    const int L = __ldg(p.context_lens + s);
-    const int nbs = (L + kBS - 1) / kBS;
+    const int nbs = blocks_of(p, s);
+    if (nbs == 0) return;                          // nothing attended: no output row
     const int64_t B = __ldg(p.cum_out + p.num_seqs);
     const int64_t W = p.workers;
     const int64_t fa = __ldg(p.cum_out + s) + (int64_t)(g * C + c) * nbs;
@@ -286,6 +301,8 @@ __global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p, int
     const int64_t base =
         ((int64_t)(q0 + grow / G) * p.num_heads + g * G + grow % G) * D + lane * EPL;
     const float inv = 1.f / den;
+    if (p.lse_out && lane == 0)
+        p.lse_out[(int64_t)(q0 + grow / G) * p.num_heads + g * G + grow % G] = M + log2f(den);
     if constexpr (EPL == 4) {
         if (p.out_f32) {
             *reinterpret_cast<float4*>(static_cast<float*>(p.out) + base) =

@@ -203,19 +203,19 @@ extern "C" size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_token
     return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float));
 }
 
-extern "C" pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
-                               const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
-                               const float* k_scale, const float* v_scale, const int8_t* k_zp,
-                               const int8_t* v_zp, const int32_t* block_tables,
-                               int32_t max_blocks_per_seq, const int32_t* context_lens,
-                               const int32_t* query_start_loc, int32_t num_seqs,
-                               int32_t num_q_tokens, int32_t max_q_len, int32_t num_heads,
-                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                               int32_t num_blocks, float scale, int32_t max_context_len,
-                               int32_t partition_size, void* workspace,
-                               size_t workspace_bytes, void* stream) {
-    if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs < 0");
-    if (num_seqs == 0) return PA_OK;
+namespace pa {
+
+// Host-side checks shared by the decode entry points; may rewrite max_q_len
+// (1 without query_start_loc).
+pa_status check_decode_args(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+                            const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+                            const float* k_scale, const float* v_scale, const int8_t* k_zp,
+                            const int8_t* v_zp, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* context_lens,
+                            const int32_t* query_start_loc, int32_t num_seqs,
+                            int32_t num_q_tokens, int32_t* max_q_len, int32_t num_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t num_blocks, int32_t max_context_len) {
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return fail(PA_ERR_INVALID_ARG, "NULL pointer");
     if (pa_status s = check_shape(num_kv_heads, head_dim, block_size)) return s;
@@ -234,26 +234,80 @@ extern "C" pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_
     if (!query_start_loc) {
         if (num_q_tokens != num_seqs)
             return fail(PA_ERR_INVALID_ARG, "without query_start_loc num_q_tokens must equal num_seqs");
-        max_q_len = 1;
+        *max_q_len = 1;
     }
-    if (max_q_len < 1 || num_q_tokens < num_seqs)
-        return fail(PA_ERR_INVALID_ARG, "max_q_len %d / num_q_tokens %d", max_q_len, num_q_tokens);
-    if (max_context_len < max_q_len)
+    if (*max_q_len < 1 || num_q_tokens < num_seqs)
+        return fail(PA_ERR_INVALID_ARG, "max_q_len %d / num_q_tokens %d", *max_q_len, num_q_tokens);
+    if (max_context_len < *max_q_len)
         return fail(PA_ERR_INVALID_ARG, "max_context_len %d < max_q_len %d", max_context_len,
-                    max_q_len);
+                    *max_q_len);
     if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks %d", num_blocks);
     if ((int64_t)max_blocks_per_seq * block_size < max_context_len)
         return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq %d cannot hold %d tokens",
                     max_blocks_per_seq, max_context_len);
+    if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16)
+        return fail(PA_ERR_INVALID_ARG, "k_cache and v_cache must be 16-byte aligned");
+    if (((uintptr_t)q | (uintptr_t)out) % 16)
+        return fail(PA_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+    return PA_OK;
+}
+
+// PA_VALIDATE=1: context lengths, query runs and block-table entries of every
+// sequence, read back from the device.
+pa_status validate_decode_arrays(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, const int32_t* query_start_loc,
+                                 int32_t num_seqs, int32_t num_q_tokens, int32_t max_q_len,
+                                 int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                                 cudaStream_t st) {
+    std::vector<int32_t> lens, bt, qsl;
+    if (pa_status s = to_host(lens, context_lens, (size_t)num_seqs, st)) return s;
+    if (pa_status s = to_host(bt, block_tables, (size_t)num_seqs * max_blocks_per_seq, st))
+        return s;
+    if (query_start_loc)
+        if (pa_status s = to_host(qsl, query_start_loc, (size_t)num_seqs + 1, st)) return s;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int32_t r = query_start_loc ? qsl[s + 1] - qsl[s] : 1;
+        int32_t L = lens[s];
+        if (query_start_loc && (qsl[s] < 0 || qsl[s + 1] > num_q_tokens))
+            return fail(PA_ERR_VALIDATION, "query_start_loc of sequence %d out of range", s);
+        if (r < 1 || r > max_q_len || L < r || L > max_context_len)
+            return fail(PA_ERR_VALIDATION, "sequence %d: context_len %d, query run %d", s, L, r);
+        for (int32_t b = 0; b < (L + block_size - 1) / block_size; ++b) {
+            int32_t e = bt[(size_t)s * max_blocks_per_seq + b];
+            if (e < 0 || e >= num_blocks)
+                return fail(PA_ERR_VALIDATION, "block_tables[%d][%d] = %d outside [0,%d)", s, b,
+                            e, num_blocks);
+        }
+    }
+    return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+                               const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+                               const float* k_scale, const float* v_scale, const int8_t* k_zp,
+                               const int8_t* v_zp, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               const int32_t* query_start_loc, int32_t num_seqs,
+                               int32_t num_q_tokens, int32_t max_q_len, int32_t num_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, float scale, int32_t max_context_len,
+                               int32_t partition_size, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs < 0");
+    if (num_seqs == 0) return PA_OK;
+    if (pa_status s = pa::check_decode_args(
+            out, out_dtype, q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, k_zp, v_zp,
+            block_tables, max_blocks_per_seq, context_lens, query_start_loc, num_seqs,
+            num_q_tokens, &max_q_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+            max_context_len))
+        return s;
     const int32_t P = partition_size;
     if (P < 0 || P % block_size != 0)
         return fail(PA_ERR_INVALID_ARG, "partition_size %d is not a multiple of %d", P, block_size);
     const int64_t parts = P > 0 ? (max_context_len + (int64_t)P - 1) / P : 1;
     if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "too many partitions (%lld)", (long long)parts);
-    if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16)
-        return fail(PA_ERR_INVALID_ARG, "k_cache and v_cache must be 16-byte aligned");
-    if (((uintptr_t)q | (uintptr_t)out) % 16)
-        return fail(PA_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
     const size_t need = pa_decode_workspace_size(num_seqs, num_q_tokens, num_heads, num_kv_heads,
                                                  head_dim, max_q_len, max_context_len,
                                                  partition_size);
@@ -261,28 +315,12 @@ extern "C" pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_
         return fail(PA_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
                     need, workspace_bytes);
     cudaStream_t st = (cudaStream_t)stream;
-    if (pa::validate_enabled()) {
-        std::vector<int32_t> lens, bt, qsl;
-        if (pa_status s = to_host(lens, context_lens, (size_t)num_seqs, st)) return s;
-        if (pa_status s = to_host(bt, block_tables, (size_t)num_seqs * max_blocks_per_seq, st))
+    if (pa::validate_enabled())
+        if (pa_status s = pa::validate_decode_arrays(block_tables, max_blocks_per_seq,
+                                                     context_lens, query_start_loc, num_seqs,
+                                                     num_q_tokens, max_q_len, block_size,
+                                                     num_blocks, max_context_len, st))
             return s;
-        if (query_start_loc)
-            if (pa_status s = to_host(qsl, query_start_loc, (size_t)num_seqs + 1, st)) return s;
-        for (int32_t s = 0; s < num_seqs; ++s) {
-            int32_t r = query_start_loc ? qsl[s + 1] - qsl[s] : 1;
-            int32_t L = lens[s];
-            if (query_start_loc && (qsl[s] < 0 || qsl[s + 1] > num_q_tokens))
-                return fail(PA_ERR_VALIDATION, "query_start_loc of sequence %d out of range", s);
-            if (r < 1 || r > max_q_len || L < r || L > max_context_len)
-                return fail(PA_ERR_VALIDATION, "sequence %d: context_len %d, query run %d", s, L, r);
-            for (int32_t b = 0; b < (L + block_size - 1) / block_size; ++b) {
-                int32_t e = bt[(size_t)s * max_blocks_per_seq + b];
-                if (e < 0 || e >= num_blocks)
-                    return fail(PA_ERR_VALIDATION, "block_tables[%d][%d] = %d outside [0,%d)", s, b,
-                                e, num_blocks);
-            }
-        }
-    }
     pa::DecodeArgs a{};
     a.out = out;
     a.out_dtype = out_dtype;

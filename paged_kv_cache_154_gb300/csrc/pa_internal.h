@@ -25,6 +25,7 @@ enum : unsigned int {
     ERR_WAIT_DRAIN = 1u << 2,   // exit drain gave up on an in-flight copy
     ERR_BAD_BLOCK = 1u << 3,    // a block-table entry outside the pool
     ERR_BAD_SLOT = 1u << 4,     // a slot outside the pool
+    ERR_BAD_GROUP = 1u << 5,    // a shared-prefix group range or prefix length out of bounds
 };
 
 inline int dtype_bytes(pa_dtype t) {
@@ -120,9 +121,29 @@ struct DecodeArgs {
     float* m_part;
     float* l_part;
     void* slots;             // balanced schedule (partition_size == 0)
+    // balanced schedule of a 16-bit cache only (null / 0 otherwise):
+    const int32_t* ctx_start;  // [num_seqs] first attended token, a multiple of 16
+    float* lse_out;            // [num_q_tokens][num_heads] base-2 log-sum-exp per output row
+    int unmasked;              // every query row sees every key < context_len
     cudaStream_t stream;
 };
 pa_status launch_decode(const DecodeArgs& a);
+
+// Host-side argument checks of the decode entry points (capi.cu).
+pa_status check_decode_args(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+                            const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+                            const float* k_scale, const float* v_scale, const int8_t* k_zp,
+                            const int8_t* v_zp, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* context_lens,
+                            const int32_t* query_start_loc, int32_t num_seqs,
+                            int32_t num_q_tokens, int32_t* max_q_len, int32_t num_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t num_blocks, int32_t max_context_len);
+pa_status validate_decode_arrays(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, const int32_t* query_start_loc,
+                                 int32_t num_seqs, int32_t num_q_tokens, int32_t max_q_len,
+                                 int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                                 cudaStream_t st);
 
 // Balanced schedule (partition_size == 0): at most this many worker warps
 // (and partial-slot pairs), and at most this many sequences per call (their

@@ -379,7 +379,8 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         my_row = 0;
         if (f < f1) {
             const Pos q = locate(cum, chunks, n_seqs, hkv, f);
-            int blk = __ldg(p.block_tables + (int64_t)q.s * p.max_blocks + q.b);
+            int blk = __ldg(p.block_tables + (int64_t)q.s * p.max_blocks + first_block(p, q.s) +
+                            q.b);
             if (blk < 0 || blk >= p.num_blocks) {
                 if (p.err) atomicOr(p.err, pa::ERR_BAD_BLOCK);
                 blk = 0;
@@ -401,11 +402,13 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     Pos cur = locate(cum, chunks, n_seqs, hkv, f0);
     WarpAttn<T, D, MT> st;
     uint32_t qreg[MT == 1 ? kKSteps : 1][4];
-    int L = 0, r = 1, q0 = 0, rows = 0, row_off = 0, seg_b0 = cur.b;
+    int L = 0, r = 1, q0 = 0, rows = 0, row_off = 0, seg_b0 = cur.b, sb = 0, last_q = 0;
     bool seg_first = true;
     auto start_segment = [&]() {
         L = __ldg(p.context_lens + cur.s);
         r = query_run(p.qsl, cur.s, &q0);
+        sb = first_block(p, cur.s);
+        last_q = p.unmasked ? L - 1 : L - r;
         row_off = cur.c * RT;
         rows = min(RT, G * r - row_off);
         if constexpr (MT == 1) {
@@ -442,8 +445,10 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
                     if (row >= rows) continue;
                     const int gr = row_off + row;
                     const float inv = 1.f / st.l_run[mt][h];
-                    const int64_t obase =
-                        ((int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G) * D;
+                    const int64_t orow = (int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G;
+                    const int64_t obase = orow * D;
+                    if (p.lse_out && qc == 0)
+                        p.lse_out[orow] = st.m_run[mt][h] + log2f(st.l_run[mt][h]);
 #pragma unroll
                     for (int nt = 0; nt < kNTiles; ++nt) {
                         const float a = st.o[mt][nt][2 * h] * inv;
@@ -462,7 +467,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
                 sl.hdr[0] = cur.s;
                 sl.hdr[1] = cur.g;
                 sl.hdr[2] = cur.c;
-                sl.hdr[3] = seg_b0 * kBS;
+                sl.hdr[3] = (sb + seg_b0) * kBS;
                 sl.hdr[4] = tok_end;
             }
 #pragma unroll
@@ -488,8 +493,9 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     for (int k = 0; k < n; ++k) {
         if (!pa::mbar_wait(bars + 8 * (k % S), (k / S) & 1, p.err, pa::ERR_WAIT_FULL)) break;
         consumed = k + 1;
-        st.template block<Lay::kQPitch>(ring + (k % S) * Lay::kStage, qreg, qtile, cur.b * kBS,
-                                        L - r, row_off, L, G, p.scale_log2, lane);
+        st.template block<Lay::kQPitch>(ring + (k % S) * Lay::kStage, qreg, qtile,
+                                        (sb + cur.b) * kBS, last_q, row_off, L, G, p.scale_log2,
+                                        lane);
         __syncwarp();
         if (issued < n) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -499,7 +505,8 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         ++cur.b;
         const bool seg_done = cur.b == cur.nbs;
         if (seg_done || k == n - 1) {
-            finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1, min(cur.b * kBS, L));
+            finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
+                           min((sb + cur.b) * kBS, L));
             if (k == n - 1) break;
             next_segment(cur, cum, chunks, n_seqs, hkv);
             seg_b0 = 0;
@@ -1008,6 +1015,10 @@ namespace pa {
 pa_status launch_decode_int8(const DecodeArgs& a);
 
 pa_status launch_decode(const DecodeArgs& a) {
+    if ((a.ctx_start || a.lse_out || a.unmasked) && (a.kv_dtype == PA_INT8 || a.partition_size))
+        return fail(PA_ERR_UNSUPPORTED,
+                    "token offsets, log-sum-exp output and unmasked rows need a 16-bit cache and "
+                    "the balanced schedule");
     if (a.kv_dtype == PA_INT8) return launch_decode_int8(a);
     if (a.partition_size > kMaxPartBlocks * kBS)
         return fail(PA_ERR_UNSUPPORTED, "partition_size %d > %d", a.partition_size,
@@ -1067,6 +1078,9 @@ pa_status launch_decode(const DecodeArgs& a) {
     b.slot_bytes = (int)shape.slot_bytes;
     b.scale_log2 = prm.scale_log2;
     b.out_f32 = prm.out_f32;
+    b.ctx_start = a.ctx_start;
+    b.lse_out = a.lse_out;
+    b.unmasked = a.unmasked;
     if (a.kv_dtype == PA_BF16) return launch_dtype<__nv_bfloat16>(a, mt, mk, mv, prm, b);
     return launch_dtype<__half>(a, mt, mk, mv, prm, b);
 }

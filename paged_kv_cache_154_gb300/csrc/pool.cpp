@@ -199,3 +199,52 @@ extern "C" pa_status pa_pool_refcount(pa_pool* p, int32_t block, int32_t* ref) {
     *ref = p->ref[block];
     return PA_OK;
 }
+
+// Groups of adjacent sequences (in the order given) that hold the same first
+// physical block -- forks of one prompt -- and the number of tokens at the
+// front that every member holds in the same physical blocks and that precede
+// every query of the member: whole blocks only, at most (L - r + 1) / 16 of
+// them for a member with L tokens and a query run of r. A group of one gets
+// prefix 0 (reading it once is reading it once per sequence).
+extern "C" pa_status pa_pool_prefix_groups(pa_pool* p, const int32_t* seqs, int32_t n,
+                                           const int32_t* q_lens, int32_t* group_start_out,
+                                           int32_t* prefix_len_out, int32_t* num_groups_out) {
+    if (!p || n < 0 || (n > 0 && (!seqs || !group_start_out || !prefix_len_out)) ||
+        !num_groups_out)
+        return pa::fail(PA_ERR_INVALID_ARG, "bad argument");
+    for (int32_t i = 0; i < n; ++i) {
+        if (pa_status s = check_seq(p, seqs[i])) return s;
+        const int32_t r = q_lens ? q_lens[i] : 1;
+        if (r < 1 || r > p->lens[seqs[i]])
+            return pa::fail(PA_ERR_INVALID_ARG, "sequence %d: query run %d, %d tokens", seqs[i], r,
+                            p->lens[seqs[i]]);
+    }
+    const int32_t bs = p->block_size;
+    int32_t ng = 0, i = 0;
+    while (i < n) {
+        const std::vector<int32_t>& t0 = p->tables[seqs[i]];
+        int32_t j = i + 1;
+        while (j < n && !t0.empty() && !p->tables[seqs[j]].empty() &&
+               p->tables[seqs[j]][0] == t0[0])
+            ++j;
+        int32_t k = 0;
+        if (j - i > 1) {
+            k = (int32_t)t0.size();
+            for (int32_t m = i; m < j; ++m) {
+                const std::vector<int32_t>& t = p->tables[seqs[m]];
+                const int32_t r = q_lens ? q_lens[m] : 1;
+                int32_t c = 0;
+                const int32_t lim = std::min<int32_t>((int32_t)t.size(), k);
+                while (c < lim && t[c] == t0[c]) ++c;
+                k = std::min(c, (p->lens[seqs[m]] - r + 1) / bs);
+            }
+        }
+        group_start_out[ng] = i;
+        prefix_len_out[ng] = k * bs;
+        ++ng;
+        i = j;
+    }
+    if (n > 0) group_start_out[ng] = n;
+    *num_groups_out = ng;
+    return PA_OK;
+}

@@ -19,7 +19,8 @@ from typing import Dict, List, Optional, Sequence
 import numpy as np
 import torch
 
-from . import (BLOCK_SIZE, Pool, append_kv, copy_blocks, decode, decode_workspace_size)
+from . import (BLOCK_SIZE, Pool, append_kv, copy_blocks, decode, decode_shared_prefix,
+               decode_shared_prefix_workspace_size, decode_workspace_size)
 
 KV_TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "int8": torch.int8}
 
@@ -39,6 +40,19 @@ class StepInputs:
     max_context_len: int
     out: torch.Tensor
     workspace: Optional[torch.Tensor]
+    shared: Optional["SharedPrefix"] = None
+
+
+@dataclass
+class SharedPrefix:
+    """Fork groups of a step for read-once shared-prefix decode."""
+    group_start: torch.Tensor         # int32 [G + 1] (device)
+    prefix_len: torch.Tensor          # int32 [G] (device)
+    group_start_host: np.ndarray
+    prefix_len_host: np.ndarray
+    max_group_q_len: int
+    max_prefix_len: int
+    workspace: torch.Tensor
 
 
 class PagedKVCache:
@@ -109,8 +123,12 @@ class PagedKVCache:
 
     # -- decode step -------------------------------------------------------------
     def prepare_step(self, step_ops, names: Dict, q: torch.Tensor, out_dtype=torch.float32,
-                     partition_size: int = 0, reserve: bool = True) -> StepInputs:
-        """Reserve the step's slots (host) and build its device inputs."""
+                     partition_size: int = 0, reserve: bool = True,
+                     shared_prefix: bool = False) -> StepInputs:
+        """Reserve the step's slots (host) and build its device inputs. With
+        shared_prefix, also the fork groups (adjacent sequences of the step
+        holding the same prompt blocks), so that attend_step reads each
+        group's shared blocks once."""
         slots, pairs, ks, vs = self.reserve(step_ops, names) if reserve else (None, [], [], [])
         seqs = [names[op.seq] for op in step_ops]
         q_lens = [int(op.k.shape[0]) for op in step_ops]
@@ -123,6 +141,18 @@ class PagedKVCache:
         nq = int(qsl[-1])
         ws_bytes = decode_workspace_size(len(seqs), nq, q.shape[1], self.num_kv_heads, q.shape[2],
                                          max(q_lens), max(lens), partition_size)
+        shared = None
+        if shared_prefix:
+            gs, pl = self.pool.prefix_groups(seqs, q_lens)
+            gq = [int(qsl[gs[g + 1]] - qsl[gs[g]]) for g in range(len(pl))]
+            sp_bytes = decode_shared_prefix_workspace_size(
+                len(seqs), nq, q.shape[1], self.num_kv_heads, q.shape[2], max(q_lens), max(lens),
+                len(pl), max(gq), int(pl.max()), max_blocks)
+            shared = SharedPrefix(
+                group_start=torch.from_numpy(gs).to(dev), prefix_len=torch.from_numpy(pl).to(dev),
+                group_start_host=gs, prefix_len_host=pl, max_group_q_len=max(gq),
+                max_prefix_len=int(pl.max()),
+                workspace=torch.empty(sp_bytes, dtype=torch.uint8, device=dev))
         return StepInputs(
             key=torch.cat(ks).to(dev), value=torch.cat(vs).to(dev),
             slots=torch.from_numpy(np.ascontiguousarray(slots)).to(dev),
@@ -134,7 +164,8 @@ class PagedKVCache:
             max_q_len=max(q_lens), max_context_len=max(lens),
             out=torch.empty((nq, q.shape[1], q.shape[2]), dtype=out_dtype, device=dev),
             workspace=(torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-                       if ws_bytes else None))
+                       if ws_bytes else None),
+            shared=shared)
 
     def write_step(self, si: StepInputs) -> None:
         """The step's cache writes: copy-on-write block copies, then the append."""
@@ -146,6 +177,13 @@ class PagedKVCache:
 
     def attend_step(self, si: StepInputs, scale: float, partition_size: int = 0) -> torch.Tensor:
         """The step's attention over the cache (decode kernel + partial merge)."""
+        if si.shared is not None:
+            sp = si.shared
+            decode_shared_prefix(si.out, si.q, self.k, self.v, si.block_tables, si.context_lens,
+                                 si.max_context_len, scale, sp.group_start, sp.prefix_len,
+                                 sp.max_group_q_len, sp.max_prefix_len, si.query_start_loc,
+                                 si.max_q_len, self.num_blocks, sp.workspace)
+            return si.out
         decode(si.out, si.q, self.k, self.v, si.block_tables, si.context_lens,
                si.max_context_len, scale, si.query_start_loc, si.max_q_len, self.num_blocks,
                self.k_scale, self.v_scale, self.k_zp, self.v_zp, partition_size,

@@ -22,7 +22,8 @@ def half_ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
     return np.exp2(np.floor(np.log2(ax)) - mant)
 
 
-def run_both(wl, partition_size=0, out_dtype=torch.float32, oracle_run=None):
+def run_both(wl, partition_size=0, out_dtype=torch.float32, oracle_run=None,
+             shared_prefix=False):
     ref = oracle_run or oracle.run(wl, threads=THREADS, canary_blocks=W.CANARY_BLOCKS,
                                    canary_byte=W.CANARY_BYTE)
     cache = PagedKVCache(wl.num_blocks, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
@@ -33,7 +34,8 @@ def run_both(wl, partition_size=0, out_dtype=torch.float32, oracle_run=None):
         slots, pairs = cache.run_phase(ops, names)
         assert np.array_equal(slots, oslots)
         assert pairs == [tuple(p) for p in opairs]
-    si = cache.prepare_step(wl.step, names, wl.q, out_dtype, partition_size)
+    si = cache.prepare_step(wl.step, names, wl.q, out_dtype, partition_size,
+                            shared_prefix=shared_prefix)
     assert np.array_equal(si.slots.cpu().numpy(), ref.step_slots)
     got_pairs = [] if si.pairs is None else [tuple(p) for p in si.pairs.cpu().tolist()]
     assert got_pairs == [tuple(p) for p in ref.step_pairs]

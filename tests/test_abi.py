@@ -155,3 +155,45 @@ def test_workspace_size():
     assert pa.decode_workspace_size(256, 400, 32, 1, 128, 5, 16384, 0) == \
         1280 + 2 * 2048 * slot32
     assert pa.decode_workspace_size(1, 1, 8, 3, 64, 1, 17, 0) == 0      # heads not a multiple
+
+
+def test_prefix_groups_match_model_on_fork_trees():
+    """pa_pool_prefix_groups against the allocator model on random fork
+    trees (forks listed next to their prompt), with query runs of 1-5."""
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        order = rng.permutation(400).astype(np.int32)
+        c = pa.Pool(400, 16, order)
+        m = BlockPool(400, 16, order)
+        seqs = []
+        for g in range(int(rng.integers(1, 5))):
+            root = c.seq_create()
+            assert m.create() == root
+            n = int(rng.integers(1, 120))
+            c.seq_append_slots(root, n)
+            m.append_slots(root, n)
+            members = [root]
+            for _ in range(int(rng.integers(0, 5))):
+                parent = members[int(rng.integers(len(members)))]
+                child = c.seq_fork(parent)
+                assert m.fork(parent) == child
+                members.append(child)
+            for s in members:
+                k = int(rng.integers(0, 40))
+                c.seq_append_slots(s, k)
+                m.append_slots(s, k)
+            seqs += members
+        q_lens = [int(rng.integers(1, min(5, m.lens[s]) + 1)) for s in seqs]
+        gs, pl = c.prefix_groups(seqs, q_lens)
+        mgs, mpl = m.prefix_groups(seqs, q_lens)
+        assert gs.tolist() == mgs and pl.tolist() == mpl
+        # what a prefix promises: shared physical blocks, before every query
+        for g in range(len(pl)):
+            members = seqs[gs[g]:gs[g + 1]]
+            nb = pl[g] // 16
+            assert pl[g] % 16 == 0
+            for i, s in zip(range(gs[g], gs[g + 1]), members):
+                assert m.block_table(s)[:nb] == m.block_table(members[0])[:nb]
+                assert pl[g] <= m.lens[s] - q_lens[i] + 1
+    with pytest.raises(pa.PAError):
+        c.prefix_groups([9999])

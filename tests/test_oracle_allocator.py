@@ -183,3 +183,26 @@ def test_copy_blocks_copies_whole_blocks_only():
         assert np.array_equal(a[4], b[1]) and np.array_equal(a[0], b[2])
         for blk in (1, 2, 3, 5):
             assert np.array_equal(a[blk], b[blk])
+
+
+def test_prefix_groups_model_is_maximal_and_sound():
+    """The model's prefix is the longest whole-block prefix that every fork
+    holds in the same physical blocks and that precedes every query: one
+    block more breaks one of those conditions."""
+    pool = BlockPool(200, 16)
+    root = pool.create()
+    pool.append_slots(root, 70)                  # 4 full blocks + 6 tokens
+    a = pool.fork(root)
+    b = pool.fork(root)
+    pool.append_slots(a, 3)                      # CoW of the shared tail block
+    pool.append_slots(b, 30)
+    lone = pool.create()
+    pool.append_slots(lone, 40)
+    gs, pl = pool.prefix_groups([root, a, b, lone])
+    assert gs == [0, 3, 4] and pl == [64, 0]     # 4 shared full blocks; a group of one gets 0
+    # a query run that reaches into the 4th block caps the prefix at 3 blocks
+    gs, pl = pool.prefix_groups([root, a, b], q_lens=[1, 1, 70 + 30 - 63 + 1])
+    assert pl == [48]
+    # forks that are not adjacent form separate groups
+    gs, pl = pool.prefix_groups([root, lone, a])
+    assert gs == [0, 1, 2, 3] and pl == [0, 0, 0]

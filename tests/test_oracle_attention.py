@@ -226,3 +226,30 @@ def test_int8_cache_attends_over_dequantised_values():
     for (K, V), (K0, V0) in zip(kv_list, W.contiguous_kv(wl)):
         err = (K.double() - K0.double()).abs().max().item()
         assert err < 0.02
+
+
+@pytest.mark.parametrize("step_q_max", [1, 4])
+def test_shared_prefix_cascade_equals_full_attention(step_q_max):
+    """Read-once decode for forks: attending a group's shared prefix [0, P)
+    with all of the group's rows, then each fork's own tokens [P, L), and
+    merging the two by log-sum-exp gives the unsplit attention (the prefix
+    precedes every query, so the causal bound never cuts it)."""
+    wl = W.best_of_n("bo_cascade", 61, num_groups=3, n_forks=4, prompt_len=70,
+                     shared_extra_max=9, private_max=30, num_heads=8, num_kv_heads=2,
+                     head_dim=64, step_q_max=step_q_max)
+    run = oracle.run(wl)
+    seqs = [run.names[s] for s in wl.decode_seqs]
+    gs, pl = run.pool.prefix_groups(seqs, wl.q_lens)
+    assert len(pl) == 3 and min(pl) >= 64           # every group shares its full prompt blocks
+    qsl = wl.query_start_loc
+    for g in range(len(pl)):
+        a, b = gs[g], gs[g + 1]
+        rows = slice(int(qsl[a]), int(qsl[b]))
+        sub_qsl = qsl[a:b + 1] - qsl[a]
+        args = (run.q64[rows], run.cache, run.block_tables[a:b], run.context_lens[a:b],
+                sub_qsl, wl.num_heads, wl.scale)
+        pre = oracle.attend(*args, 0, pl[g])
+        suf = oracle.attend(*args, pl[g])
+        merged = oracle.lse_merge(np.stack([pre[0], suf[0]]), np.stack([pre[1], suf[1]]),
+                                  np.stack([pre[2], suf[2]]))
+        np.testing.assert_allclose(merged, run.out[rows], rtol=0, atol=1e-12)

@@ -199,7 +199,7 @@ def best_of_n(name: str, seed: int, num_groups: int, n_forks: int,
               prompt_len: int, shared_extra_max: int, private_max: int,
               num_heads: int, num_kv_heads: int, head_dim: int,
               kv_dtype: str = "bf16", pool_factor: float = 1.2,
-              partition_size: int = 512) -> Workload:
+              partition_size: int = 512, step_q_max: int = 1) -> Workload:
     """Best-of-N groups sharing a prompt by refcount (copy-on-write).
 
     Each group has a parent holding `prompt_len + s` tokens, s in
@@ -208,7 +208,8 @@ def best_of_n(name: str, seed: int, num_groups: int, n_forks: int,
     decoded, so every child's first append into the shared tail copies it.
     Child 0 has no private tokens (its step append copies the tail); the
     others first append U[0, private_max] private tokens. The step appends one
-    token to every child and decodes all children.
+    token to every child (or, with step_q_max > 1, a verify run of U[1,
+    step_q_max] tokens) and decodes all children.
     """
     rng = np.random.default_rng(seed)
     vals = _Values(seed)
@@ -216,12 +217,14 @@ def best_of_n(name: str, seed: int, num_groups: int, n_forks: int,
     s_extra = rng.integers(1, shared_extra_max + 1, size=num_groups)
     private = rng.integers(0, private_max + 1, size=(num_groups, n_forks))
     private[:, 0] = 0
+    step_r = (np.ones((num_groups, n_forks), np.int64) if step_q_max == 1 else
+              rng.integers(1, step_q_max + 1, size=(num_groups, n_forks)))
     need = 0
     for g in range(num_groups):
         plen = prompt_len + int(s_extra[g])
         need += (plen + BLOCK_SIZE - 1) // BLOCK_SIZE
         for i in range(n_forks):
-            tail = int(s_extra[g]) + int(private[g, i]) + 1
+            tail = int(s_extra[g]) + int(private[g, i]) + int(step_r[g, i])
             need += (tail + BLOCK_SIZE - 1) // BLOCK_SIZE
     num_blocks = int(math.ceil(pool_factor * need))
     free_order = _free_order(rng, num_blocks)
@@ -251,12 +254,12 @@ def best_of_n(name: str, seed: int, num_groups: int, n_forks: int,
             if private[g, i] > 0:
                 k, v = kv(int(private[g, i]))
                 phase1.append(Append(child, k, v))
-            children.append(child)
-            context_lens.append(plen + int(private[g, i]) + 1)
-    for child in children:
-        k, v = kv(1)
+            children.append((child, int(step_r[g, i])))
+            context_lens.append(plen + int(private[g, i]) + int(step_r[g, i]))
+    for child, r in children:
+        k, v = kv(r)
         step.append(Append(child, k, v))
-    q = vals.normal((len(children), num_heads, head_dim), src)
+    q = vals.normal((int(step_r.sum()), num_heads, head_dim), src)
     return Workload(name=name, seed=seed, num_heads=num_heads,
                     num_kv_heads=num_kv_heads, head_dim=head_dim,
                     kv_dtype=kv_dtype, src_dtype=src, q_dtype=src,
