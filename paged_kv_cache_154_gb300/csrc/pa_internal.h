@@ -152,26 +152,35 @@ constexpr int kBalancedMaxWorkers = 2048;
 constexpr int kBalancedMaxSeqs = 8192;
 
 struct BalancedShape {
-    int rows_per_tile;       // query rows per worker tile (16 or 32)
+    int rows_per_tile;       // query rows per worker tile of this kernel family
     int64_t max_chunks;      // row tiles per (sequence, kv head), at most
-    int64_t workers;         // cap on worker warps
+    int64_t workers;         // cap on workers (partial-slot pairs)
     int64_t cum_bytes;       // workspace prefix sums, 256-byte aligned
     int64_t slot_bytes;      // one partial slot
     int64_t virtual_blocks;  // upper bound of the schedule's work units
     int64_t workspace_bytes;
 };
 
+// Query rows per tile: 16 while a KV head has at most 16 rows (G q heads x
+// the longest query run), else 64 for the 16-bit kernels (four warps of 16
+// rows share each block) and 32 for the INT8 kernel.
+inline int tile_rows(int64_t rows, bool int8) { return rows <= 16 ? 16 : (int8 ? 32 : 64); }
+
+// The workspace is sized for either kernel family: the worker cap from the
+// smaller tile (more work units) and the slot from the larger one.
 inline BalancedShape balanced_shape(int num_seqs, int num_heads, int num_kv_heads,
-                                    int head_dim, int max_q_len, int max_context_len) {
+                                    int head_dim, int max_q_len, int max_context_len,
+                                    bool int8 = false) {
     BalancedShape b{};
     const int64_t rows = (int64_t)(num_heads / num_kv_heads) * max_q_len;
-    b.rows_per_tile = rows <= 16 ? 16 : 32;
+    b.rows_per_tile = tile_rows(rows, int8);
     b.max_chunks = (rows + b.rows_per_tile - 1) / b.rows_per_tile;
-    b.virtual_blocks =
-        (int64_t)num_seqs * num_kv_heads * b.max_chunks * ((max_context_len + 15) / 16);
+    const int64_t small = tile_rows(rows, true), large = tile_rows(rows, false);
+    b.virtual_blocks = (int64_t)num_seqs * num_kv_heads * ((rows + small - 1) / small) *
+                       ((max_context_len + 15) / 16);
     b.workers = b.virtual_blocks < kBalancedMaxWorkers ? b.virtual_blocks : kBalancedMaxWorkers;
     b.cum_bytes = ((int64_t)4 * (num_seqs + 1) + 255) / 256 * 256;
-    b.slot_bytes = (32 + 4 * (int64_t)b.rows_per_tile * (head_dim + 2) + 15) / 16 * 16;
+    b.slot_bytes = (32 + 4 * large * (head_dim + 2) + 15) / 16 * 16;
     b.workspace_bytes = b.cum_bytes + 2 * b.workers * b.slot_bytes;
     return b;
 }
@@ -182,7 +191,8 @@ inline pa_status balanced_check(const DecodeArgs& a) {
         return fail(PA_ERR_UNSUPPORTED, "more than %d sequences in one call with partition_size 0",
                     kBalancedMaxSeqs);
     const BalancedShape b = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim,
-                                           a.max_q_len, a.max_context_len);
+                                           a.max_q_len, a.max_context_len,
+                                           a.kv_dtype == PA_INT8);
     if (b.max_chunks > 255 || b.virtual_blocks > 0x7fffffffll)
         return fail(PA_ERR_UNSUPPORTED, "decode call too large for one balanced launch");
     return PA_OK;

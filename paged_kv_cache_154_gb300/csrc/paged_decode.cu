@@ -136,11 +136,12 @@ struct WarpAttn {
     }
 
     // One 16-token block staged at kb (K tile) and kb + tile (V tile).
-    //   qreg   A fragments of Q (MT == 1), or qsm: smem Q tile base (MT > 1)
+    //   qreg   A fragments of Q (MT == 1), or qsm: smem Q tile base (MT > 1 or
+    //          QSMEM; rows at a pitch of QPITCH bytes)
     //   tok0   absolute position of the block's first token
     //   last_q L - r: query row i sees keys <= L - r + i (row i = row / G)
     //   row_off index of this tile's first query row among the KV head's rows
-    template <int QPITCH>
+    template <int QPITCH, bool QSMEM = false>
     __device__ __forceinline__ void block(uint32_t kb, const uint32_t (*qreg)[4], uint32_t qsm,
                                           int tok0, int last_q, int row_off, int L, int G,
                                           float scale_log2, int lane) {
@@ -166,7 +167,7 @@ struct WarpAttn {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
                 uint32_t a[4];
-                if constexpr (MT == 1) {
+                if constexpr (MT == 1 && !QSMEM) {
                     a[0] = qreg[ks][0];
                     a[1] = qreg[ks][1];
                     a[2] = qreg[ks][2];
@@ -517,6 +518,239 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     // drain: no copy of this warp may still be in flight when it exits
     for (int k = consumed; k < issued; ++k)
         if (!pa::mbar_wait(bars + 8 * (k % S), (k / S) & 1, p.err, pa::ERR_WAIT_DRAIN)) break;
+}
+
+// ---------------------------------------------------------------------------
+// Balanced schedule with 64-row tiles (more than 16 query rows per KV head:
+// large GQA groups with verify runs, MQA, the prefix phase of shared-prefix
+// decode). One CTA per share: warp 0 streams the K/V tiles of the share's
+// blocks through a ring the CTA shares, and warp w computes tile rows
+// 16w .. 16w + 15 against every block, so each block is read once for up to
+// 64 rows. A stage is refilled when all four warps have released it (an
+// mbarrier with four arrivals); warps with no rows in a segment still wait
+// for every block and release it, which keeps them in step with the ring.
+// ---------------------------------------------------------------------------
+
+constexpr int kRowsTile = 64;
+constexpr int kRowsStages = 4;   // 4 CTAs of ~52 KB shared memory per SM
+
+template <int D, int S>
+struct RowsLayout {
+    static constexpr int kStage = 2 * kBS * D * 2;
+    static constexpr int kRing = S * kStage;
+    static constexpr int kQPitch = D * 2 + 16;          // padded: conflict-free ldmatrix
+    static constexpr int kQTile = 16 * kQPitch;         // one warp's 16 query rows
+    __host__ __device__ static int smem_bytes(int num_seqs) {
+        return pa::sched::header_bytes(num_seqs, S) + kRing + kWorkerWarps * kQTile + 1024;
+    }
+};
+
+template <typename T, int D, int S>
+__global__ void __launch_bounds__(kWorkerWarps * 32, 4)
+    paged_decode_rows_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                             const __grid_constant__ CUtensorMap tmap_v,
+                             const pa::sched::Params p) {
+    using namespace pa::sched;
+    using Lay = RowsLayout<D, S>;
+    using PK = Pack<T>;
+    constexpr int kKSteps = D / 16;
+    constexpr int kNTiles = D / 8;
+    constexpr int RT = kRowsTile;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = pa::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const smem = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hkv = p.num_kv_heads, G = p.group, n_seqs = p.num_seqs;
+    int32_t* const cum = reinterpret_cast<int32_t*>(smem + kWorkerWarps * S * 8);
+    uint8_t* const chunks = reinterpret_cast<uint8_t*>(cum + n_seqs + 1);
+    const uint32_t full = base, empty = base + 8 * S;
+    const uint32_t ring = base + header_bytes(n_seqs, S);   // 1024-aligned
+    const uint32_t qtile = ring + Lay::kRing + warp * Lay::kQTile;
+
+    build_prefix(cum, chunks, p);
+    const int64_t B = cum[n_seqs];
+    const int64_t wid = blockIdx.x;                          // one share per CTA
+    const int64_t f0 = share_start(wid, B, p.workers);
+    const int64_t f1 = share_start(wid + 1, B, p.workers);
+    const int n = (int)(f1 - f0);
+    if (n <= 0) return;                                      // uniform over the CTA
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            pa::mbar_init(full + 8 * i, 1);
+            pa::mbar_init(empty + 8 * i, kWorkerWarps);
+        }
+        pa::fence_barrier_init();
+        pa::prefetch_tensormap(&tmap_k);
+        pa::prefetch_tensormap(&tmap_v);
+    }
+    __syncthreads();
+
+    // Producer (warp 0): each lane keeps the TMA row of virtual block win +
+    // lane and whether that block is read by one row chunk only (then it is
+    // loaded with an evict-first hint; blocks that further chunks read again
+    // stay at normal priority).
+    uint64_t pol_once = 0, pol_again = 0;
+    if (warp == 0 && lane == 0) {
+        pol_once = pa::policy_evict_first();
+        pol_again = pa::policy_evict_normal();
+    }
+    int win = -32, my_row = 0, my_once = 1;
+    auto refresh = [&](int wbase) {
+        win = wbase;
+        const int64_t f = f0 + wbase + lane;
+        my_row = 0;
+        my_once = 1;
+        if (f < f1) {
+            const Pos q = locate(cum, chunks, n_seqs, hkv, f);
+            int blk = __ldg(p.block_tables + (int64_t)q.s * p.max_blocks + first_block(p, q.s) +
+                            q.b);
+            if (blk < 0 || blk >= p.num_blocks) {
+                if (p.err) atomicOr(p.err, pa::ERR_BAD_BLOCK);
+                blk = 0;
+            }
+            my_row = (blk * hkv + q.g) * kBS;
+            my_once = q.C == 1;
+        }
+    };
+    auto issue = [&](int k) {   // warp 0, warp-uniform
+        if (k >= win + 32) refresh(k & ~31);
+        const int row = __shfl_sync(0xffffffffu, my_row, k - win);
+        const int once = __shfl_sync(0xffffffffu, my_once, k - win);
+        if (lane == 0)
+            issue_tile<D>(ring + (k % S) * Lay::kStage, full + 8 * (k % S), &tmap_k, &tmap_v, row,
+                          once ? pol_once : pol_again);
+    };
+    int issued = 0, consumed = 0;
+    if (warp == 0)
+        for (; issued < S && issued < n; ++issued) issue(issued);
+
+    Pos cur = locate(cum, chunks, n_seqs, hkv, f0);
+    // Q stays in shared memory (this warp's 16 rows) and is read with ldmatrix
+    // per block: keeping the fragments in registers would cost 32 registers a
+    // thread and one CTA per SM.
+    WarpAttn<T, D, 1> st;
+    int L = 0, r = 1, q0 = 0, rows = 0, row_off = 0, seg_b0 = cur.b, sb = 0, last_q = 0;
+    bool seg_first = true, busy = false;
+    auto start_segment = [&]() {
+        L = __ldg(p.context_lens + cur.s);
+        r = query_run(p.qsl, cur.s, &q0);
+        sb = first_block(p, cur.s);
+        last_q = p.unmasked ? L - 1 : L - r;
+        row_off = cur.c * RT;
+        rows = min(RT, G * r - row_off);
+        busy = 16 * warp < rows;
+        if (busy) {
+            __syncwarp();
+            for (int e = lane; e < 16 * (D / 8); e += 32) {
+                const int row = e / (D / 8), ch = e - row * (D / 8);
+                const int tr = 16 * warp + row;               // tile row
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (tr < rows) {
+                    const int gr = row_off + tr;
+                    const T* src = static_cast<const T*>(p.q) +
+                                   ((int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G) * D;
+                    v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+                }
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                                 qtile + row * Lay::kQPitch + ch * 16),
+                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
+            __syncwarp();
+        }
+        st.reset();
+    };
+    auto finish_segment = [&](bool complete, int slot_idx, int tok_end) {
+        Slot sl(p.slots + (2 * wid + slot_idx) * (int64_t)p.slot_bytes, RT);
+        if (!complete && warp == 0 && lane == 0) {
+            sl.hdr[0] = cur.s;
+            sl.hdr[1] = cur.g;
+            sl.hdr[2] = cur.c;
+            sl.hdr[3] = (sb + seg_b0) * kBS;
+            sl.hdr[4] = tok_end;
+        }
+        if (!busy) return;
+        st.quad_sum();
+        const int quad = lane >> 2, qc = lane & 3;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = 16 * warp + quad + 8 * h;          // tile row
+            if (row >= rows) continue;
+            if (complete) {
+                const int gr = row_off + row;
+                const float inv = 1.f / st.l_run[0][h];
+                const int64_t orow = (int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G;
+                if (p.lse_out && qc == 0) p.lse_out[orow] = st.m_run[0][h] + log2f(st.l_run[0][h]);
+#pragma unroll
+                for (int nt = 0; nt < kNTiles; ++nt) {
+                    const float a = st.o[0][nt][2 * h] * inv;
+                    const float b = st.o[0][nt][2 * h + 1] * inv;
+                    const int64_t idx = orow * D + nt * 8 + 2 * qc;
+                    if (p.out_f32)
+                        *reinterpret_cast<float2*>(static_cast<float*>(p.out) + idx) =
+                            make_float2(a, b);
+                    else
+                        PK::store2(static_cast<T*>(p.out) + idx, a, b);
+                }
+            } else {
+                if (qc == 0) {
+                    sl.m[row] = st.m_run[0][h];
+                    sl.l[row] = st.l_run[0][h];
+                }
+#pragma unroll
+                for (int nt = 0; nt < kNTiles; ++nt)
+                    *reinterpret_cast<float2*>(sl.o + (int64_t)row * D + nt * 8 + 2 * qc) =
+                        make_float2(st.o[0][nt][2 * h], st.o[0][nt][2 * h + 1]);
+            }
+        }
+    };
+    start_segment();
+
+    for (int k = 0; k < n; ++k) {
+        const int stg = k % S;
+        if (!__all_sync(0xffffffffu,
+                        pa::mbar_wait(full + 8 * stg, (k / S) & 1, p.err, pa::ERR_WAIT_FULL)))
+            break;
+        if (warp == 0) consumed = k + 1;
+        if (busy)
+            st.template block<Lay::kQPitch, true>(ring + stg * Lay::kStage, nullptr, qtile,
+                                                  (sb + cur.b) * kBS, last_q, row_off + 16 * warp,
+                                                  L, G, p.scale_log2, lane);
+        __syncwarp();
+        if (lane == 0) pa::mbar_arrive(empty + 8 * stg);     // this warp is done with the stage
+        // warp 0 refills the stage block k - 1 used once every warp has released it
+        if (warp == 0 && k >= 1 && k - 1 + S < n) {
+            const int kp = k - 1;
+            if (!__all_sync(0xffffffffu, pa::mbar_wait(empty + 8 * (kp % S), (kp / S) & 1, p.err,
+                                                       pa::ERR_WAIT_EMPTY)))
+                break;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(kp + S);
+            ++issued;
+        }
+        ++cur.b;
+        const bool seg_done = cur.b == cur.nbs;
+        if (seg_done || k == n - 1) {
+            finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
+                           min((sb + cur.b) * kBS, L));
+            if (k == n - 1) break;
+            next_segment(cur, cum, chunks, n_seqs, hkv);
+            seg_b0 = 0;
+            seg_first = false;
+            start_segment();
+        }
+    }
+    // no copy may still be in flight when the CTA exits (this wait ignores the
+    // abort bits: it ends when the copy lands or after its own time limit)
+    if (warp == 0 && lane == 0)
+        for (int k = consumed; k < issued; ++k)
+            if (!pa::mbar_wait(full + 8 * (k % S), (k / S) & 1, nullptr, 0)) {
+                if (p.err) atomicOr(p.err, pa::ERR_WAIT_DRAIN);
+                break;
+            }
 }
 
 // ===========================================================================
@@ -990,16 +1224,58 @@ pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const 
                            "segment reduce launch");
 }
 
+template <typename T, int D>
+pa_status launch_rows(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                      pa::sched::Params prm) {
+    constexpr int S = kRowsStages;
+    using Lay = RowsLayout<D, S>;
+    auto kern = paged_decode_rows_kernel<T, D, S>;
+    const int smem = Lay::smem_bytes(a.num_seqs);
+    static bool attr_set = false;   // per instantiation and process; benign race (idempotent)
+    if (!attr_set) {
+        if (pa_status s = pa::cuda_status(
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Lay::smem_bytes(pa::kBalancedMaxSeqs)),
+                "decode: set shared memory size"))
+            return s;
+        attr_set = true;
+    }
+    int ctas = 0, sms = 0;
+    if (pa_status s = g_residency.get(reinterpret_cast<const void*>(kern), smem, &ctas, &sms))
+        return s;
+    if (ctas < 1) return pa::fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
+    const pa::BalancedShape shape = pa::balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
+                                                       a.head_dim, a.max_q_len, a.max_context_len);
+    const int64_t workers = std::min<int64_t>((int64_t)ctas * sms, shape.workers);
+    prm.workers = (int)workers;
+    if (pa_status s = pa::cuda_status(
+            pa::launch_pdl(kern, dim3((unsigned)workers), dim3(kWorkerWarps * 32), smem, a.stream,
+                           mk, mv, prm),
+            "decode launch"))
+        return s;
+    const int row_slots = (int)std::min<int64_t>(kRowsTile,
+                                                 (int64_t)(a.num_heads / a.num_kv_heads) *
+                                                     a.max_q_len);
+    const int64_t rctas = pa::sched::reduce_ctas(a.num_seqs, a.num_kv_heads, shape.max_chunks,
+                                                 row_slots);
+    if (rctas > 0x7fffffff) return pa::fail(PA_ERR_UNSUPPORTED, "reduce grid too large");
+    return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<T, D>,
+                                          dim3((unsigned)rctas), dim3(128), 0, a.stream, prm,
+                                          (int)shape.max_chunks, row_slots),
+                           "segment reduce launch");
+}
+
 template <typename T>
 pa_status launch_dtype(const pa::DecodeArgs& a, int mt, const CUtensorMap& mk,
                        const CUtensorMap& mv, const DecodeParams& prm,
                        const pa::sched::Params& bprm) {
     if (a.partition_size == 0) {
+        // 16-row tiles: one warp per share; larger tiles: one CTA per share
         if (a.head_dim == 128)
-            return mt == 1 ? launch_balanced<T, 128, 1>(a, mk, mv, bprm)
-                           : launch_balanced<T, 128, 2>(a, mk, mv, bprm);
-        return mt == 1 ? launch_balanced<T, 64, 1>(a, mk, mv, bprm)
-                       : launch_balanced<T, 64, 2>(a, mk, mv, bprm);
+            return bprm.rows_per_tile == 16 ? launch_balanced<T, 128, 1>(a, mk, mv, bprm)
+                                            : launch_rows<T, 128>(a, mk, mv, bprm);
+        return bprm.rows_per_tile == 16 ? launch_balanced<T, 64, 1>(a, mk, mv, bprm)
+                                        : launch_rows<T, 64>(a, mk, mv, bprm);
     }
     if (a.head_dim == 128)
         return mt == 1 ? launch_partitioned<T, 128, 1>(a, mk, mv, prm)
@@ -1030,11 +1306,8 @@ pa_status launch_decode(const DecodeArgs& a) {
         return fail(PA_ERR_UNSUPPORTED,
                     "%lld query rows per KV head (q heads per KV head x max_q_len) > 32 with "
                     "fixed partitions; use partition_size 0", (long long)rows);
-    if (a.partition_size == 0) {
+    if (a.partition_size == 0)
         if (pa_status s = balanced_check(a)) return s;
-        mt = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim, a.max_q_len,
-                            a.max_context_len).rows_per_tile / 16;
-    }
     CUtensorMap mk, mv;
     if (pa_status s = g_maps.get(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim)) return s;
     if (pa_status s = g_maps.get(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim)) return s;

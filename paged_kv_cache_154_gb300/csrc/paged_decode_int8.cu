@@ -698,7 +698,8 @@ pa_status launch8(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensor
         return s;
     if (ctas < 1) return pa::fail(PA_ERR_UNSUPPORTED, "int8 decode kernel does not fit on an SM");
     const pa::BalancedShape shape = pa::balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
-                                                       a.head_dim, a.max_q_len, a.max_context_len);
+                                                       a.head_dim, a.max_q_len, a.max_context_len,
+                                                       true);
     // one share per CTA, every CTA resident at once
     const int64_t workers = std::min<int64_t>((int64_t)ctas * sms, shape.workers);
     prm.workers = (int)workers;
@@ -739,7 +740,7 @@ pa_status launch_decode_int8(const DecodeArgs& a) {
     if (((uintptr_t)a.k_scale | (uintptr_t)a.v_scale | (uintptr_t)a.k_zp | (uintptr_t)a.v_zp) % 16)
         return fail(PA_ERR_INVALID_ARG, "k_scale, v_scale, k_zp and v_zp must be 16-byte aligned");
     const BalancedShape shape = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
-                                               a.head_dim, a.max_q_len, a.max_context_len);
+                                               a.head_dim, a.max_q_len, a.max_context_len, true);
     CUtensorMap mk, mv;
     if (pa_status s = g_maps8.get(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim))
         return s;

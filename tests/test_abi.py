@@ -145,15 +145,16 @@ def test_workspace_size():
     rows = 4 * 32 * 256
     assert n == rows * 128 * 4 + 2 * rows * 4
     # balanced schedule: prefix sums, then 2 slots per worker (workers capped at 2048);
-    # a slot is a 32-byte header + m, l, O for a tile of 16 (or 32) query rows
+    # a slot is a 32-byte header + m, l, O for a tile of 16 (or 64) query rows
     slot = 32 + 4 * 16 * (128 + 2)
     assert pa.decode_workspace_size(64, 64, 32, 8, 128, 1, 4096, 0) == 512 + 2 * 2048 * slot
     slot64 = 32 + 4 * 16 * 66
     assert pa.decode_workspace_size(1, 1, 8, 2, 64, 1, 17, 0) == 256 + 2 * (2 * 2) * slot64
-    # 32 q heads on one KV head with verify runs of 5: tiles of 32 rows, 5 chunks
-    slot32 = 32 + 4 * 32 * 130
+    # 32 q heads on one KV head with verify runs of 5 (160 rows): slots sized for the
+    # 64-row tiles of the 16-bit kernels (the INT8 kernel's 32-row tiles fit in them)
+    slot_big = 32 + 4 * 64 * 130
     assert pa.decode_workspace_size(256, 400, 32, 1, 128, 5, 16384, 0) == \
-        1280 + 2 * 2048 * slot32
+        1280 + 2 * 2048 * slot_big
     assert pa.decode_workspace_size(1, 1, 8, 3, 64, 1, 17, 0) == 0      # heads not a multiple
 
 

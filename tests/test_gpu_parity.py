@@ -172,7 +172,7 @@ def _written_slots(ws: torch.Tensor, wl, max_q_len: int):
     a 32-byte header {seq, kv head, chunk, first token, end token} and fp32
     m[RT], l[RT], O[RT][d]."""
     G = wl.num_heads // wl.num_kv_heads
-    rt = 16 if G * max_q_len <= 16 else 32
+    rt = 16 if G * max_q_len <= 16 else 64          # rows per tile of the 16-bit kernels
     slot_bytes = (32 + 4 * rt * (wl.head_dim + 2) + 15) // 16 * 16
     cum_bytes = (4 * (wl.num_seqs + 1) + 255) // 256 * 256
     raw = ws.cpu().numpy()[cum_bytes:]
@@ -193,10 +193,10 @@ def _written_slots(ws: torch.Tensor, wl, max_q_len: int):
     ("many_short", [1, 2, 3, 17, 31, 33, 5, 64, 100, 7] * 6, [1] * 60, 16, 4, 128),
     # one long sequence and MQA: far more shares than segments, most cut
     ("one_long", [20000], [1], 8, 1, 128),
-    # verify runs and GQA 8, partial slots with 2 m-tiles of rows
+    # verify runs and GQA 8: 32 rows, one 64-row tile served by two of the CTA's warps
     ("verify_long", [3000, 777, 4100], [4, 1, 3], 32, 4, 128),
-    # 64 query rows per KV head: two row chunks per (sequence, kv head)
-    ("chunked_rows", [2500, 900], [2, 1], 32, 1, 128),
+    # 96 query rows per KV head: two row chunks per (sequence, kv head)
+    ("chunked_rows", [2500, 900], [3, 1], 32, 1, 128),
 ])
 def test_balanced_partials_match_oracle(case):
     name, lens, qlens, H, Hkv, d = case
@@ -238,7 +238,7 @@ def test_balanced_partials_match_oracle(case):
 
 def test_many_query_rows_per_kv_head_use_row_chunks():
     """MQA with 32 q heads and verify runs of up to 5 tokens: up to 160 query
-    rows per KV head, served as row tiles of 32 (five chunks re-reading the
+    rows per KV head, served as row tiles of 64 (three chunks re-reading the
     same KV), checked against the oracle."""
     wl = W.simple("mqa_rows160", 71, [300, 1000, 77, 2600, 16, 5], [5, 1, 3, 4, 2, 5], 32, 1,
                   128, "bf16")
