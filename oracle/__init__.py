@@ -32,7 +32,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-DTYPE_CODE = {"f16": 0, "bf16": 1, "f32": 2, "int8": 3}
+DTYPE_CODE = {"f16": 0, "bf16": 1, "f32": 2, "int8": 3, "fp8": 4}
 
 
 def build(force: bool = False) -> str:
@@ -71,6 +71,13 @@ def lib() -> ctypes.CDLL:
         L.orc_copy_blocks.restype = None
         L.orc_f16_to_f64.argtypes = [ctypes.c_uint16]
         L.orc_f16_to_f64.restype = f64
+        L.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_to_f64.restype = f64
+        L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_append_fp8.argtypes = [P, P, P, ctypes.c_int, P, i64, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int]
+        L.orc_append_fp8.restype = None
         _lib = L
     return _lib
 
@@ -114,6 +121,8 @@ class HostCache:
         return self.k.shape[3]
 
     def arrays(self):
+        """The per-block arrays (what a block copy copies and the cache
+        comparison compares); FP8's per-head scales are not per block."""
         out = [self.k, self.v]
         if self.kv_dtype == "int8":
             out += [self.k_scale, self.v_scale, self.k_zp, self.v_zp]
@@ -122,15 +131,21 @@ class HostCache:
 
 def empty_cache(kv_dtype: str, num_blocks: int, num_kv_heads: int,
                 block_size: int, head_dim: int, canary_blocks: int = 0,
-                canary_byte: int = 0) -> HostCache:
+                canary_byte: int = 0, head_scales=None) -> HostCache:
     """Zeroed cache of num_blocks + canary_blocks blocks; the trailing canary
-    blocks are filled with canary_byte (they must never change)."""
+    blocks are filled with canary_byte (they must never change). FP8 caches
+    take head_scales = (k_scale, v_scale), fp32 [num_kv_heads] each."""
     nb = num_blocks + canary_blocks
     shp = (nb, num_kv_heads, block_size, head_dim)
     if kv_dtype == "int8":
         c = HostCache("int8", np.zeros(shp, np.int8), np.zeros(shp, np.int8),
                       np.zeros(shp[:3], np.float32), np.zeros(shp[:3], np.float32),
                       np.zeros(shp[:3], np.int8), np.zeros(shp[:3], np.int8))
+    elif kv_dtype == "fp8":
+        ks, vs = head_scales
+        c = HostCache("fp8", np.zeros(shp, np.uint8), np.zeros(shp, np.uint8),
+                      np.ascontiguousarray(ks, dtype=np.float32),
+                      np.ascontiguousarray(vs, dtype=np.float32))
     else:
         c = HostCache(kv_dtype, np.zeros(shp, np.uint16), np.zeros(shp, np.uint16))
     if canary_blocks:
@@ -153,7 +168,11 @@ def append(cache: HostCache, k_src, v_src, slots: np.ndarray, src_dtype: str) ->
     kb, vb = _bits16(k_src), _bits16(v_src)
     assert kb.shape == (T, cache.num_kv_heads, cache.head_dim)
     L = lib()
-    if cache.kv_dtype == "int8":
+    if cache.kv_dtype == "fp8":
+        for src, codes, sc in ((kb, cache.k, cache.k_scale), (vb, cache.v, cache.v_scale)):
+            L.orc_append_fp8(_p(codes), _p(sc), _p(src), DTYPE_CODE[src_dtype], _p(slots), T,
+                             cache.num_kv_heads, cache.head_dim, cache.block_size)
+    elif cache.kv_dtype == "int8":
         for src, codes, sc, zp in ((kb, cache.k, cache.k_scale, cache.k_zp),
                                    (vb, cache.v, cache.v_scale, cache.v_zp)):
             L.orc_append_int8(_p(codes), _p(sc), _p(zp), _p(src), DTYPE_CODE[src_dtype],
@@ -174,6 +193,21 @@ def copy_blocks(cache: HostCache, pairs: List[Tuple[int, int]]) -> None:
     for a in cache.arrays():
         per_block = a[0].nbytes
         lib().orc_copy_blocks(_p(a), per_block, _p(pr), pr.shape[0])
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 code -> value (fp64), from the format's definition."""
+    L = lib()
+    flat = np.asarray(codes, dtype=np.uint8).reshape(-1)
+    return np.array([L.orc_e4m3_to_f64(int(c)) for c in flat]).reshape(np.shape(codes))
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """fp32 values -> nearest FP8 E4M3 codes (ties to even, saturating at 448)."""
+    L = lib()
+    flat = np.asarray(x, dtype=np.float32).reshape(-1)
+    return np.array([L.orc_e4m3_encode(float(v)) for v in flat],
+                    dtype=np.uint8).reshape(np.shape(x))
 
 
 def quantize_row(x: np.ndarray) -> Tuple[np.ndarray, float, int]:
@@ -285,7 +319,8 @@ def run(wl, threads: int = 1, canary_blocks: int = 0, canary_byte: int = 0,
     src_dtype = {"torch.float16": "f16", "torch.bfloat16": "bf16"}[str(wl.src_dtype)]
     pool = BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
     cache = empty_cache(wl.kv_dtype, wl.num_blocks, wl.num_kv_heads, wl.block_size,
-                        wl.head_dim, canary_blocks, canary_byte)
+                        wl.head_dim, canary_blocks, canary_byte,
+                        head_scales=getattr(wl, "head_scales", None))
     names: dict = {}
     ph_slots, ph_pairs = [], []
     for ops in wl.phases:

@@ -13,7 +13,9 @@
  *
  * Cache layout (this project's reading; the pages fix none): per K and per V,
  * cache[num_blocks][num_kv_heads][block_size][head_dim], and for INT8 a
- * per-(token, kv_head) fp32 scale and int8 zero point, [num_blocks][num_kv_heads][block_size].
+ * per-(token, kv_head) fp32 scale and int8 zero point, [num_blocks][num_kv_heads][block_size];
+ * for FP8 (E4M3) one fp32 scale per kv head, [num_kv_heads] (p2 "ybb.press" §5.2:
+ * per-head scaling factors for an FP8 KV cache).
  * A slot is phys_block * block_size + offset; a negative slot is skipped.
  *
  * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (no fast-math: the
@@ -28,6 +30,7 @@
 #define ORC_BF16 1
 #define ORC_F32 2
 #define ORC_INT8 3
+#define ORC_FP8 4
 
 /* ---- element decoding from the IEEE 754 definitions ---------------------- */
 
@@ -82,6 +85,72 @@ void orc_quantize_row(const float* x, int d, int8_t* codes, float* scale_out,
     }
     *scale_out = scale;
     *zp_out = (int8_t)zp;
+}
+
+/* ---- FP8 E4M3 (the OCP 8-bit float "E4M3": 1 sign bit, 4 exponent bits with
+ * bias 7, 3 fraction bits; no infinities; exponent 15 with fraction 7 is NaN,
+ * so the largest finite value is 1.75 * 2^8 = 448; exponent 0 holds the
+ * subnormals m * 2^-9). Decoded here from that definition.                   */
+double orc_e4m3_to_f64(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 0xf, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp((double)(8 + m), e - 10);                /* (1 + m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to even; magnitudes above 448 (including infinity)
+ * saturate to 448; NaN gives 0x7F. The value is scaled by a power of two so
+ * that rint() (round half to even) picks the fraction exactly.              */
+uint8_t orc_e4m3_encode(float xf) {
+    double x = (double)xf;
+    if (isnan(x)) return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    uint8_t code;
+    if (a >= 448.0) {
+        code = 0x7e;
+    } else if (a < ldexp(1.0, -6)) {                        /* subnormal range */
+        code = (uint8_t)rint(ldexp(a, 9));                  /* 0..8; 8 is the smallest normal */
+    } else {
+        int k;
+        frexp(a, &k);                                       /* a = f * 2^k, f in [0.5, 1) */
+        int e = k - 1;                                      /* 2^e <= a < 2^(e+1) */
+        double n = rint(ldexp(a, 3 - e));                   /* 8..16 */
+        if (n == 16.0) {
+            n = 8.0;
+            e += 1;
+        }
+        int c = ((e + 7) << 3) | ((int)n - 8);
+        code = (uint8_t)(c > 0x7e ? 0x7e : c);
+    }
+    return sign | code;
+}
+
+/* FP8 quantiser: code = E4M3(x / scale), the quotient the correctly rounded
+ * fp32 division; dequantised value = E4M3 value * scale in fp32.             */
+void orc_append_fp8(uint8_t* codes, const float* head_scale, const uint16_t* src,
+                    int src_dtype, const int64_t* slots, int64_t num_tokens,
+                    int num_kv_heads, int head_dim, int block_size) {
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slots[t];
+        if (slot < 0) continue;
+        int64_t blk = slot / block_size, off = slot % block_size;
+        for (int g = 0; g < num_kv_heads; ++g) {
+            const uint16_t* s = src + (t * num_kv_heads + g) * head_dim;
+            uint8_t* dst = codes + ((blk * num_kv_heads + g) * block_size + off) * head_dim;
+            for (int j = 0; j < head_dim; ++j) {
+                float y = src_to_f32(s + j, src_dtype) / head_scale[g];
+                dst[j] = orc_e4m3_encode(y);
+            }
+        }
+    }
+}
+
+static double dequant_fp8(uint8_t c, float scale) {
+    float x = (float)orc_e4m3_to_f64(c) * scale;            /* E4M3 values are exact in fp32 */
+    return (double)x;
 }
 
 /* [p4] Quantization: x = (x_q - zero_point) * scale, one fp32 rounding */
@@ -171,6 +240,8 @@ static double load_kv(const orc_cache* c, int is_v, int64_t blk, int g, int off,
         case ORC_F16: return f16_to_f64(((const uint16_t*)base)[e]);
         case ORC_BF16: return (double)bf16_to_f32(((const uint16_t*)base)[e]);
         case ORC_F32: return (double)((const float*)base)[e];
+        case ORC_FP8:
+            return dequant_fp8(((const uint8_t*)base)[e], (is_v ? c->v_scale : c->k_scale)[g]);
         default:
             return dequant(((const int8_t*)base)[e],
                            (is_v ? c->v_zp : c->k_zp)[r],

@@ -253,3 +253,34 @@ def test_shared_prefix_cascade_equals_full_attention(step_q_max):
         merged = oracle.lse_merge(np.stack([pre[0], suf[0]]), np.stack([pre[1], suf[1]]),
                                   np.stack([pre[2], suf[2]]))
         np.testing.assert_allclose(merged, run.out[rows], rtol=0, atol=1e-12)
+
+
+def test_fp8_cache_attends_over_dequantised_values():
+    """FP8: the oracle attends over E4M3(code) * scale_h (fp32), per-head
+    scales calibrated to the data. Gather the codes with numpy indexing,
+    decode them with torch's float8_e4m3fn, scale in fp32, compare with SDPA."""
+    wl = W.simple("fp8", 62, [40, 17, 90], [1, 3, 2], 8, 2, 64, "fp8")
+    run = oracle.run(wl)
+    c = run.cache
+    ks, vs = wl.head_scales
+    kv_list = []
+    for s, L in enumerate(run.context_lens):
+        t = np.arange(L)
+        blk = run.block_tables[s, t // 16]
+        off = t % 16
+        dk = torch.from_numpy(np.ascontiguousarray(c.k[blk, :, off, :])).view(
+            torch.float8_e4m3fn).float().numpy()
+        dv = torch.from_numpy(np.ascontiguousarray(c.v[blk, :, off, :])).view(
+            torch.float8_e4m3fn).float().numpy()
+        K = dk * ks[None, :, None]
+        V = dv * vs[None, :, None]
+        kv_list.append((torch.from_numpy(K), torch.from_numpy(V)))
+    ref = sdpa_reference(wl, kv_list)
+    np.testing.assert_allclose(run.out, ref, rtol=0, atol=1e-12)
+    # round trip: within half an E4M3 step (relative 2^-4) of the originals
+    for (K, V), (K0, V0) in zip(kv_list, W.contiguous_kv(wl)):
+        for a, b, sc in ((K, K0, ks), (V, V0, vs)):
+            err = (a.double() - b.double()).abs()
+            bound = b.double().abs() * 2.0 ** -4 + torch.from_numpy(sc).double()[None, :, None] \
+                * 2.0 ** -10
+            assert (err <= bound).all()

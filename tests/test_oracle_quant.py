@@ -69,3 +69,54 @@ def test_planted_rounding_mistake_is_caught():
     codes, scale, zp = oracle.quantize_row(x)
     away = (np.sign(x) * np.floor(np.abs(x) + 0.5)).astype(int) + zp
     assert not np.array_equal(codes.astype(int), away)
+
+
+# ---- FP8 E4M3 (page 2 "ybb.press" §5.2: FP8 KV cache, per-head scales) -------
+
+def test_e4m3_decode_table_matches_torch_float8():
+    """All 256 codes decoded from the format definition equal torch's
+    float8_e4m3fn values (NaN where torch has NaN)."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    dec = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+    assert ((dec == ref) | (np.isnan(dec) & np.isnan(ref))).all()
+    assert np.nanmax(dec) == 448.0 and np.isnan(dec[0x7F]) and np.isnan(dec[0xFF])
+    assert dec[0x01] == 2.0 ** -9 and dec[0x08] == 2.0 ** -6    # smallest subnormal / normal
+
+
+def test_e4m3_encode_matches_torch_below_overflow():
+    """Round to nearest, ties to even, against torch's cast, on random values,
+    exact ties between neighbours, and the subnormal range."""
+    import torch
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.normal(size=20000) * 40, rng.normal(size=5000) * 0.01,
+                        rng.uniform(-460, 460, size=5000)]).astype(np.float32)
+    vals = np.unique(np.abs(oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))))
+    mids = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)   # exact ties (representable)
+    x = np.concatenate([x, mids, -mids, vals.astype(np.float32)])
+    x = x[np.abs(x) < 464]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), ref)
+
+
+def test_e4m3_encode_saturates_and_round_trips():
+    """Magnitudes past the largest finite value saturate to +-448 (the
+    satfinite convention; a plain cast would give NaN from 464 up), NaN stays
+    NaN, and every finite code round-trips."""
+    big = np.array([448, 463.99, 464, 1e9, np.inf, -464, -np.inf], np.float32)
+    assert oracle.e4m3_encode(big).tolist() == [0x7E] * 5 + [0xFE] * 2
+    assert oracle.e4m3_encode(np.array([np.nan], np.float32))[0] == 0x7F
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(finite).astype(np.float32)),
+                          finite)
+
+
+def test_planted_e4m3_bias_mistake_is_caught():
+    """A decoder with exponent bias 8 instead of 7 disagrees with torch: the
+    table pin above would fail."""
+    import torch
+    codes = np.arange(0x08, 0x78, dtype=np.uint8)
+    wrong = oracle.e4m3_decode(codes) / 2.0                    # bias off by one
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+    assert not np.array_equal(wrong, ref)

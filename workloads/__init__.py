@@ -32,7 +32,7 @@ import torch
 BLOCK_SIZE = 16
 SEED_BASE = 1540
 
-KV_DTYPES = ("f16", "bf16", "int8")
+KV_DTYPES = ("f16", "bf16", "int8", "fp8")
 TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -84,6 +84,7 @@ class Workload:
     partition_size: int = 512
     block_size: int = BLOCK_SIZE
     notes: dict = field(default_factory=dict)
+    head_scales: Optional[tuple] = None   # FP8 caches: (k_scale, v_scale), fp32 [H_kv] each
 
     @property
     def decode_seqs(self) -> List[int]:
@@ -157,7 +158,7 @@ def simple(name: str, seed: int, context_lens, q_lens, num_heads: int,
         assert L >= r >= 1, (L, r)
     rng = np.random.default_rng(seed)
     vals = _Values(seed)
-    src = torch.bfloat16 if kv_dtype == "int8" else TORCH_DTYPES[kv_dtype]
+    src = torch.bfloat16 if kv_dtype in ("int8", "fp8") else TORCH_DTYPES[kv_dtype]
     if q_dtype is None:
         q_dtype = src
     need = sum((L + BLOCK_SIZE - 1) // BLOCK_SIZE for L in context_lens)
@@ -192,7 +193,29 @@ def simple(name: str, seed: int, context_lens, q_lens, num_heads: int,
                     num_blocks=num_blocks, free_order=free_order,
                     scale=_softmax_scale(head_dim), phases=[phase0], step=step,
                     q=q, context_lens=context_lens,
-                    partition_size=partition_size)
+                    partition_size=partition_size,
+                    head_scales=(calibrate_fp8([phase0], step, num_kv_heads)
+                                 if kv_dtype == "fp8" else None))
+
+
+FP8_MAX = 448.0   # largest finite E4M3 value
+
+
+def calibrate_fp8(phases, step, num_kv_heads: int) -> tuple:
+    """Per-KV-head FP8 scales from the data the workload will append (page 2
+    "ybb.press" §5.2: per-head scaling factors found on calibration data):
+    scale_h = max |x| over head h / 448, in fp32, separately for K and V, so
+    no value saturates. Bookkeeping over generated values; no cache
+    arithmetic."""
+    amax = np.zeros((2, num_kv_heads), np.float64)
+    for ops in list(phases) + [step]:
+        for op in ops:
+            if isinstance(op, Append):
+                for i, t in enumerate((op.k, op.v)):
+                    a = t.float().abs().amax(dim=(0, 2)).double().numpy()
+                    amax[i] = np.maximum(amax[i], a)
+    sc = np.where(amax > 0, amax / FP8_MAX, 1.0).astype(np.float32)
+    return sc[0].copy(), sc[1].copy()
 
 
 def best_of_n(name: str, seed: int, num_groups: int, n_forks: int,
