@@ -33,6 +33,7 @@ METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak); seq-steps/s at 1 GPU"
 PROFILES = {
     "16bit": ("paged_decode_llama3_8b.md", ("paged_decode.cu", "balanced.cuh", "ptx.cuh")),
     "int8": ("paged_decode_int8_mixed.md", ("paged_decode_int8.cu", "balanced.cuh", "ptx.cuh")),
+    "fp8": ("paged_decode_fp8_llama3_8b.md", ("paged_decode_fp8.cu", "balanced.cuh", "ptx.cuh")),
 }
 
 
@@ -89,7 +90,7 @@ def step_bytes(wl, out_bytes_per_elem=4):
     """Algorithmic bytes of one step: every sequence's K and V for all its
     tokens (the attention must read them), q, the output, and the appended
     rows (written once)."""
-    kv_elem = 1 if wl.kv_dtype == "int8" else 2
+    kv_elem = 1 if wl.kv_dtype in ("int8", "fp8") else 2
     per_tok = 2 * wl.num_kv_heads * wl.head_dim * kv_elem
     if wl.kv_dtype == "int8":
         per_tok += 2 * wl.num_kv_heads * 5          # fp32 scale + int8 zero point, K and V
@@ -103,7 +104,7 @@ def step_bytes(wl, out_bytes_per_elem=4):
 
 
 def kernel_family(kv_dtype: str) -> str:
-    return "int8" if kv_dtype == "int8" else "16bit"
+    return kv_dtype if kv_dtype in ("int8", "fp8") else "16bit"
 
 
 def kernel_digest(family: str = "16bit"):
@@ -192,7 +193,7 @@ def build_state(wl, device, partition_size, shared_prefix=False):
     import torch
     from paged_kv_cache_154_gb300.engine import PagedKVCache
     cache = PagedKVCache(wl.num_blocks, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
-                         device=device, free_order=wl.free_order)
+                         device=device, free_order=wl.free_order, head_scales=wl.head_scales)
     names = {}
     for ops in wl.phases:
         cache.run_phase(ops, names)
@@ -205,7 +206,7 @@ def build_state(wl, device, partition_size, shared_prefix=False):
 def unique_kv_bytes(wl, group_start, prefix_len):
     """KV bytes read-once decode must read: each group's shared prefix once,
     every sequence's tokens after it once."""
-    per_tok = 2 * wl.num_kv_heads * wl.head_dim * (1 if wl.kv_dtype == "int8" else 2)
+    per_tok = 2 * wl.num_kv_heads * wl.head_dim * (1 if wl.kv_dtype in ("int8", "fp8") else 2)
     toks = 0
     for g in range(len(prefix_len)):
         toks += int(prefix_len[g])
@@ -345,6 +346,8 @@ def run_ours(args, rank, world, local):
                                 if si.shared is not None else
                                 "pa_decode (paged_decode_int8_kernel + segment_reduce_kernel)"
                                 if wl.kv_dtype == "int8" else
+                                "pa_decode (paged_decode_fp8_kernel + segment_reduce_kernel)"
+                                if wl.kv_dtype == "fp8" else
                                 "pa_decode (paged_decode_balanced_kernel + segment_reduce_kernel)"
                                 if args.partition_size == 0 else
                                 "pa_decode (paged_decode_kernel + split_kv_reduce_kernel)"),
@@ -415,7 +418,7 @@ def cpu_baseline(wl, budget_s=12.0, sample_seqs=None):
     n = wl.num_seqs if sample_seqs is None else min(sample_seqs, wl.num_seqs)
     qsl = wl.query_start_loc[: n + 1]
     nbytes = 0
-    kv_elem = 1 if wl.kv_dtype == "int8" else 2
+    kv_elem = 1 if wl.kv_dtype in ("int8", "fp8") else 2
     for s in range(n):
         nbytes += 2 * wl.context_lens[s] * wl.num_kv_heads * wl.head_dim * kv_elem
     nq = int(qsl[-1])
@@ -451,7 +454,7 @@ def run_reference(args, rank, world):
         n += 1
     qsl = wl.query_start_loc[: n + 1]
     nq = int(qsl[-1])
-    kv_elem = 1 if wl.kv_dtype == "int8" else 2
+    kv_elem = 1 if wl.kv_dtype in ("int8", "fp8") else 2
     nbytes = sum(2 * wl.context_lens[s] * wl.num_kv_heads * wl.head_dim * kv_elem
                  for s in range(n)) + nq * wl.num_heads * wl.head_dim * 6
 

@@ -66,7 +66,13 @@ typedef enum pa_status {
     PA_ERR_DEVICE = 7         /* a kernel reported an error word (see pa_device_error) */
 } pa_status;
 
-typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2, PA_INT8 = 3 } pa_dtype;
+/* PA_FP8_E4M3: 8-bit float codes (1 sign, 4 exponent bits with bias 7, 3
+ * fraction bits, no infinities, largest finite 448) with one fp32 scale per
+ * KV head ([p2] §5.2: FP8 KV cache with per-head scaling factors found on
+ * calibration data); the value of a code is E4M3(code) * scale[head]. */
+typedef enum pa_dtype {
+    PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2, PA_INT8 = 3, PA_FP8_E4M3 = 4
+} pa_dtype;
 
 /* Message for the last failing call on this thread ("" if none). */
 const char* pa_last_error(void);
@@ -177,6 +183,10 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, void* k_scale,
  * 0), zp = clamp(-128 - rint(mn/scale)), code = clamp(rint(x/scale) + zp),
  * IEEE fp32 division and round-half-to-even; scale and zp are stored per
  * (token, kv head) ([p2] §5.2: per-head rather than global scales).
+ * For kv_dtype FP8_E4M3, k_scale / v_scale are the caller's per-head scales,
+ * fp32 [num_kv_heads] (read only; k_zp, v_zp unused): code =
+ * E4M3(x / scale[head]) with the IEEE fp32 quotient rounded to the nearest
+ * E4M3 value, ties to even, magnitudes past 448 saturating to +-448.
  * slot_mapping: device int64 [num_tokens]; a negative slot skips the token. */
 pa_status pa_append_kv(const void* key, const void* value, pa_dtype src_dtype,
                        void* k_cache, void* v_cache, pa_dtype kv_dtype,

@@ -18,7 +18,7 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpa.so")
 
-PA_F16, PA_BF16, PA_F32, PA_INT8 = 0, 1, 2, 3
+PA_F16, PA_BF16, PA_F32, PA_INT8, PA_FP8_E4M3 = 0, 1, 2, 3, 4
 STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
           3: "PA_ERR_OUT_OF_BLOCKS", 4: "PA_ERR_BAD_REFCOUNT", 5: "PA_ERR_CUDA",
           6: "PA_ERR_VALIDATION", 7: "PA_ERR_DEVICE"}
@@ -96,7 +96,7 @@ def version() -> str:
 def _dtype_code(t) -> int:
     import torch
     return {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.float32: PA_F32,
-            torch.int8: PA_INT8}[t.dtype]
+            torch.int8: PA_INT8, torch.float8_e4m3fn: PA_FP8_E4M3}[t.dtype]
 
 
 def _ptr(t) -> Optional[int]:

@@ -61,7 +61,9 @@ using pa::fail;
 
 namespace {
 
-bool is_kv_dtype(pa_dtype t) { return t == PA_F16 || t == PA_BF16 || t == PA_INT8; }
+bool is_kv_dtype(pa_dtype t) {
+    return t == PA_F16 || t == PA_BF16 || t == PA_INT8 || t == PA_FP8_E4M3;
+}
 
 pa_status check_shape(int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
     if (block_size != 16)
@@ -153,9 +155,11 @@ extern "C" pa_status pa_append_kv(const void* key, const void* value, pa_dtype s
     if (src_dtype != PA_F16 && src_dtype != PA_BF16)
         return fail(PA_ERR_UNSUPPORTED, "src_dtype %d (F16 or BF16)", (int)src_dtype);
     if (!is_kv_dtype(kv_dtype)) return fail(PA_ERR_INVALID_ARG, "kv_dtype %d", (int)kv_dtype);
-    if (kv_dtype != PA_INT8 && kv_dtype != src_dtype)
+    if ((kv_dtype == PA_F16 || kv_dtype == PA_BF16) && kv_dtype != src_dtype)
         return fail(PA_ERR_UNSUPPORTED, "a %s cache takes %s rows only",
                     kv_dtype == PA_F16 ? "F16" : "BF16", kv_dtype == PA_F16 ? "F16" : "BF16");
+    if (kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale))
+        return fail(PA_ERR_INVALID_ARG, "FP8 cache needs per-head k_scale and v_scale");
     if (pa_status s = check_shape(num_kv_heads, head_dim, block_size)) return s;
     if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks %d", num_blocks);
     if (kv_dtype == PA_INT8 && (!k_scale || !v_scale || !k_zp || !v_zp))
@@ -225,8 +229,10 @@ pa_status check_decode_args(void* out, pa_dtype out_dtype, const void* q, pa_dty
     if (!is_kv_dtype(kv_dtype)) return fail(PA_ERR_INVALID_ARG, "kv_dtype %d", (int)kv_dtype);
     if (q_dtype != PA_F16 && q_dtype != PA_BF16)
         return fail(PA_ERR_UNSUPPORTED, "q_dtype %d (F16 or BF16)", (int)q_dtype);
-    if (kv_dtype != PA_INT8 && q_dtype != kv_dtype)
+    if ((kv_dtype == PA_F16 || kv_dtype == PA_BF16) && q_dtype != kv_dtype)
         return fail(PA_ERR_UNSUPPORTED, "q_dtype must equal kv_dtype for F16/BF16 caches");
+    if (kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale))
+        return fail(PA_ERR_INVALID_ARG, "FP8 cache needs per-head k_scale and v_scale");
     if (out_dtype != PA_F32 && out_dtype != q_dtype)
         return fail(PA_ERR_UNSUPPORTED, "out_dtype must be F32 or the q dtype");
     if (kv_dtype == PA_INT8 && (!k_scale || !v_scale || !k_zp || !v_zp))

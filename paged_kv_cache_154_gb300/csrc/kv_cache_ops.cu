@@ -1,5 +1,5 @@
-// KV-cache writes: append through a slot mapping (F16/BF16 copy, or INT8
-// quantisation) and copy-on-write block copies.
+// KV-cache writes: append through a slot mapping (F16/BF16 copy, INT8 or
+// FP8 quantisation) and copy-on-write block copies.
 //
 // Append restates the decode workflow of "cs336 lecture 10" (KV Cache:
 // append the new K, V to the cache) and the block table of "KV Cache ...
@@ -10,6 +10,7 @@
 // §2.1 of that page (copy a shared block only when it is modified).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "pa_internal.h"
 
@@ -122,6 +123,65 @@ __global__ void append_kv_int8_kernel(const T* __restrict__ key, const T* __rest
     }
 }
 
+// FP8 E4M3 append ("LLM推理优化深度实战" §5.2: FP8 KV cache, one scale per
+// KV head): one thread per 16 consecutive elements of a (token, kv head) row,
+// K and V together. code = E4M3(x / scale[head]): the IEEE fp32 quotient
+// (__fdiv_rn), converted with round-to-nearest-even and saturation at +-448.
+template <typename T>
+__global__ void append_kv_fp8_kernel(const T* __restrict__ key, const T* __restrict__ value,
+                                     uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                                     const float* __restrict__ k_scale,
+                                     const float* __restrict__ v_scale,
+                                     const int64_t* __restrict__ slots, int num_tokens,
+                                     int num_kv_heads, int head_dim, int64_t num_slots,
+                                     unsigned int* err) {
+    const int per_row = head_dim / 16;
+    const int64_t per_token = (int64_t)num_kv_heads * per_row;
+    const int64_t total = (int64_t)num_tokens * per_token;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / per_token;
+        const int64_t rem = i - t * per_token;
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (err) atomicOr(err, pa::ERR_BAD_SLOT);
+            continue;
+        }
+        const int g = (int)(rem / per_row), c = (int)(rem - (int64_t)g * per_row);
+        const int64_t blk = slot / kBlock, off = slot % kBlock;
+        const int64_t src = (t * num_kv_heads + g) * head_dim + c * 16;
+        const int64_t dst = ((blk * num_kv_heads + g) * kBlock + off) * head_dim + c * 16;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const T* in = (which ? value : key) + src;
+            const float s = __ldg((which ? v_scale : k_scale) + g);
+            const uint4 raw0 = __ldg(reinterpret_cast<const uint4*>(in));
+            const uint4 raw1 = __ldg(reinterpret_cast<const uint4*>(in) + 1);
+            const T* h0 = reinterpret_cast<const T*>(&raw0);
+            const T* h1 = reinterpret_cast<const T*>(&raw1);
+            uint32_t out[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int pr = 0; pr < 2; ++pr) {
+                    const int e = 4 * w + 2 * pr;
+                    const T* h = e < 8 ? h0 + e : h1 + (e - 8);
+                    const float2 y = make_float2(__fdiv_rn(to_f32<T>(h[0]), s),
+                                                 __fdiv_rn(to_f32<T>(h[1]), s));
+                    const __nv_fp8x2_storage_t q =
+                        __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+                    word |= (uint32_t)q << (16 * pr);
+                }
+                out[w] = word;
+            }
+            *reinterpret_cast<uint4*>((which ? v_cache : k_cache) + dst) =
+                make_uint4(out[0], out[1], out[2], out[3]);
+        }
+    }
+}
+
 struct CopyParams {
     uint4* arrays[6];
     int64_t vecs_per_block[6];
@@ -151,7 +211,25 @@ namespace pa {
 pa_status launch_append_kv(const AppendArgs& a) {
     unsigned int* err = device_error_word();
     const int64_t num_slots = (int64_t)a.num_blocks * a.block_size;
-    if (a.kv_dtype != PA_INT8) {
+    if (a.kv_dtype == PA_FP8_E4M3) {
+        const int64_t total = (int64_t)a.num_tokens * a.num_kv_heads * (a.head_dim / 16);
+        const int threads = 256;
+        const int64_t blocks = (total + threads - 1) / threads;
+        const int grid = (int)(blocks < 65535 ? blocks : 65535);
+        if (((uintptr_t)a.k_scale | (uintptr_t)a.v_scale) % 4)
+            return fail(PA_ERR_INVALID_ARG, "k_scale / v_scale must be 4-byte aligned");
+        if (a.src_dtype == PA_BF16)
+            append_kv_fp8_kernel<__nv_bfloat16><<<grid, threads, 0, a.stream>>>(
+                static_cast<const __nv_bfloat16*>(a.key),
+                static_cast<const __nv_bfloat16*>(a.value), static_cast<uint8_t*>(a.k_cache),
+                static_cast<uint8_t*>(a.v_cache), a.k_scale, a.v_scale, a.slots, a.num_tokens,
+                a.num_kv_heads, a.head_dim, num_slots, err);
+        else
+            append_kv_fp8_kernel<__half><<<grid, threads, 0, a.stream>>>(
+                static_cast<const __half*>(a.key), static_cast<const __half*>(a.value),
+                static_cast<uint8_t*>(a.k_cache), static_cast<uint8_t*>(a.v_cache), a.k_scale,
+                a.v_scale, a.slots, a.num_tokens, a.num_kv_heads, a.head_dim, num_slots, err);
+    } else if (a.kv_dtype != PA_INT8) {
         const int vec_per_row = a.head_dim * 2 / 16;
         const int64_t total = (int64_t)a.num_tokens * a.num_kv_heads * vec_per_row;
         const int threads = 256;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -32,7 +33,7 @@ inline int dtype_bytes(pa_dtype t) {
     switch (t) {
         case PA_F16: case PA_BF16: return 2;
         case PA_F32: return 4;
-        case PA_INT8: return 1;
+        case PA_INT8: case PA_FP8_E4M3: return 1;
     }
     return 0;
 }
@@ -129,6 +130,12 @@ struct DecodeArgs {
 };
 pa_status launch_decode(const DecodeArgs& a);
 
+// TMA tensor map of a cache ([num_blocks][num_kv_heads][16][head_dim] of
+// elem_bytes-byte elements), cached per (pointer, shape, device)
+// (tensor_maps.cu).
+pa_status cache_tensor_map(CUtensorMap* out, const void* ptr, int num_blocks, int num_kv_heads,
+                           int head_dim, int elem_bytes);
+
 // Host-side argument checks of the decode entry points (capi.cu).
 pa_status check_decode_args(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
                             const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
@@ -161,21 +168,28 @@ struct BalancedShape {
     int64_t workspace_bytes;
 };
 
+// Kernel families of the balanced schedule.
+enum TileKind { kTile16Bit = 0, kTileInt8 = 1, kTileFp8 = 2 };
+
 // Query rows per tile: 16 while a KV head has at most 16 rows (G q heads x
 // the longest query run), else 64 for the 16-bit kernels (four warps of 16
-// rows share each block) and 32 for the INT8 kernel.
-inline int tile_rows(int64_t rows, bool int8) { return rows <= 16 ? 16 : (int8 ? 32 : 64); }
+// rows share each block) and 32 for the INT8 kernel; the FP8 kernel always
+// uses 16 (one warp per tile, further rows as further chunks).
+inline int tile_rows(int64_t rows, int kind) {
+    if (rows <= 16 || kind == kTileFp8) return 16;
+    return kind == kTileInt8 ? 32 : 64;
+}
 
-// The workspace is sized for either kernel family: the worker cap from the
-// smaller tile (more work units) and the slot from the larger one.
+// The workspace is sized for every kernel family: the worker cap from the
+// smallest tile (most work units) and the slot from the largest.
 inline BalancedShape balanced_shape(int num_seqs, int num_heads, int num_kv_heads,
                                     int head_dim, int max_q_len, int max_context_len,
-                                    bool int8 = false) {
+                                    int kind = kTile16Bit) {
     BalancedShape b{};
     const int64_t rows = (int64_t)(num_heads / num_kv_heads) * max_q_len;
-    b.rows_per_tile = tile_rows(rows, int8);
+    b.rows_per_tile = tile_rows(rows, kind);
     b.max_chunks = (rows + b.rows_per_tile - 1) / b.rows_per_tile;
-    const int64_t small = tile_rows(rows, true), large = tile_rows(rows, false);
+    const int64_t small = tile_rows(rows, kTileFp8), large = tile_rows(rows, kTile16Bit);
     b.virtual_blocks = (int64_t)num_seqs * num_kv_heads * ((rows + small - 1) / small) *
                        ((max_context_len + 15) / 16);
     b.workers = b.virtual_blocks < kBalancedMaxWorkers ? b.virtual_blocks : kBalancedMaxWorkers;
@@ -192,7 +206,9 @@ inline pa_status balanced_check(const DecodeArgs& a) {
                     kBalancedMaxSeqs);
     const BalancedShape b = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim,
                                            a.max_q_len, a.max_context_len,
-                                           a.kv_dtype == PA_INT8);
+                                           a.kv_dtype == PA_INT8       ? kTileInt8
+                                           : a.kv_dtype == PA_FP8_E4M3 ? kTileFp8
+                                                                       : kTile16Bit);
     if (b.max_chunks > 255 || b.virtual_blocks > 0x7fffffffll)
         return fail(PA_ERR_UNSUPPORTED, "decode call too large for one balanced launch");
     return PA_OK;

@@ -1045,72 +1045,7 @@ __global__ void __launch_bounds__(128)
 // host side
 // ---------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
 
-// Tensor map of one cache viewed as rows of head_dim 16-bit elements:
-// [num_blocks * num_kv_heads * 16 rows][head_dim], box 16 rows x 64 columns,
-// 128-byte swizzle.
-pa_status make_cache_map(CUtensorMap* m, const void* cache, int num_blocks, int num_kv_heads,
-                         int head_dim) {
-    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-    if (!fn) return pa::fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-    const uint64_t rows = (uint64_t)num_blocks * num_kv_heads * kBS;
-    if (rows > 0x7fffffffull) return pa::fail(PA_ERR_UNSUPPORTED, "cache has too many rows for TMA");
-    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)kBS};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(cache), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return pa::fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return PA_OK;
-}
-
-// A few recently used maps, so a decode step does not re-encode them.
-struct MapCache {
-    struct Entry {
-        const void* ptr;
-        int num_blocks, num_kv_heads, head_dim, device;
-        CUtensorMap map;
-    };
-    std::mutex mu;
-    Entry e[16];
-    int n = 0, next = 0;
-
-    pa_status get(CUtensorMap* out, const void* ptr, int nb, int hkv, int d) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        std::lock_guard<std::mutex> lock(mu);
-        for (int i = 0; i < n; ++i)
-            if (e[i].ptr == ptr && e[i].num_blocks == nb && e[i].num_kv_heads == hkv &&
-                e[i].head_dim == d && e[i].device == dev) {
-                *out = e[i].map;
-                return PA_OK;
-            }
-        CUtensorMap m;
-        if (pa_status st = make_cache_map(&m, ptr, nb, hkv, d)) return st;
-        Entry& x = e[next];
-        x = Entry{ptr, nb, hkv, d, dev, m};
-        next = (next + 1) % 16;
-        if (n < 16) ++n;
-        *out = m;
-        return PA_OK;
-    }
-};
-MapCache g_maps;
 
 constexpr int kBalancedStages = 2;
 
@@ -1289,13 +1224,16 @@ pa_status launch_dtype(const pa::DecodeArgs& a, int mt, const CUtensorMap& mk,
 namespace pa {
 
 pa_status launch_decode_int8(const DecodeArgs& a);
+pa_status launch_decode_fp8(const DecodeArgs& a);
 
 pa_status launch_decode(const DecodeArgs& a) {
-    if ((a.ctx_start || a.lse_out || a.unmasked) && (a.kv_dtype == PA_INT8 || a.partition_size))
+    if ((a.ctx_start || a.lse_out || a.unmasked) &&
+        (a.kv_dtype == PA_INT8 || a.kv_dtype == PA_FP8_E4M3 || a.partition_size))
         return fail(PA_ERR_UNSUPPORTED,
                     "token offsets, log-sum-exp output and unmasked rows need a 16-bit cache and "
                     "the balanced schedule");
     if (a.kv_dtype == PA_INT8) return launch_decode_int8(a);
+    if (a.kv_dtype == PA_FP8_E4M3) return launch_decode_fp8(a);
     if (a.partition_size > kMaxPartBlocks * kBS)
         return fail(PA_ERR_UNSUPPORTED, "partition_size %d > %d", a.partition_size,
                     kMaxPartBlocks * kBS);
@@ -1309,8 +1247,10 @@ pa_status launch_decode(const DecodeArgs& a) {
     if (a.partition_size == 0)
         if (pa_status s = balanced_check(a)) return s;
     CUtensorMap mk, mv;
-    if (pa_status s = g_maps.get(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim)) return s;
-    if (pa_status s = g_maps.get(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim)) return s;
+    if (pa_status s = cache_tensor_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
+        return s;
+    if (pa_status s = cache_tensor_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
+        return s;
     DecodeParams prm{};
     prm.out = a.out;
     prm.q = a.q;

@@ -1,0 +1,529 @@
+// Paged decode attention over an FP8 (E4M3) cache with one scale per KV head.
+//
+// "LLM推理优化深度实战" §5.2 describes the FP8 KV cache: codes in 8-bit floats
+// with a per-head scaling factor found on calibration data, half the bytes of
+// a 16-bit cache. The value of a code is E4M3(code) * scale[head], and the
+// attention is the usual softmax(Q K^T / sqrt(d)) V ("KV Cache ...
+// PagedAttention" §二), so
+//
+//   S[i][t] = k_scale[g] * sum_j q_ij E4M3(k_code[t][j])
+//   O[i][j] = v_scale[g] * sum_t P[i][t] E4M3(v_code[t][j])
+//
+// Every E4M3 value is exact in fp16 (3 fraction bits, exponents -9 .. 8), so
+// the tiles are converted with the hardware f16x2 <- e4m3x2 conversion and
+// the products run on fp16 tensor cores. q is converted to fp16 after an
+// exact power-of-two scaling per row (largest |q| into [2^14, 2^15)); the
+// scale, the softmax scale and k_scale[g] are applied to S, v_scale[g] to the
+// output. P goes to fp16 under a running maximum that is moved only when a
+// block raises it by more than 2^8 (so P <= 256 and O is rarely rescaled).
+//
+// Work split: the balanced schedule (balanced.cuh), one warp per share with
+// its own TMA ring, 16 query rows per tile (more rows become more chunks).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+
+#include <algorithm>
+
+#include "balanced.cuh"
+#include "pa_internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+using pa::sched::kBS;
+using pa::sched::kWorkerWarps;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kStages = 4;
+constexpr float kLazyMax = 8.f;
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// two E4M3 codes (low byte first) -> f16x2 (low half first), exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    const __half2_raw h =
+        __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+__device__ __forceinline__ float exp2i(int e) {   // 2^e for e in [-126, 127]
+    e = max(-126, min(127, e));
+    return __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
+// byte offset of 16-byte chunk `chunk` of token row `row` in a code tile as
+// the tensor map writes it: 128-byte swizzle for d = 128, 64-byte for d = 64
+template <int D>
+__device__ __forceinline__ uint32_t tile8_offset(int row, int chunk) {
+    if constexpr (D == 128) return row * 128 + ((chunk ^ (row & 7)) << 4);
+    else return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+}
+
+template <int D>
+struct Fp8Layout {
+    static constexpr int kTile = kBS * D;                 // one K (or V) code tile
+    static constexpr int kStage = 2 * kTile;
+    static constexpr int kRing = kStages * kStage;
+    static_assert(kTile % 1024 == 0 && kRing % 1024 == 0, "TMA swizzle alignment");
+    __host__ __device__ static int smem_bytes(int num_seqs) {
+        return pa::sched::header_bytes(num_seqs, kStages) + kWorkerWarps * kRing + 1024;
+    }
+};
+
+struct Fp8Scales {
+    const float* k_scale;   // [num_kv_heads]
+    const float* v_scale;
+};
+
+template <typename TQ, int D>
+__global__ void __launch_bounds__(kWorkerWarps * 32)
+    paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v,
+                            const pa::sched::Params p, const Fp8Scales x) {
+    using namespace pa::sched;
+    using Lay = Fp8Layout<D>;
+    constexpr int S = kStages;
+    constexpr int KCH = D / 16;          // 16-dim chunks = k-steps of Q K^T
+    constexpr int NT = D / 8;            // n-tiles of O
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = pa::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const smem = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = lane >> 2, qc = lane & 3;
+    const int mat = lane >> 3, mrow = lane & 7;
+    const int ld_tok = (mat & 1) * 8 + mrow;   // m0, m2: tokens 0-7; m1, m3: tokens 8-15
+    const int ld_chk = mat >> 1;               // m0, m1: chunk 2pp; m2, m3: chunk 2pp + 1
+    const int hkv = p.num_kv_heads, G = p.group, n_seqs = p.num_seqs;
+    int32_t* const cum = reinterpret_cast<int32_t*>(smem + kWorkerWarps * S * 8);
+    uint8_t* const chunks = reinterpret_cast<uint8_t*>(cum + n_seqs + 1);
+    const uint32_t bars = base + warp * S * 8;
+    const uint32_t ring = base + header_bytes(n_seqs, S) + warp * Lay::kRing;
+
+    build_prefix(cum, chunks, p);
+    const int64_t B = cum[n_seqs];
+    const int64_t wid = (int64_t)blockIdx.x * kWorkerWarps + warp;
+    const int64_t f0 = share_start(wid, B, p.workers);
+    const int64_t f1 = share_start(wid + 1, B, p.workers);
+    const int n = (int)(f1 - f0);
+    if (n <= 0) return;
+
+    uint64_t pol_once = 0, pol_again = 0;
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i) pa::mbar_init(bars + 8 * i, 1);
+        pa::fence_barrier_init();
+        pa::prefetch_tensormap(&tmap_k);
+        pa::prefetch_tensormap(&tmap_v);
+        pol_once = pa::policy_evict_first();
+        pol_again = pa::policy_evict_normal();
+    }
+    __syncwarp();
+
+    // each lane keeps the TMA row of virtual block win + lane and whether
+    // later row chunks read that block again
+    int win = -32, my_row = 0, my_once = 1;
+    auto refresh = [&](int wbase) {
+        win = wbase;
+        const int64_t f = f0 + wbase + lane;
+        my_row = 0;
+        my_once = 1;
+        if (f < f1) {
+            const Pos q = locate(cum, chunks, n_seqs, hkv, f);
+            int blk = __ldg(p.block_tables + (int64_t)q.s * p.max_blocks + first_block(p, q.s) +
+                            q.b);
+            if (blk < 0 || blk >= p.num_blocks) {
+                if (p.err) atomicOr(p.err, pa::ERR_BAD_BLOCK);
+                blk = 0;
+            }
+            my_row = (blk * hkv + q.g) * kBS;
+            my_once = q.C == 1;
+        }
+    };
+    auto issue = [&](int k) {   // warp-uniform
+        if (k >= win + 32) refresh(k & ~31);
+        const int row = __shfl_sync(0xffffffffu, my_row, k - win);
+        const int once = __shfl_sync(0xffffffffu, my_once, k - win);
+        if (lane == 0) {
+            const uint32_t bar = bars + 8 * (k % S);
+            const uint32_t dst = ring + (k % S) * Lay::kStage;
+            const uint64_t pol = once ? pol_once : pol_again;
+            pa::mbar_arrive_expect_tx(bar, 2 * Lay::kTile);
+            pa::tma_load_2d(dst, &tmap_k, 0, row, bar, pol);
+            pa::tma_load_2d(dst + Lay::kTile, &tmap_v, 0, row, bar, pol);
+        }
+    };
+    int issued = 0;
+    for (; issued < S && issued < n; ++issued) issue(issued);
+
+    Pos cur = locate(cum, chunks, n_seqs, hkv, f0);
+    float o[NT][4];
+    float m_run[2], l_run[2], rowmul[2], vsc = 0.f;
+    uint32_t qa[KCH][4];
+    int L = 0, r = 1, q0 = 0, rows = 0, row_off = 0, seg_b0 = cur.b, sb = 0, last_q = 0;
+    bool seg_first = true;
+
+    // Segment start: this warp's 16 q rows as fp16 A fragments, each row
+    // scaled by 2^(14 - e_row); the lane's dims of k-step ks are 16 ks + 4 qc
+    // .. + 3, placed at MMA k positions (2 qc, 2 qc + 1) and (2 qc + 8, 2 qc +
+    // 9) -- the order in which a K fragment holds the code bytes.
+    auto start_segment = [&]() {
+        L = __ldg(p.context_lens + cur.s);
+        r = query_run(p.qsl, cur.s, &q0);
+        sb = first_block(p, cur.s);
+        last_q = L - r;
+        row_off = cur.c * kBS;
+        rows = min(kBS, G * r - row_off);
+        const float ksc = __ldg(x.k_scale + cur.g);
+        vsc = __ldg(x.v_scale + cur.g);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = quad + 8 * h;
+            float v[KCH][4];
+            if (row < rows) {
+                const int gr = row_off + row;
+                const TQ* src = static_cast<const TQ*>(p.q) +
+                                ((int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G) * D +
+                                4 * qc;
+#pragma unroll
+                for (int ks = 0; ks < KCH; ++ks) {
+                    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + 16 * ks));
+                    const TQ* t = reinterpret_cast<const TQ*>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[ks][e] = (float)t[e];
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < KCH; ++ks)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[ks][e] = 0.f;
+            }
+            float mx = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KCH; ++ks)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(v[ks][e]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            int ex = 0;
+            if (mx > 0.f) {
+                ex = (int)((__float_as_uint(mx) >> 23) & 0xff) - 127;   // floor(log2 max|q|)
+                ex = max(-100, min(100, ex));
+            }
+            const float up = exp2i(14 - ex);
+#pragma unroll
+            for (int ks = 0; ks < KCH; ++ks) {
+                __half2 lo = __floats2half2_rn(v[ks][0] * up, v[ks][1] * up);
+                __half2 hi = __floats2half2_rn(v[ks][2] * up, v[ks][3] * up);
+                qa[ks][h] = *reinterpret_cast<uint32_t*>(&lo);
+                qa[ks][2 + h] = *reinterpret_cast<uint32_t*>(&hi);
+            }
+            rowmul[h] = row < rows ? p.scale_log2 * exp2i(ex - 14) * ksc : 0.f;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+    };
+
+    auto finish_segment = [&](bool complete, int slot_idx, int tok_end) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+        }
+        Slot sl(p.slots + (2 * wid + slot_idx) * (int64_t)p.slot_bytes, kBS);
+        if (!complete && lane == 0) {
+            sl.hdr[0] = cur.s;
+            sl.hdr[1] = cur.g;
+            sl.hdr[2] = cur.c;
+            sl.hdr[3] = (sb + seg_b0) * kBS;
+            sl.hdr[4] = tok_end;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = quad + 8 * h;
+            if (row >= rows) continue;
+            const float mul = complete ? vsc / l_run[h] : vsc;
+            int64_t obase = 0;
+            if (complete) {
+                const int gr = row_off + row;
+                obase = ((int64_t)(q0 + gr / G) * p.num_heads + cur.g * G + gr % G) * D;
+            } else if (qc == 0) {
+                sl.m[row] = m_run[h];
+                sl.l[row] = l_run[h];
+            }
+#pragma unroll
+            for (int c = 0; c < KCH; ++c) {
+                // n-tile 2c holds dims 16c + 4qc and + 2, n-tile 2c + 1 dims + 1 and + 3
+                const float4 v = make_float4(o[2 * c][2 * h] * mul, o[2 * c + 1][2 * h] * mul,
+                                             o[2 * c][2 * h + 1] * mul,
+                                             o[2 * c + 1][2 * h + 1] * mul);
+                const int col = 16 * c + 4 * qc;
+                if (!complete) {
+                    *reinterpret_cast<float4*>(sl.o + (int64_t)row * D + col) = v;
+                } else if (p.out_f32) {
+                    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + col) = v;
+                } else {
+                    TQ* o16 = static_cast<TQ*>(p.out) + obase + col;
+                    if constexpr (std::is_same<TQ, __half>::value) {
+                        *reinterpret_cast<__half2*>(o16) = __floats2half2_rn(v.x, v.y);
+                        *reinterpret_cast<__half2*>(o16 + 2) = __floats2half2_rn(v.z, v.w);
+                    } else {
+                        *reinterpret_cast<__nv_bfloat162*>(o16) = __floats2bfloat162_rn(v.x, v.y);
+                        *reinterpret_cast<__nv_bfloat162*>(o16 + 2) =
+                            __floats2bfloat162_rn(v.z, v.w);
+                    }
+                }
+            }
+        }
+    };
+
+    start_segment();
+    int consumed = 0;
+    for (int k = 0; k < n; ++k) {
+        const int st = k % S;
+        if (!pa::mbar_wait(bars + 8 * st, (k / S) & 1, p.err, pa::ERR_WAIT_FULL)) break;
+        consumed = k + 1;
+        const uint32_t kb = ring + st * Lay::kStage, vb = kb + Lay::kTile;
+        const int tok0 = (sb + cur.b) * kBS;
+
+        // ---- S = Q K^T over the block's 16 tokens (two n-tiles of 8) ----
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int pp = 0; pp < KCH / 2; ++pp) {
+            uint32_t rr[4];
+            pa::ldmatrix_x4(kb + tile8_offset<D>(ld_tok, 2 * pp + ld_chk), rr[0], rr[1], rr[2],
+                            rr[3]);
+            // rr[j]: k-step 2pp + j/2, tokens (j & 1) * 8 + quad, dims 4qc .. 4qc + 3
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mma_f16(s[j & 1], qa[2 * pp + (j >> 1)], e4m3x2_to_f16x2(rr[j]),
+                        e4m3x2_to_f16x2(rr[j] >> 16));
+        }
+
+        // ---- scales, mask, online softmax (lazy max) ----
+        const bool need_mask = tok0 + kBS - 1 > last_q;
+        float alpha[2];
+        bool rescale = false;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = quad + 8 * h;
+            const float rm = rowmul[h];
+            float a[4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) a[2 * nt + e] = s[nt][2 * h + e] * rm;
+            if (need_mask) {
+                const int bound = min(last_q + (row_off + row) / G, L - 1);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (tok0 + nt * 8 + 2 * qc + e > bound) a[2 * nt + e] = -INFINITY;
+            }
+            float mx = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            float al = 1.f;
+            if (mx > m_run[h] + kLazyMax) {
+                al = pa::ex2(m_run[h] - mx);         // 0 while m_run is -inf
+                m_run[h] = mx;
+                rescale = true;
+            }
+            const float m_use = m_run[h] == -INFINITY ? 0.f : m_run[h];
+            float sum = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float pv = pa::ex2(a[2 * nt + e] - m_use);
+                    s[nt][2 * h + e] = pv;
+                    sum += pv;
+                }
+            l_run[h] = l_run[h] * al + sum;
+            alpha[h] = al;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                o[nt][0] *= alpha[0];
+                o[nt][1] *= alpha[0];
+                o[nt][2] *= alpha[1];
+                o[nt][3] *= alpha[1];
+            }
+        }
+        uint32_t pa_[4];
+        {
+            __half2 h0 = __floats2half2_rn(s[0][0], s[0][1]);
+            __half2 h1 = __floats2half2_rn(s[0][2], s[0][3]);
+            __half2 h2 = __floats2half2_rn(s[1][0], s[1][1]);
+            __half2 h3 = __floats2half2_rn(s[1][2], s[1][3]);
+            pa_[0] = *reinterpret_cast<uint32_t*>(&h0);
+            pa_[1] = *reinterpret_cast<uint32_t*>(&h1);
+            pa_[2] = *reinterpret_cast<uint32_t*>(&h2);
+            pa_[3] = *reinterpret_cast<uint32_t*>(&h3);
+        }
+
+        // ---- O += P V ----
+        const int valid = L - tok0;   // tokens of this block inside the context (>= 1)
+        uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
+        if (valid < kBS) {
+            // codes past the context may hold anything (even NaN): zero them
+            const int t0 = 2 * qc, t1 = 2 * qc + 8;
+            keep0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+            keep1 = (t1 < valid ? 0x0000ffffu : 0u) | (t1 + 1 < valid ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int pp = 0; pp < KCH / 2; ++pp) {
+            uint32_t rr[4];
+            pa::ldmatrix_x4_trans(vb + tile8_offset<D>(ld_tok, 2 * pp + ld_chk), rr[0], rr[1],
+                                  rr[2], rr[3]);
+            // rr[2 half + 0]: tokens 2qc, 2qc + 1; rr[2 half + 1]: tokens 2qc + 8, + 9;
+            // bytes (t, dim 2 quad), (t, dim 2 quad + 1), (t + 1, 2 quad), (t + 1, 2 quad + 1)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int c = 2 * pp + half;
+                const uint32_t u0 = rr[2 * half] & keep0, u1 = rr[2 * half + 1] & keep1;
+                mma_f16(o[2 * c], pa_, e4m3x2_to_f16x2(prmt(u0, 0, 0x0020)),
+                        e4m3x2_to_f16x2(prmt(u1, 0, 0x0020)));
+                mma_f16(o[2 * c + 1], pa_, e4m3x2_to_f16x2(prmt(u0, 0, 0x0031)),
+                        e4m3x2_to_f16x2(prmt(u1, 0, 0x0031)));
+            }
+        }
+        __syncwarp();
+        if (issued < n) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(issued);
+            ++issued;
+        }
+        ++cur.b;
+        const bool seg_done = cur.b == cur.nbs;
+        if (seg_done || k == n - 1) {
+            finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
+                           min((sb + cur.b) * kBS, L));
+            if (k == n - 1) break;
+            next_segment(cur, cum, chunks, n_seqs, hkv);
+            seg_b0 = 0;
+            seg_first = false;
+            start_segment();
+        }
+    }
+    // drain: no copy of this warp may still be in flight when it exits
+    for (int k = consumed; k < issued; ++k)
+        if (!pa::mbar_wait(bars + 8 * (k % S), (k / S) & 1, p.err, pa::ERR_WAIT_DRAIN)) break;
+}
+
+template <typename TQ, int D>
+pa_status launch_fp8(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                     pa::sched::Params prm, const Fp8Scales& x) {
+    using Lay = Fp8Layout<D>;
+    auto kern = paged_decode_fp8_kernel<TQ, D>;
+    static bool attr_set = false;   // per instantiation; benign race (idempotent)
+    if (!attr_set) {
+        if (pa_status s = pa::cuda_status(
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Lay::smem_bytes(pa::kBalancedMaxSeqs)),
+                "fp8 decode: set shared memory size"))
+            return s;
+        attr_set = true;
+    }
+    const int smem = Lay::smem_bytes(a.num_seqs);
+    int dev = 0, sms = 0, ctas = 0;
+    if (pa_status s = pa::cuda_status(cudaGetDevice(&dev), "cudaGetDevice")) return s;
+    if (pa_status s = pa::cuda_status(
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count"))
+        return s;
+    if (pa_status s = pa::cuda_status(
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, kern, kWorkerWarps * 32, smem),
+            "occupancy query"))
+        return s;
+    if (ctas < 1) return pa::fail(PA_ERR_UNSUPPORTED, "fp8 decode kernel does not fit on an SM");
+    const pa::BalancedShape shape = pa::balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
+                                                       a.head_dim, a.max_q_len, a.max_context_len,
+                                                       pa::kTileFp8);
+    const int64_t workers =
+        std::min<int64_t>((int64_t)ctas * sms * kWorkerWarps, shape.workers);
+    prm.workers = (int)workers;
+    const int grid = (int)((workers + kWorkerWarps - 1) / kWorkerWarps);
+    if (pa_status s = pa::cuda_status(
+            pa::launch_pdl(kern, dim3(grid), dim3(kWorkerWarps * 32), smem, a.stream, mk, mv, prm,
+                           x),
+            "fp8 decode launch"))
+        return s;
+    const int row_slots = (int)std::min<int64_t>(kBS, (int64_t)(a.num_heads / a.num_kv_heads) *
+                                                          a.max_q_len);
+    const int64_t rctas = pa::sched::reduce_ctas(a.num_seqs, a.num_kv_heads, shape.max_chunks,
+                                                 row_slots);
+    if (rctas > 0x7fffffff) return pa::fail(PA_ERR_UNSUPPORTED, "reduce grid too large");
+    return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<TQ, D>,
+                                          dim3((unsigned)rctas), dim3(128), 0, a.stream, prm,
+                                          (int)shape.max_chunks, row_slots),
+                           "segment reduce launch");
+}
+
+}  // namespace
+
+namespace pa {
+
+pa_status launch_decode_fp8(const DecodeArgs& a) {
+    if (a.partition_size != 0)
+        return fail(PA_ERR_UNSUPPORTED, "FP8 caches use the balanced schedule (partition_size 0)");
+    if (pa_status s = balanced_check(a)) return s;
+    if (((uintptr_t)a.k_scale | (uintptr_t)a.v_scale) % 4)
+        return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be 4-byte aligned");
+    const BalancedShape shape = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
+                                               a.head_dim, a.max_q_len, a.max_context_len,
+                                               kTileFp8);
+    CUtensorMap mk, mv;
+    if (pa_status s = cache_tensor_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 1))
+        return s;
+    if (pa_status s = cache_tensor_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 1))
+        return s;
+    pa::sched::Params b{};
+    b.out = a.out;
+    b.q = a.q;
+    b.block_tables = a.block_tables;
+    b.context_lens = a.context_lens;
+    b.qsl = a.query_start_loc;
+    b.cum_out = static_cast<int32_t*>(a.slots);
+    b.slots = static_cast<uint8_t*>(a.slots) + shape.cum_bytes;
+    b.err = device_error_word();
+    b.max_blocks = a.max_blocks_per_seq;
+    b.num_heads = a.num_heads;
+    b.num_kv_heads = a.num_kv_heads;
+    b.group = a.num_heads / a.num_kv_heads;
+    b.num_seqs = a.num_seqs;
+    b.num_blocks = a.num_blocks;
+    b.rows_per_tile = shape.rows_per_tile;
+    b.slot_bytes = (int)shape.slot_bytes;
+    b.scale_log2 = a.scale * kLog2e;
+    b.out_f32 = a.out_dtype == PA_F32;
+    const Fp8Scales x{a.k_scale, a.v_scale};
+    if (a.q_dtype == PA_BF16)
+        return a.head_dim == 128 ? launch_fp8<__nv_bfloat16, 128>(a, mk, mv, b, x)
+                                 : launch_fp8<__nv_bfloat16, 64>(a, mk, mv, b, x);
+    return a.head_dim == 128 ? launch_fp8<__half, 128>(a, mk, mv, b, x)
+                             : launch_fp8<__half, 64>(a, mk, mv, b, x);
+}
+
+}  // namespace pa

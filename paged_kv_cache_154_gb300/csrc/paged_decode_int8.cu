@@ -608,69 +608,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
 // host side
 // ---------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
 
-// INT8 cache as rows of head_dim bytes: [num_blocks * H_kv * 16][head_dim],
-// box = one (block, kv head) tile of 16 rows, 128-byte (d = 128) or 64-byte
-// (d = 64) swizzle.
-pa_status make_map8(CUtensorMap* m, const void* cache, int num_blocks, int hkv, int d) {
-    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-    if (!fn) return pa::fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-    const uint64_t rows = (uint64_t)num_blocks * hkv * kBS;
-    if (rows > 0x7fffffffull) return pa::fail(PA_ERR_UNSUPPORTED, "cache has too many rows for TMA");
-    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)d};
-    cuuint32_t box[2] = {(cuuint32_t)d, (cuuint32_t)kBS};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return pa::fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return PA_OK;
-}
-
-struct Map8Cache {
-    struct Entry {
-        const void* ptr;
-        int nb, hkv, d, dev;
-        CUtensorMap map;
-    };
-    std::mutex mu;
-    Entry e[16];
-    int n = 0, next = 0;
-    pa_status get(CUtensorMap* out, const void* ptr, int nb, int hkv, int d) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        std::lock_guard<std::mutex> lock(mu);
-        for (int i = 0; i < n; ++i)
-            if (e[i].ptr == ptr && e[i].nb == nb && e[i].hkv == hkv && e[i].d == d &&
-                e[i].dev == dev) {
-                *out = e[i].map;
-                return PA_OK;
-            }
-        CUtensorMap m;
-        if (pa_status s = make_map8(&m, ptr, nb, hkv, d)) return s;
-        e[next] = Entry{ptr, nb, hkv, d, dev, m};
-        next = (next + 1) % 16;
-        if (n < 16) ++n;
-        *out = m;
-        return PA_OK;
-    }
-};
-Map8Cache g_maps8;
 
 template <typename TQ, int D, int MT>
 pa_status launch8(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -699,7 +637,7 @@ pa_status launch8(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensor
     if (ctas < 1) return pa::fail(PA_ERR_UNSUPPORTED, "int8 decode kernel does not fit on an SM");
     const pa::BalancedShape shape = pa::balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
                                                        a.head_dim, a.max_q_len, a.max_context_len,
-                                                       true);
+                                                       pa::kTileInt8);
     // one share per CTA, every CTA resident at once
     const int64_t workers = std::min<int64_t>((int64_t)ctas * sms, shape.workers);
     prm.workers = (int)workers;
@@ -740,11 +678,12 @@ pa_status launch_decode_int8(const DecodeArgs& a) {
     if (((uintptr_t)a.k_scale | (uintptr_t)a.v_scale | (uintptr_t)a.k_zp | (uintptr_t)a.v_zp) % 16)
         return fail(PA_ERR_INVALID_ARG, "k_scale, v_scale, k_zp and v_zp must be 16-byte aligned");
     const BalancedShape shape = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
-                                               a.head_dim, a.max_q_len, a.max_context_len, true);
+                                               a.head_dim, a.max_q_len, a.max_context_len,
+                                               kTileInt8);
     CUtensorMap mk, mv;
-    if (pa_status s = g_maps8.get(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim))
+    if (pa_status s = cache_tensor_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 1))
         return s;
-    if (pa_status s = g_maps8.get(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim))
+    if (pa_status s = cache_tensor_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 1))
         return s;
     pa::sched::Params b{};
     b.out = a.out;

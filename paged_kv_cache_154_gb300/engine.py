@@ -22,7 +22,8 @@ import torch
 from . import (BLOCK_SIZE, Pool, append_kv, copy_blocks, decode, decode_shared_prefix,
                decode_shared_prefix_workspace_size, decode_workspace_size)
 
-KV_TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "int8": torch.int8}
+KV_TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "int8": torch.int8,
+            "fp8": torch.float8_e4m3fn}
 
 
 @dataclass
@@ -58,7 +59,9 @@ class SharedPrefix:
 class PagedKVCache:
     def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, kv_dtype: str,
                  device="cuda", free_order: Optional[Sequence[int]] = None,
-                 canary_blocks: int = 0, canary_byte: int = 0):
+                 canary_blocks: int = 0, canary_byte: int = 0, head_scales=None):
+        """head_scales: FP8 caches only, (k_scale, v_scale) per KV head (fp32,
+        calibrated by the caller)."""
         self.num_blocks = num_blocks
         self.num_kv_heads = num_kv_heads
         self.head_dim = head_dim
@@ -75,6 +78,12 @@ class PagedKVCache:
             self.v_scale = torch.zeros(shp[:3], dtype=torch.float32, device=self.device)
             self.k_zp = torch.zeros(shp[:3], dtype=torch.int8, device=self.device)
             self.v_zp = torch.zeros(shp[:3], dtype=torch.int8, device=self.device)
+        if kv_dtype == "fp8":
+            if head_scales is None:
+                raise ValueError("an FP8 cache needs per-head scales (k_scale, v_scale)")
+            ks, vs = head_scales
+            self.k_scale = torch.as_tensor(np.asarray(ks, np.float32)).to(self.device)
+            self.v_scale = torch.as_tensor(np.asarray(vs, np.float32)).to(self.device)
         if canary_blocks:
             for t in self.arrays():
                 t[num_blocks:].view(torch.uint8).fill_(canary_byte)

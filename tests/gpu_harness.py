@@ -11,7 +11,7 @@ import workloads as W
 import paged_kv_cache_154_gb300 as pa
 from paged_kv_cache_154_gb300.engine import PagedKVCache
 
-TOL = {"f16": 2e-3, "bf16": 2e-3, "int8": 1e-2}   # max abs error on attention outputs
+TOL = {"f16": 2e-3, "bf16": 2e-3, "int8": 1e-2, "fp8": 2e-3}   # max abs error on attention outputs
 THREADS = os.cpu_count() or 1
 
 
@@ -28,7 +28,7 @@ def run_both(wl, partition_size=0, out_dtype=torch.float32, oracle_run=None,
                                    canary_byte=W.CANARY_BYTE)
     cache = PagedKVCache(wl.num_blocks, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
                          free_order=wl.free_order, canary_blocks=W.CANARY_BLOCKS,
-                         canary_byte=W.CANARY_BYTE)
+                         canary_byte=W.CANARY_BYTE, head_scales=wl.head_scales)
     names = {}
     for ops, oslots, opairs in zip(wl.phases, ref.phase_slots, ref.phase_pairs):
         slots, pairs = cache.run_phase(ops, names)

@@ -236,7 +236,7 @@ def best_of_n(name: str, seed: int, num_groups: int, n_forks: int,
     """
     rng = np.random.default_rng(seed)
     vals = _Values(seed)
-    src = TORCH_DTYPES[kv_dtype]
+    src = torch.bfloat16 if kv_dtype in ("int8", "fp8") else TORCH_DTYPES[kv_dtype]
     s_extra = rng.integers(1, shared_extra_max + 1, size=num_groups)
     private = rng.integers(0, private_max + 1, size=(num_groups, n_forks))
     private[:, 0] = 0
@@ -291,7 +291,9 @@ def best_of_n(name: str, seed: int, num_groups: int, n_forks: int,
                     step=step, q=q, context_lens=context_lens,
                     partition_size=partition_size,
                     notes={"shared_extra": s_extra.tolist(),
-                           "private": private.tolist()})
+                           "private": private.tolist()},
+                    head_scales=(calibrate_fp8([phase0, phase1], step, num_kv_heads)
+                                 if kv_dtype == "fp8" else None))
 
 
 # --------------------------------------------------------------------------
@@ -320,6 +322,17 @@ def llama3_8b(batch: int = 64, lo: int = 512, hi: int = 4096, shard: int = 0) ->
     lens = rng.integers(lo, hi + 1, size=batch)
     return simple("llama3_8b_decode", seed, lens, [1] * batch,
                   num_heads=32, num_kv_heads=8, head_dim=128, kv_dtype="bf16")
+
+
+def llama3_8b_fp8(batch: int = 64, lo: int = 512, hi: int = 4096, shard: int = 0) -> Workload:
+    """The Llama-3-8B-shaped decode step with an FP8 (E4M3) cache: 64
+    sequences, lengths U[512, 4096], 32 q / 8 KV heads, head_dim 128, bf16 q,
+    per-head scales calibrated on the appended data."""
+    seed = SEED_BASE + 6 + SHARD_STRIDE * shard
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, size=batch)
+    return simple("llama3_8b_fp8", seed, lens, [1] * batch, num_heads=32, num_kv_heads=8,
+                  head_dim=128, kv_dtype="fp8", q_dtype=torch.bfloat16)
 
 
 def llama2_70b_best_of_5(num_groups: int = 8, prompt_len: int = 4096,
@@ -364,6 +377,7 @@ NAMED = {
     "llama2_70b_best_of_5": llama2_70b_best_of_5,
     "long_context": long_context,
     "mixed_int8": mixed_int8,
+    "llama3_8b_fp8": llama3_8b_fp8,
 }
 
 
