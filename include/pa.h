@@ -138,6 +138,46 @@ pa_status pa_pool_stats(pa_pool* pool, int32_t* free_blocks, int32_t* used,
 /* Reference count of one physical block. */
 pa_status pa_pool_refcount(pa_pool* pool, int32_t block, int32_t* ref);
 
+/* ---- Prefix cache ([p1] §2.4: requests sharing a prefix reuse its KV,
+ * found by a hash of the prefix tokens, least recently used entries evicted;
+ * [p3]: hash(prefix_tokens) -> KV blocks). Per whole block: a full block is
+ * named by the complete token prefix that ends with it (looked up by a hash
+ * of (prefix of the previous block, this block's 16 token ids) and then
+ * compared token by token, so equal names mean equal prefixes). Off until
+ * enabled; the calls above behave exactly as before while it is off. ---- */
+
+/* Turn the prefix cache on (or change its size): up to max_cached_blocks
+ * registered blocks that no sequence holds are kept for reuse, oldest
+ * released first out. Allocation uses the free list first and evicts the
+ * oldest cached block only when the free list is empty; pa_pool_stats'
+ * free count does not include cached blocks. */
+pa_status pa_pool_enable_prefix_cache(pa_pool* pool, int32_t max_cached_blocks);
+
+/* A new sequence that starts with the longest chain of cached whole blocks
+ * matching token_ids[0 .. n_tokens) -- at most (n_tokens - 1) / 16 blocks, so
+ * at least one token is left to compute. *n_cached_out = tokens covered (a
+ * multiple of 16): the sequence holds them (refcounts raised) and its length
+ * is that; append the rest with pa_seq_append_tokens and write their K/V. */
+pa_status pa_seq_create_with_prefix(pa_pool* pool, const int32_t* token_ids,
+                                    int32_t n_tokens, int32_t* seq_out,
+                                    int32_t* n_cached_out);
+
+/* pa_seq_append_slots for tokens whose ids are known: every block the append
+ * fills is registered under its prefix (unless a block already holds that
+ * prefix), so later requests can reuse it. A sequence that ever took a plain
+ * pa_seq_append_slots registers nothing after that. Requires the prefix
+ * cache to be enabled. */
+pa_status pa_seq_append_tokens(pa_pool* pool, int32_t seq, const int32_t* token_ids,
+                               int32_t n_tokens, int64_t* slots_out,
+                               int32_t* cow_pair_out, int32_t* n_cow);
+
+/* cached_free = registered blocks no sequence holds (the LRU list),
+ * registered = blocks registered under a prefix, hit_blocks / lookup_blocks
+ * = blocks found / looked up by pa_seq_create_with_prefix. Any output may be
+ * NULL. */
+pa_status pa_pool_prefix_stats(pa_pool* pool, int32_t* cached_free, int32_t* registered,
+                               int64_t* hit_blocks, int64_t* lookup_blocks);
+
 /* Fork groups for pa_decode_shared_prefix ([p2] §2.1: best-of-N forks share
  * the prompt's blocks by reference count). Walks seqs[0..n) in order; a run
  * of adjacent sequences whose first physical block is the same forms one

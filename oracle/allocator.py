@@ -30,6 +30,7 @@ An append is all-or-nothing: if the free list cannot cover it, nothing changes.
 """
 from __future__ import annotations
 
+from collections import OrderedDict
 from typing import Dict, List, Optional, Sequence, Tuple
 
 
@@ -57,6 +58,19 @@ class BlockPool:
         self.tables: Dict[int, List[int]] = {}
         self.lens: Dict[int, int] = {}
         self._next = 0
+        # prefix cache (see enable_prefix_cache)
+        self.pc_on = False
+        self.pc_max = 0
+        self.nodes: Dict[int, list] = {}          # id -> [parent, tokens, block, children]
+        self.edges: Dict[tuple, int] = {}         # (parent, tokens) -> id
+        self.next_node = 0
+        self.block_node: Dict[int, int] = {}      # registered block -> node
+        self.lru: "OrderedDict[int, None]" = OrderedDict()   # oldest first
+        self.seq_nodes: Dict[int, List[int]] = {}
+        self.seq_tail: Dict[int, List[int]] = {}
+        self.seq_known: Dict[int, bool] = {}
+        self.hits = 0
+        self.lookups = 0
 
     # -- sequences ---------------------------------------------------------
     def create(self) -> int:
@@ -64,6 +78,9 @@ class BlockPool:
         self._next += 1
         self.tables[sid] = []
         self.lens[sid] = 0
+        self.seq_nodes[sid] = []
+        self.seq_tail[sid] = []
+        self.seq_known[sid] = True
         return sid
 
     def _get(self, sid: int) -> List[int]:
@@ -76,6 +93,9 @@ class BlockPool:
         child = self.create()
         self.tables[child] = list(table)
         self.lens[child] = self.lens[parent]
+        self.seq_nodes[child] = list(self.seq_nodes[parent])
+        self.seq_tail[child] = list(self.seq_tail[parent])
+        self.seq_known[child] = self.seq_known[parent]
         for b in table:
             self.ref[b] += 1
         return child
@@ -91,12 +111,13 @@ class BlockPool:
             return [], None
         cow = (L % bs != 0) and self.ref[table[-1]] > 1
         new_blocks = -(-(L + n) // bs) - len(table)
-        if new_blocks + (1 if cow else 0) > len(self.free):
-            raise OutOfBlocks(f"need {new_blocks + int(cow)} blocks, {len(self.free)} free")
+        avail = len(self.free) + len(self.lru)
+        if new_blocks + (1 if cow else 0) > avail:
+            raise OutOfBlocks(f"need {new_blocks + int(cow)} blocks, {avail} free")
         pair = None
         if cow:
             src = table[-1]
-            dst = self.free.pop()
+            dst = self._take()
             self.ref[src] -= 1
             self.ref[dst] = 1
             table[-1] = dst
@@ -105,12 +126,16 @@ class BlockPool:
         for i in range(n):
             pos = L + i
             if pos >= len(table) * bs:
-                b = self.free.pop()
+                b = self._take()
                 self.ref[b] = 1
                 table.append(b)
             slots.append(table[pos // bs] * bs + pos % bs)
         self.lens[sid] = L + n
+        if n > 0 and not self._with_tokens:
+            self.seq_known[sid] = False          # tokens unknown: nothing more to register
         return slots, pair
+
+    _with_tokens = False
 
     def release(self, sid: int) -> None:
         table = self._get(sid)
@@ -120,9 +145,12 @@ class BlockPool:
         for b in table:
             self.ref[b] -= 1
             if self.ref[b] == 0:
-                self.free.append(b)
+                self._release(b)
         del self.tables[sid]
         del self.lens[sid]
+        del self.seq_nodes[sid]
+        del self.seq_tail[sid]
+        del self.seq_known[sid]
 
     # -- views -------------------------------------------------------------
     def block_table(self, sid: int) -> List[int]:
@@ -176,4 +204,131 @@ class BlockPool:
             i = j
         starts.append(len(seqs))
         return starts, prefixes
+
+    # -- prefix cache ------------------------------------------------------
+    # Page 1 ("大模型推理优化全攻略" §2.4) sketches a prefix KV cache: a hash of
+    # the prefix tokens finds the cached KV, lookups refresh an entry, and an
+    # ordered dict evicts the least recently used one past a capacity; page 3
+    # states the mapping hash(prefix_tokens) -> KV blocks. Restated per block:
+    # a full block is named by the whole token prefix ending with it, a trie
+    # node (parent node, the block's tokens); blocks no sequence holds wait in
+    # an LRU of at most max_cached_blocks, and allocation evicts its oldest
+    # entry only when the free list is empty.
+
+    def enable_prefix_cache(self, max_cached_blocks: int) -> None:
+        if max_cached_blocks < 0:
+            raise ValueError("max_cached_blocks < 0")
+        self.pc_on = True
+        self.pc_max = max_cached_blocks
+        while len(self.lru) > self.pc_max:
+            old, _ = self.lru.popitem(last=False)
+            self._unregister(old)
+            self.free.append(old)
+
+    def _take(self) -> int:
+        if self.free:
+            return self.free.pop()
+        b, _ = self.lru.popitem(last=False)
+        self._unregister(b)
+        return b
+
+    def _release(self, b: int) -> None:
+        if b not in self.block_node:
+            self.free.append(b)
+            return
+        self.lru[b] = None
+        if len(self.lru) > self.pc_max:
+            old, _ = self.lru.popitem(last=False)
+            self._unregister(old)
+            self.free.append(old)
+
+    def _unregister(self, b: int) -> None:
+        nid = self.block_node.pop(b, None)
+        if nid is None:
+            return
+        self.nodes[nid][2] = -1
+        while nid >= 0 and nid in self.nodes:
+            parent, tokens, block, children = self.nodes[nid]
+            if block >= 0 or children > 0:
+                return
+            del self.edges[(parent, tokens)]
+            del self.nodes[nid]
+            if parent >= 0:
+                self.nodes[parent][3] -= 1
+            nid = parent
+
+    def _node(self, parent: int, tokens: tuple) -> int:
+        nid = self.edges.get((parent, tokens))
+        if nid is None:
+            nid = self.next_node
+            self.next_node += 1
+            self.nodes[nid] = [parent, tokens, -1, 0]
+            self.edges[(parent, tokens)] = nid
+            if parent >= 0:
+                self.nodes[parent][3] += 1
+        return nid
+
+    def append_tokens(self, sid: int, tokens: Sequence[int]) -> Tuple[List[int], Optional[Tuple[int, int]]]:
+        """append_slots for known token ids; every block this fills is
+        registered under its prefix (unless that prefix already has a block)."""
+        if not self.pc_on:
+            raise ValueError("the prefix cache is not enabled")
+        L = self.lens[sid] if sid in self.lens else 0
+        self._with_tokens = True
+        try:
+            slots, pair = self.append_slots(sid, len(tokens))
+        finally:
+            self._with_tokens = False
+        if not self.seq_known[sid]:
+            return slots, pair
+        bs = self.block_size
+        tail, chain = self.seq_tail[sid], self.seq_nodes[sid]
+        for i, t in enumerate(tokens):
+            tail.append(int(t))
+            if len(tail) < bs:
+                continue
+            b = (L + i) // bs
+            parent = -1 if b == 0 else chain[b - 1]
+            if parent >= 0 and parent not in self.nodes:
+                self.seq_known[sid] = False
+                break
+            nid = self._node(parent, tuple(tail))
+            chain.append(nid)
+            blk = self.tables[sid][b]
+            if self.nodes[nid][2] < 0 and blk not in self.block_node:
+                self.nodes[nid][2] = blk
+                self.block_node[blk] = nid
+            tail.clear()
+        return slots, pair
+
+    def create_with_prefix(self, tokens: Sequence[int]) -> Tuple[int, int]:
+        """A new sequence holding the longest chain of cached whole blocks
+        that the tokens start with, leaving at least one token to compute.
+        Returns (sequence id, tokens already cached)."""
+        if not self.pc_on:
+            raise ValueError("the prefix cache is not enabled")
+        sid = self.create()
+        bs = self.block_size
+        parent = -1
+        b = 0
+        while (b + 1) * bs <= len(tokens) - 1:
+            self.lookups += 1
+            nid = self.edges.get((parent, tuple(int(t) for t in tokens[b * bs:(b + 1) * bs])))
+            if nid is None or self.nodes[nid][2] < 0:
+                break
+            blk = self.nodes[nid][2]
+            if self.ref[blk] == 0:
+                del self.lru[blk]
+            self.ref[blk] += 1
+            self.tables[sid].append(blk)
+            self.seq_nodes[sid].append(nid)
+            self.hits += 1
+            parent = nid
+            b += 1
+        self.lens[sid] = b * bs
+        return sid, b * bs
+
+    def prefix_stats(self) -> Tuple[int, int, int, int]:
+        """(cached unreferenced blocks, registered blocks, hit blocks, looked-up blocks)."""
+        return len(self.lru), len(self.block_node), self.hits, self.lookups
 

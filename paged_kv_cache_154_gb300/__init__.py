@@ -60,6 +60,10 @@ _SIGS = {
                             _I32, ctypes.c_float, _I32, _I32, _P], ctypes.c_int),
     "pa_device_error": ([_P, _P], ctypes.c_int),
     "pa_pool_prefix_groups": ([_P, _P, _I32, _P, _P, _P, _P], ctypes.c_int),
+    "pa_pool_enable_prefix_cache": ([_P, _I32], ctypes.c_int),
+    "pa_seq_create_with_prefix": ([_P, _P, _I32, _P, _P], ctypes.c_int),
+    "pa_seq_append_tokens": ([_P, _I32, _P, _I32, _P, _P, _P], ctypes.c_int),
+    "pa_pool_prefix_stats": ([_P, _P, _P, _P, _P], ctypes.c_int),
     "pa_decode_shared_prefix_workspace_size": ([_I32] * 11, _SZ),
     "pa_decode_shared_prefix": ([_P, ctypes.c_int, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P,
                                  _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
@@ -180,6 +184,39 @@ class Pool:
         out = _I32()
         _check(lib().pa_pool_refcount(self._h, block, ctypes.addressof(out)))
         return out.value
+
+    # -- prefix cache ------------------------------------------------------
+    def enable_prefix_cache(self, max_cached_blocks: int) -> None:
+        _check(lib().pa_pool_enable_prefix_cache(self._h, int(max_cached_blocks)))
+
+    def create_with_prefix(self, token_ids: Sequence[int]) -> Tuple[int, int]:
+        """pa_seq_create_with_prefix: (sequence id, tokens already cached)."""
+        t = np.ascontiguousarray(token_ids, dtype=np.int32)
+        sid, n = _I32(), _I32()
+        _check(lib().pa_seq_create_with_prefix(self._h, t.ctypes.data if len(t) else None,
+                                               len(t), ctypes.addressof(sid),
+                                               ctypes.addressof(n)))
+        return sid.value, n.value
+
+    def append_tokens(self, seq: int, token_ids: Sequence[int]
+                      ) -> Tuple[np.ndarray, Optional[Tuple[int, int]]]:
+        """pa_seq_append_tokens: (slots, copy pair or None)."""
+        t = np.ascontiguousarray(token_ids, dtype=np.int32)
+        slots = np.zeros(max(1, len(t)), np.int64)
+        pair = np.zeros(2, np.int32)
+        ncow = _I32()
+        _check(lib().pa_seq_append_tokens(self._h, seq, t.ctypes.data if len(t) else None,
+                                          len(t), slots.ctypes.data, pair.ctypes.data,
+                                          ctypes.addressof(ncow)))
+        return slots[:len(t)].copy(), ((int(pair[0]), int(pair[1])) if ncow.value else None)
+
+    def prefix_stats(self) -> Tuple[int, int, int, int]:
+        """(cached unreferenced blocks, registered blocks, hit blocks, looked-up blocks)."""
+        c, r = _I32(), _I32()
+        h, l = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().pa_pool_prefix_stats(self._h, ctypes.addressof(c), ctypes.addressof(r),
+                                          ctypes.addressof(h), ctypes.addressof(l)))
+        return c.value, r.value, h.value, l.value
 
     def prefix_groups(self, seqs: Sequence[int],
                       q_lens: Optional[Sequence[int]] = None) -> Tuple[np.ndarray, np.ndarray]:

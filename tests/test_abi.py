@@ -198,3 +198,103 @@ def test_prefix_groups_match_model_on_fork_trees():
                 assert pl[g] <= m.lens[s] - q_lens[i] + 1
     with pytest.raises(pa.PAError):
         c.prefix_groups([9999])
+
+
+def _trace_ops(rng, n_ops, prompts):
+    """A serving-like trace: requests share system prompts (page 1 §2.4's
+    example) and differ after them; some finish, some get forked."""
+    ops = []
+    for _ in range(n_ops):
+        u = rng.random()
+        if u < 0.45:
+            p = prompts[int(rng.integers(len(prompts)))]
+            user = rng.integers(0, 50, size=int(rng.integers(1, 40))).tolist()
+            ops.append(("req", p + user))
+        elif u < 0.65:
+            ops.append(("gen", int(rng.integers(1, 20))))
+        elif u < 0.75:
+            ops.append(("fork", None))
+        elif u < 0.80:
+            ops.append(("plain", int(rng.integers(1, 20))))
+        else:
+            ops.append(("free", None))
+    return ops
+
+
+@pytest.mark.parametrize("max_cached", [0, 8, 64])
+def test_prefix_cache_matches_model_on_serving_traces(max_cached):
+    rng = np.random.default_rng(17 + max_cached)
+    prompts = [rng.integers(0, 50, size=n).tolist() for n in (200, 64, 37, 16, 5)]
+    order = rng.permutation(180).astype(np.int32)
+    c = pa.Pool(180, 16, order)
+    m = BlockPool(180, 16, order)
+    c.enable_prefix_cache(max_cached)
+    m.enable_prefix_cache(max_cached)
+    live = []
+    for kind, arg in _trace_ops(rng, 1500, prompts):
+        try:
+            if kind == "req":
+                ms, mn = m.create_with_prefix(arg)
+                cs, cn = c.create_with_prefix(arg)
+                assert (cs, cn) == (ms, mn)
+                live.append(ms)
+                try:
+                    mslots, mp = m.append_tokens(ms, arg[mn:])
+                except OutOfBlocks:
+                    with pytest.raises(pa.PAError):
+                        c.append_tokens(cs, arg[cn:])
+                    raise
+                cslots, cp = c.append_tokens(cs, arg[cn:])
+                assert cslots.tolist() == mslots and cp == mp
+            elif kind == "gen" and live:
+                s = live[int(rng.integers(len(live)))]
+                toks = rng.integers(0, 50, size=arg).tolist()
+                try:
+                    mslots, mp = m.append_tokens(s, toks)
+                except OutOfBlocks:
+                    with pytest.raises(pa.PAError):
+                        c.append_tokens(s, toks)
+                    raise
+                cslots, cp = c.append_tokens(s, toks)
+                assert cslots.tolist() == mslots and cp == mp
+            elif kind == "plain" and live:
+                s = live[int(rng.integers(len(live)))]
+                try:
+                    mslots, mp = m.append_slots(s, arg)
+                except OutOfBlocks:
+                    with pytest.raises(pa.PAError):
+                        c.seq_append_slots(s, arg)
+                    raise
+                cslots, cp = c.seq_append_slots(s, arg)
+                assert cslots.tolist() == mslots and cp == mp
+            elif kind == "fork" and live:
+                p = live[int(rng.integers(len(live)))]
+                assert c.seq_fork(p) == m.fork(p)
+                live.append(m._next - 1)
+            elif kind == "free" and live:
+                s = live.pop(int(rng.integers(len(live))))
+                c.seq_free(s)
+                m.release(s)
+        except OutOfBlocks:
+            while len(live) > 3:                 # make room, then carry on
+                s = live.pop(0)
+                c.seq_free(s)
+                m.release(s)
+        assert c.stats() == m.stats()
+        assert c.prefix_stats() == m.prefix_stats()
+    for s in live:
+        mb = max(1, len(m.block_table(s)))
+        t, l = c.block_tables([s], mb)
+        assert t[0, :len(m.block_table(s))].tolist() == m.block_table(s)
+    assert m.hits > 50                           # the trace really reuses prefixes
+
+
+def test_prefix_cache_api_errors():
+    c = pa.Pool(8, 16)
+    with pytest.raises(pa.PAError):
+        c.create_with_prefix([1, 2, 3])          # not enabled
+    s = c.seq_create()
+    with pytest.raises(pa.PAError):
+        c.append_tokens(s, [1])
+    with pytest.raises(pa.PAError):
+        c.enable_prefix_cache(-1)

@@ -206,3 +206,53 @@ def test_prefix_groups_model_is_maximal_and_sound():
     # forks that are not adjacent form separate groups
     gs, pl = pool.prefix_groups([root, lone, a])
     assert gs == [0, 1, 2, 3] and pl == [0, 0, 0]
+
+
+def test_prefix_cache_model_reuses_exactly_the_same_prefixes():
+    """What the model promises: a reused block holds the very tokens the new
+    request starts with (the whole prefix up to that block, not just the
+    block's own 16 tokens), at least one token is left to compute, and a
+    different earlier token breaks the chain even when later blocks agree."""
+    pool = BlockPool(64, 16)
+    pool.enable_prefix_cache(16)
+    toks = list(range(100, 150))                     # 50 tokens: 3 full blocks + 2
+    a = pool.create()
+    pool.append_tokens(a, toks)
+    assert pool.prefix_stats()[1] == 3               # three full blocks registered
+    b, n = pool.create_with_prefix(toks + [7])
+    assert n == 48 and pool.block_table(b) == pool.block_table(a)[:3]
+    c, n = pool.create_with_prefix(toks[:48])        # exactly 3 blocks: keep one token
+    assert n == 32
+    d, n = pool.create_with_prefix([0] + toks[1:])   # first token differs
+    assert n == 0
+    e, n = pool.create_with_prefix(toks[:16] + [9] * 16 + toks[32:] + [1])
+    assert n == 16                                   # block 1 differs, block 2 unreachable
+    for s in (a, b, c, d, e):
+        pool.release(s)
+    assert pool.prefix_stats()[0] == 3               # registered blocks wait in the LRU
+
+
+def test_prefix_cache_model_lru_eviction_order():
+    """Released registered blocks leave in the order they were released
+    (oldest first) once the LRU is over capacity, and allocation takes the
+    free list before evicting anything."""
+    pool = BlockPool(6, 16, free_order=range(6))
+    pool.enable_prefix_cache(2)
+    seqs = []
+    for base in (0, 1000, 2000):
+        s = pool.create()
+        pool.append_tokens(s, list(range(base, base + 16)))   # one full block each
+        seqs.append(s)
+    blocks = [pool.block_table(s)[0] for s in seqs]
+    for s in seqs:
+        pool.release(s)
+    assert list(pool.lru) == blocks[1:]              # capacity 2: the first was evicted
+    assert pool.free[-1] == blocks[0]
+    s, n = pool.create_with_prefix(list(range(1000, 1016)) + [5])
+    assert n == 16 and list(pool.lru) == blocks[2:]  # a hit revives its block
+    t = pool.create()
+    assert len(pool.free) == 4
+    pool.append_slots(t, 16 * 4)                     # the four free blocks: no eviction
+    assert list(pool.lru) == blocks[2:]
+    pool.append_slots(t, 16)                         # free list empty: evict the oldest
+    assert list(pool.lru) == [] and pool.prefix_stats()[1] == 1
