@@ -1,4 +1,4 @@
-// The balanced decode schedule, shared by the 16-bit and the INT8 kernels.
+// The balanced decode schedule, shared by the 16-bit, INT8 and FP8 kernels.
 //
 // Work space. Each sequence s has nb_s = ceil(L_s / 16) blocks and R_s = G *
 // r_s query rows per KV head (G q heads per KV head, r_s query tokens). Rows
@@ -62,10 +62,6 @@ __device__ __forceinline__ int first_block(const Params& p, int s) {
     return p.ctx_start ? __ldg(p.ctx_start + s) / kBS : 0;
 }
 
-// Blocks a sequence attends: from first_block to the last block holding a token.
-__device__ __forceinline__ int blocks_of(const Params& p, int s) {
-    return max(0, (__ldg(p.context_lens + s) + kBS - 1) / kBS - first_block(p, s));
-}
 
 // A partial slot: int32 {seq, kv head, chunk, first token, end token, 0, 0, 0},
 // then fp32 m[RT] (base-2 units), l[RT], O[RT][D] (not normalised). Row j of a
@@ -102,6 +98,39 @@ __device__ __forceinline__ int chunks_of(const Params& p, int s) {
     return (p.group * r + p.rows_per_tile - 1) / p.rows_per_tile;
 }
 
+// Causal block skipping: row chunk c of a sequence (L tokens, a query run of
+// r, query i at position L - r + i) attends blocks first_block .. end - 1,
+// where end is the block holding the last key that the chunk's last query
+// row sees (all blocks with unmasked rows). A chunk of early queries of a
+// long run -- a prefill -- thus skips the blocks no row of it can see.
+__device__ __forceinline__ int chunk_blocks(const Params& p, int L, int r, int sb, int c) {
+    const int nb = (L + kBS - 1) / kBS;
+    int end = nb;
+    if (!p.unmasked) {
+        const int jmax = min(r - 1, ((c + 1) * p.rows_per_tile - 1) / p.group);
+        end = min(nb, (L - r + jmax) / kBS + 1);
+    }
+    return max(0, end - sb);
+}
+
+// Blocks of every row chunk of sequence s together (one kv head).
+__device__ __forceinline__ int seq_blocks(const Params& p, int s, int C) {
+    int q0;
+    const int L = __ldg(p.context_lens + s), r = query_run(p.qsl, s, &q0), sb = first_block(p, s);
+    int total = 0;
+    for (int c = 0; c < C; ++c) total += chunk_blocks(p, L, r, sb, c);
+    return total;
+}
+
+// Blocks of segment (s, c); a single-chunk sequence reads it off the prefix sums.
+__device__ __forceinline__ int segment_blocks(const Params& p, const int32_t* cum,
+                                              const uint8_t* chunks, int s, int c) {
+    if (chunks[s] == 1) return (cum[s + 1] - cum[s]) / p.num_kv_heads;
+    int q0;
+    const int r = query_run(p.qsl, s, &q0);
+    return chunk_blocks(p, __ldg(p.context_lens + s), r, first_block(p, s), c);
+}
+
 __host__ __device__ __forceinline__ int64_t share_start(int64_t w, int64_t B, int64_t W) {
     return w * B / W;
 }
@@ -112,8 +141,9 @@ __host__ __device__ __forceinline__ int header_bytes(int num_seqs, int stages) {
     return ((kWorkerWarps * stages * 8 + (num_seqs + 1) * 4 + num_seqs) + 1023) / 1024 * 1024;
 }
 
-// cum[s] = num_kv_heads * sum_{s' < s} C_s' * nb_s' and chunks[s] = C_s, by one
-// CTA; CTA 0 also copies cum to the workspace for the reduce kernel.
+// cum[s] = num_kv_heads * (blocks of all row chunks of the sequences before
+// s) and chunks[s] = C_s, by one CTA; CTA 0 also copies cum to the workspace
+// for the reduce kernel.
 static __device__ void build_prefix(int32_t* cum, uint8_t* chunks, const Params& p) {
     __shared__ int32_t warp_tot[32];
     pa::grid_dependents_launch();   // the reduce kernel may be scheduled early
@@ -126,7 +156,7 @@ static __device__ void build_prefix(int32_t* cum, uint8_t* chunks, const Params&
     for (int i = a; i < b; ++i) {
         const int c = chunks_of(p, i);
         chunks[i] = (uint8_t)c;
-        local += p.num_kv_heads * c * blocks_of(p, i);
+        local += p.num_kv_heads * seq_blocks(p, i, c);
     }
     const int lane = tid & 31, warp = tid >> 5;
     int32_t x = local;
@@ -151,7 +181,7 @@ static __device__ void build_prefix(int32_t* cum, uint8_t* chunks, const Params&
     int32_t run = x - local + (warp > 0 ? warp_tot[warp - 1] : 0);
     for (int i = a; i < b; ++i) {
         cum[i] = run;
-        run += p.num_kv_heads * chunks[i] * blocks_of(p, i);
+        run += p.num_kv_heads * seq_blocks(p, i, chunks[i]);
     }
     if (tid == nt - 1) cum[n] = run;
     __syncthreads();
@@ -164,8 +194,11 @@ struct Pos {
     int s, g, c, b, nbs, C;
 };
 
-__device__ __forceinline__ Pos locate(const int32_t* cum, const uint8_t* chunks, int n, int hkv,
+// Virtual blocks of a sequence are laid out kv head by kv head, and within a
+// kv head chunk by chunk, each chunk's blocks in order.
+__device__ __forceinline__ Pos locate(const Params& p, const int32_t* cum, const uint8_t* chunks,
                                       int64_t f) {
+    const int n = p.num_seqs;
     int lo = 0, hi = n;   // largest s with cum[s] <= f
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -175,28 +208,46 @@ __device__ __forceinline__ Pos locate(const int32_t* cum, const uint8_t* chunks,
     Pos q;
     q.s = lo;
     q.C = chunks[lo];
-    q.nbs = (cum[lo + 1] - cum[lo]) / (hkv * q.C);
+    const int span = (cum[lo + 1] - cum[lo]) / p.num_kv_heads;   // one kv head's blocks
     const int local = (int)(f - cum[lo]);
-    const int seg = local / q.nbs;
-    q.b = local - seg * q.nbs;
-    q.g = seg / q.C;
-    q.c = seg - q.g * q.C;
+    q.g = local / span;
+    int rem = local - q.g * span;
+    if (q.C == 1) {
+        q.c = 0;
+        q.nbs = span;
+    } else {
+        int q0;
+        const int L = __ldg(p.context_lens + lo), r = query_run(p.qsl, lo, &q0);
+        const int sb = first_block(p, lo);
+        for (q.c = 0;; ++q.c) {
+            q.nbs = chunk_blocks(p, L, r, sb, q.c);
+            if (rem < q.nbs || q.c == q.C - 1) break;
+            rem -= q.nbs;
+        }
+    }
+    q.b = rem;
     return q;
 }
 
-// The next segment after (s, g, c).
-__device__ __forceinline__ void next_segment(Pos& q, const int32_t* cum, const uint8_t* chunks,
-                                             int n, int hkv) {
+// The next segment after (s, g, c) that has blocks.
+__device__ __forceinline__ void next_segment(const Params& p, Pos& q, const int32_t* cum,
+                                             const uint8_t* chunks) {
     q.b = 0;
-    if (++q.c < q.C) return;
-    q.c = 0;
-    if (++q.g < hkv) return;
-    q.g = 0;
-    do {
-        ++q.s;
-    } while (q.s < n - 1 && cum[q.s + 1] == cum[q.s]);
-    q.C = chunks[q.s];
-    q.nbs = (cum[q.s + 1] - cum[q.s]) / (hkv * q.C);
+    for (;;) {
+        if (++q.c >= q.C) {
+            q.c = 0;
+            if (++q.g >= p.num_kv_heads) {
+                q.g = 0;
+                if (++q.s >= p.num_seqs) {
+                    q.nbs = 0;
+                    return;
+                }
+                q.C = chunks[q.s];
+            }
+        }
+        q.nbs = segment_blocks(p, cum, chunks, q.s, q.c);
+        if (q.nbs > 0) return;
+    }
 }
 
 template <typename T>
@@ -236,11 +287,15 @@ __global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p, int
     const int r = query_run(p.qsl, s, &q0);
     const int G = p.group, RT = p.rows_per_tile;
     if (row >= min(RT, G * r - c * RT)) return;    // before any 64-bit division
-    const int nbs = blocks_of(p, s);
+    const int L = __ldg(p.context_lens + s), sb = first_block(p, s);
+    const int nbs = chunk_blocks(p, L, r, sb, c);
     if (nbs == 0) return;                          // nothing attended: no output row
     const int64_t B = __ldg(p.cum_out + p.num_seqs);
     const int64_t W = p.workers;
-    const int64_t fa = __ldg(p.cum_out + s) + (int64_t)(g * C + c) * nbs;
+    int before = 0;                                // blocks of the chunks before c
+    for (int cc = 0; cc < c; ++cc) before += chunk_blocks(p, L, r, sb, cc);
+    const int span = (__ldg(p.cum_out + s + 1) - __ldg(p.cum_out + s)) / p.num_kv_heads;
+    const int64_t fa = __ldg(p.cum_out + s) + (int64_t)g * span + before;
     const int64_t fb = fa + nbs;
     const int64_t wa = ((fa + 1) * W - 1) / B;     // share holding virtual block fa
     const int64_t wb = (fb * W - 1) / B;           // share holding virtual block fb - 1

@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         const int64_t f = f0 + wbase + lane;
         my_row = 0;
         if (f < f1) {
-            const Pos q = locate(cum, chunks, n_seqs, hkv, f);
+            const Pos q = locate(p, cum, chunks, f);
             int blk = __ldg(p.block_tables + (int64_t)q.s * p.max_blocks + first_block(p, q.s) +
                             q.b);
             if (blk < 0 || blk >= p.num_blocks) {
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     for (; issued < S && issued < n; ++issued) issue(issued);
 
     // Consumer side: walk the share block by block, segment by segment.
-    Pos cur = locate(cum, chunks, n_seqs, hkv, f0);
+    Pos cur = locate(p, cum, chunks, f0);
     WarpAttn<T, D, MT> st;
     uint32_t qreg[MT == 1 ? kKSteps : 1][4];
     int L = 0, r = 1, q0 = 0, rows = 0, row_off = 0, seg_b0 = cur.b, sb = 0, last_q = 0;
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
             finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
                            min((sb + cur.b) * kBS, L));
             if (k == n - 1) break;
-            next_segment(cur, cum, chunks, n_seqs, hkv);
+            next_segment(p, cur, cum, chunks);
             seg_b0 = 0;
             seg_first = false;
             start_segment();
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
         my_row = 0;
         my_once = 1;
         if (f < f1) {
-            const Pos q = locate(cum, chunks, n_seqs, hkv, f);
+            const Pos q = locate(p, cum, chunks, f);
             int blk = __ldg(p.block_tables + (int64_t)q.s * p.max_blocks + first_block(p, q.s) +
                             q.b);
             if (blk < 0 || blk >= p.num_blocks) {
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
     if (warp == 0)
         for (; issued < S && issued < n; ++issued) issue(issued);
 
-    Pos cur = locate(cum, chunks, n_seqs, hkv, f0);
+    Pos cur = locate(p, cum, chunks, f0);
     // Q stays in shared memory (this warp's 16 rows) and is read with ldmatrix
     // per block: keeping the fragments in registers would cost 32 registers a
     // thread and one CTA per SM.
@@ -737,7 +737,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
             finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
                            min((sb + cur.b) * kBS, L));
             if (k == n - 1) break;
-            next_segment(cur, cum, chunks, n_seqs, hkv);
+            next_segment(p, cur, cum, chunks);
             seg_b0 = 0;
             seg_first = false;
             start_segment();

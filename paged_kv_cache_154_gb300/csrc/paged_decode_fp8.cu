@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         my_row = 0;
         my_once = 1;
         if (f < f1) {
-            const Pos q = locate(cum, chunks, n_seqs, hkv, f);
+            const Pos q = locate(p, cum, chunks, f);
             int blk = __ldg(p.block_tables + (int64_t)q.s * p.max_blocks + first_block(p, q.s) +
                             q.b);
             if (blk < 0 || blk >= p.num_blocks) {
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     int issued = 0;
     for (; issued < S && issued < n; ++issued) issue(issued);
 
-    Pos cur = locate(cum, chunks, n_seqs, hkv, f0);
+    Pos cur = locate(p, cum, chunks, f0);
     float o[NT][4];
     float m_run[2], l_run[2], rowmul[2], vsc = 0.f;
     uint32_t qa[KCH][4];
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
             finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
                            min((sb + cur.b) * kBS, L));
             if (k == n - 1) break;
-            next_segment(cur, cum, chunks, n_seqs, hkv);
+            next_segment(p, cur, cum, chunks);
             seg_b0 = 0;
             seg_first = false;
             start_segment();

@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
         const int64_t f = f0 + wb + lane;
         my_tile = 0;
         if (f < f1) {
-            const Pos q = locate(cum, chunks, n_seqs, hkv, f);
+            const Pos q = locate(p, cum, chunks, f);
             int blk = __ldg(p.block_tables + (int64_t)q.s * p.max_blocks + q.b);
             if (blk < 0 || blk >= p.num_blocks) {
                 if (p.err) atomicOr(p.err, pa::ERR_BAD_BLOCK);
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
     if (warp == 0)
         for (; issued < S && issued < n; ++issued) issue(issued);
 
-    Pos cur = locate(cum, chunks, n_seqs, hkv, f0);
+    Pos cur = locate(p, cum, chunks, f0);
     float o[NT][4];
     float m_run[2], l_run[2], rowmul[2];
     uint32_t qa[QA][4];
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
             if (__syncthreads_or(aborted)) break;       // a CTA-wide decision
             finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1, min(cur.b * kBS, L));
             if (k == n - 1) break;
-            next_segment(cur, cum, chunks, n_seqs, hkv);
+            next_segment(p, cur, cum, chunks);
             seg_b0 = 0;
             seg_first = false;
             start_segment();

@@ -322,3 +322,39 @@ def test_graph_replay_matches_eager():
     assert pa.device_error() == 0
     assert torch.equal(si.out, eager)
     check_cache_bits(ref, cache)
+
+
+PREFILL = [
+    # name, lens (post-append), q_lens, H, Hkv, d, dtype: chunked prefill over cached context
+    ("prefill_fresh_gqa4", [64, 200, 128], [64, 200, 128], 32, 8, 128, "bf16"),
+    ("prefill_over_context", [164, 900, 1000], [64, 200, 128], 32, 8, 128, "bf16"),
+    ("prefill_mha_d64_f16", [300, 90], [150, 90], 8, 8, 64, "f16"),
+    ("prefill_mqa", [400, 333], [96, 33], 32, 1, 128, "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL, ids=lambda c: c[0])
+def test_paged_prefill_matches_oracle(case):
+    """Long query runs (prefill chunks): causal attention over the paged cache,
+    row chunks skip the blocks none of their queries can see."""
+    name, lens, qlens, H, Hkv, d, dt = case
+    wl = W.simple(name, 600 + len(lens), lens, qlens, H, Hkv, d, dt)
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, dt)
+
+
+@pytest.mark.parametrize("kv", ["int8", "fp8"])
+def test_paged_prefill_quantised_caches(kv):
+    wl = W.simple("prefill_" + kv, 610, [300, 700], [120, 64], 32, 8, 128, kv,
+                  q_dtype=torch.bfloat16)
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, kv)
+
+
+@pytest.mark.slow
+def test_paged_prefill_config():
+    wl = W.paged_prefill()
+    ref, cache, si, out = run_both(wl)
+    check_out(ref, out, "bf16")

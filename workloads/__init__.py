@@ -335,6 +335,20 @@ def llama3_8b_fp8(batch: int = 64, lo: int = 512, hi: int = 4096, shard: int = 0
                   head_dim=128, kv_dtype="fp8", q_dtype=torch.bfloat16)
 
 
+def paged_prefill(batch: int = 8, chunk: int = 512, prior_max: int = 4096,
+                  shard: int = 0) -> Workload:
+    """Chunked prefill over the paged cache, Llama-3-8B-shaped (32 q / 8 KV
+    heads, head_dim 128, bf16): 8 sequences that already hold U[0, 4096]
+    cached tokens each append a chunk of 512 prompt tokens and attend them
+    causally (query i of the chunk sees the prior tokens and chunk tokens
+    0 .. i): 2048 query rows per KV head."""
+    seed = SEED_BASE + 7 + SHARD_STRIDE * shard
+    rng = np.random.default_rng(seed)
+    prior = rng.integers(0, prior_max + 1, size=batch)
+    return simple("paged_prefill_llama3_8b", seed, prior + chunk, [chunk] * batch,
+                  num_heads=32, num_kv_heads=8, head_dim=128, kv_dtype="bf16")
+
+
 def llama2_70b_best_of_5(num_groups: int = 8, prompt_len: int = 4096,
                          shard: int = 0) -> Workload:
     """Llama-2-70B-shaped best-of-5: 8 prompts of 4096 (+1..15 shared) tokens,
@@ -378,6 +392,7 @@ NAMED = {
     "long_context": long_context,
     "mixed_int8": mixed_int8,
     "llama3_8b_fp8": llama3_8b_fp8,
+    "paged_prefill": paged_prefill,
 }
 
 
