@@ -21,6 +21,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "pa_internal.h"
 #include "ptx.cuh"
 
@@ -261,14 +263,192 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int o
     }
 }
 
-// Merges the pieces of every cut segment. One warp per (sequence, kv head,
+// Merge records. A segment that share boundaries cut has its first piece in
+// the share where it starts (share wa); that share's worker owns the merge.
+// Every worker writes, on every call, words 5..7 of its second slot's header:
+// {1, wb, slot of the first piece} for an owner (wb = the share holding the
+// segment's last block), {0, 0, 0} otherwise; an owner also writes words 5, 6
+// of its first slot's header: the segment's first query token and its rows in
+// the tile. With the first piece's own header {sequence, kv head, chunk, ..}
+// this is all the reduce needs, in one round of loads.
+__device__ __forceinline__ void write_merge_record(const Params& p, int64_t wid, int owner,
+                                                   int64_t wb, int first_slot, int q0 = 0,
+                                                   int rows = 0) {
+    if (wid >= p.workers) return;
+    int32_t* h1 = reinterpret_cast<int32_t*>(p.slots + (2 * wid + 1) * (int64_t)p.slot_bytes);
+    h1[5] = owner;
+    h1[6] = (int32_t)wb;
+    h1[7] = first_slot;
+    if (owner) {
+        int32_t* h0 = reinterpret_cast<int32_t*>(p.slots + 2 * wid * (int64_t)p.slot_bytes);
+        h0[5] = q0;
+        h0[6] = rows;
+    }
+}
+
+// Called at the end of a share: is its last segment cut after the share (not
+// all of its blocks done) and did it start in this share (its first piece
+// here)? Then this worker owns the merge; wb = the share holding its last
+// block, at virtual index f1 + (blocks left) - 1.
+__device__ __forceinline__ void record_last_segment(const Params& p, int64_t wid, int64_t f1,
+                                                    int64_t B, bool seg_done, int seg_b0,
+                                                    int blocks_left, bool seg_first, int q0,
+                                                    int rows) {
+    if (!seg_done && seg_b0 == 0) {
+        const int64_t fb = f1 + blocks_left;                 // one past the segment's end
+        write_merge_record(p, wid, 1, (fb * p.workers - 1) / B, seg_first ? 0 : 1, q0, rows);
+    }
+}
+
+// Merges the pieces of every cut segment: one CTA of eight warps per worker,
+// reading the worker's two slot headers in one round; a non-owner returns at
+// once. The owner's segment is merged row by row; when it has fewer than
+// eight rows the warps of a row split its pieces (warp j folds pieces j,
+// j + wpr, ...) and meet in shared memory. A lane owns D / 32 columns. Pieces
+// are read four at a time (independent loads) and folded into an online
+// log-sum-exp: out = sum 2^(m - M) O / sum 2^(m - M) l. At most 64 registers
+// a thread, so four CTAs fit on an SM.
+constexpr int kReduceWarps = 8;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kReduceWarps, 4) segment_reduce_kernel(const Params p) {
+    constexpr int EPL = D / 32;
+    constexpr int kBatch = 4;
+    __shared__ int32_t hdr[17];                     // slot 0 words 0..7, slot 1 words 0..7, B
+    __shared__ float part[kReduceWarps][D + 2];
+    pa::grid_dependency_wait();     // the decode kernel's partials must be complete
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t w = blockIdx.x;
+    if (w >= p.workers) return;
+    if (threadIdx.x < 16)
+        hdr[threadIdx.x] = __ldg(reinterpret_cast<const int32_t*>(
+                                     p.slots + (2 * w + (threadIdx.x >> 3)) *
+                                                   (int64_t)p.slot_bytes) +
+                                 (threadIdx.x & 7));
+    else if (threadIdx.x == 16)
+        hdr[16] = __ldg(p.cum_out + p.num_seqs);
+    __syncthreads();
+    if (hdr[8 + 5] != 1) return;                    // not the owner of a cut segment
+    const int64_t wb = hdr[8 + 6];
+    const int first_slot = hdr[8 + 7];
+    const int32_t* piece = hdr + 8 * first_slot;
+    const int g = piece[1], c = piece[2];
+    const int q0 = hdr[5], rows = hdr[6];
+    const int RT = p.rows_per_tile, G = p.group;
+    const int64_t W = p.workers;
+    const int64_t B = hdr[16];
+    const bool may_be_empty = B < W;                 // only then can a share hold no block
+    // warps per row: 1 with eight rows or more, else up to 8 / rows
+    const int wpr = rows >= 8 ? 1 : (rows >= 4 ? 2 : (rows >= 2 ? 4 : 8));
+    const int rows_per_round = kReduceWarps / wpr;
+    for (int row0 = 0; row0 < rows; row0 += rows_per_round) {
+        const int row = row0 + warp / wpr, sub = warp % wpr;
+        const bool active = row < rows;
+        float M = -INFINITY, den = 0.f, acc[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+        if (active) {
+            for (int64_t w0 = w + sub; w0 <= wb; w0 += (int64_t)kBatch * wpr) {
+                float lv[kBatch], mv[kBatch], ov[kBatch][EPL];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int64_t x = w0 + (int64_t)j * wpr;
+                    bool ok = x <= wb;
+                    if (ok && may_be_empty && x != w)
+                        ok = share_start(x, B, W) != share_start(x + 1, B, W);
+                    lv[j] = 0.f;
+                    mv[j] = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) ov[j][e] = 0.f;
+                    if (ok) {
+                        // later shares start inside the segment: their piece is in slot 0
+                        const int slot = x == w ? first_slot : 0;
+                        Slot sl(p.slots + (2 * x + slot) * (int64_t)p.slot_bytes, RT);
+                        lv[j] = __ldg(sl.l + row);
+                        mv[j] = __ldg(sl.m + row);
+                        const float* src = sl.o + (int64_t)row * D + lane * EPL;
+                        if constexpr (EPL == 4) {
+                            const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+                            ov[j][0] = t.x; ov[j][1] = t.y; ov[j][2] = t.z; ov[j][3] = t.w;
+                        } else {
+                            const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+                            ov[j][0] = t.x; ov[j][1] = t.y;
+                        }
+                    }
+                }
+                float Mb = M;
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j)
+                    if (lv[j] > 0.f) Mb = fmaxf(Mb, mv[j]);
+                if (Mb == -INFINITY) continue;             // no piece of this batch saw a key
+                const float a = exp2f(M - Mb);
+                den *= a;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] *= a;
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const float wgt = lv[j] > 0.f ? exp2f(mv[j] - Mb) : 0.f;
+                    den += wgt * lv[j];
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) acc[e] += wgt * ov[j][e];
+                }
+                M = Mb;
+            }
+        }
+        if (wpr > 1) {
+            // the row's warps meet in shared memory; the first of them folds
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) part[warp][lane * EPL + e] = acc[e];
+            if (lane == 0) {
+                part[warp][D] = M;
+                part[warp][D + 1] = den;
+            }
+            __syncthreads();
+            if (active && sub == 0) {
+                float Mt = -INFINITY;
+                for (int j = 0; j < wpr; ++j)
+                    if (part[warp + j][D + 1] > 0.f) Mt = fmaxf(Mt, part[warp + j][D]);
+                float dt = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+                for (int j = 0; j < wpr; ++j) {
+                    const float wgt =
+                        part[warp + j][D + 1] > 0.f ? exp2f(part[warp + j][D] - Mt) : 0.f;
+                    dt += wgt * part[warp + j][D + 1];
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) acc[e] += wgt * part[warp + j][lane * EPL + e];
+                }
+                M = Mt;
+                den = dt;
+            }
+            __syncthreads();                         // part is reused by the next round
+        }
+        if (!active || sub != 0) continue;
+        const int grow = c * RT + row;
+        const int64_t orow = (int64_t)(q0 + grow / G) * p.num_heads + g * G + grow % G;
+        const int64_t base = orow * D + lane * EPL;
+        const float inv = 1.f / den;
+        if (p.lse_out && lane == 0) p.lse_out[orow] = M + log2f(den);
+        if constexpr (EPL == 4) {
+            if (p.out_f32) {
+                *reinterpret_cast<float4*>(static_cast<float*>(p.out) + base) =
+                    make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+                continue;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) store_out<T>(p.out, base + e, acc[e] * inv, p.out_f32);
+    }
+}
+
+// Merges the pieces of every cut segment, one warp per (sequence, kv head,
 // chunk, query row) -- a flat grid of 4-warp CTAs over num_seqs x num_kv_heads
 // x max_chunks x row_slots items (row_slots = the most rows a chunk can have)
 // -- so the items that exist run in about one wave. A lane owns D / 32
 // columns. Pieces are read eight at a time (independent loads), then folded
 // into an online log-sum-exp: out = sum 2^(m - M) O / sum 2^(m - M) l.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p, int max_chunks,
+__global__ void __launch_bounds__(128) segment_reduce_rows_kernel(const Params p, int max_chunks,
                                                              int row_slots) {
     constexpr int EPL = D / 32;
     constexpr int kBatch = 8;
@@ -369,9 +549,20 @@ __global__ void __launch_bounds__(128) segment_reduce_kernel(const Params p, int
     for (int e = 0; e < EPL; ++e) store_out<T>(p.out, base + e, acc[e] * inv, p.out_f32);
 }
 
-// Grid of segment_reduce_kernel for a call: (items + 3) / 4 CTAs of 128 threads.
-inline int64_t reduce_ctas(int num_seqs, int num_kv_heads, int64_t max_chunks, int row_slots) {
-    return ((int64_t)num_seqs * num_kv_heads * max_chunks * row_slots + 3) / 4;
+// Launch the reduce for a balanced decode call (PDL, after the decode kernel).
+// One warp per (sequence, kv head, chunk, row) item while there are at most
+// 64K items (every item merges its own row, in parallel); past that (prefill:
+// thousands of rows per sequence, nearly all of them in segments held whole)
+// one CTA per worker, so only the owners of cut segments do any work.
+template <typename T, int D>
+cudaError_t launch_segment_reduce(const Params& prm, int max_chunks, int row_slots,
+                                  cudaStream_t stream) {
+    const int64_t items = (int64_t)prm.num_seqs * prm.num_kv_heads * max_chunks * row_slots;
+    if (items <= (1 << 16))
+        return pa::launch_pdl(segment_reduce_rows_kernel<T, D>, dim3((unsigned)((items + 3) / 4)),
+                              dim3(128), 0, stream, prm, max_chunks, row_slots);
+    return pa::launch_pdl(segment_reduce_kernel<T, D>, dim3((unsigned)prm.workers),
+                          dim3(32 * kReduceWarps), 0, stream, prm);
 }
 
 }  // namespace sched

@@ -357,6 +357,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     const int64_t f0 = share_start(wid, B, p.workers);
     const int64_t f1 = share_start(wid + 1, B, p.workers);
     const int n = (int)(f1 - f0);
+    if (lane == 0) write_merge_record(p, wid, 0, 0, 0);   // none unless set at the end
     if (n <= 0) return;
 
     if (lane == 0) {
@@ -508,7 +509,12 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         if (seg_done || k == n - 1) {
             finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
                            min((sb + cur.b) * kBS, L));
-            if (k == n - 1) break;
+            if (k == n - 1) {
+                if (lane == 0)
+                    record_last_segment(p, wid, f1, B, seg_done, seg_b0,
+                                        cur.nbs - cur.b, seg_first, q0, rows);
+                break;
+            }
             next_segment(p, cur, cum, chunks);
             seg_b0 = 0;
             seg_first = false;
@@ -575,6 +581,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
     const int64_t f0 = share_start(wid, B, p.workers);
     const int64_t f1 = share_start(wid + 1, B, p.workers);
     const int n = (int)(f1 - f0);
+    if (threadIdx.x == 0) write_merge_record(p, wid, 0, 0, 0);   // none unless set at the end
     if (n <= 0) return;                                      // uniform over the CTA
 
     if (threadIdx.x == 0) {
@@ -736,7 +743,12 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
         if (seg_done || k == n - 1) {
             finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
                            min((sb + cur.b) * kBS, L));
-            if (k == n - 1) break;
+            if (k == n - 1) {
+                if (threadIdx.x == 0)
+                    record_last_segment(p, wid, f1, B, seg_done, seg_b0,
+                                        cur.nbs - cur.b, seg_first, q0, rows);
+                break;
+            }
             next_segment(p, cur, cum, chunks);
             seg_b0 = 0;
             seg_first = false;
@@ -1146,16 +1158,10 @@ pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const 
             pa::launch_pdl(kern, dim3(grid), dim3(kWorkerWarps * 32), smem, a.stream, mk, mv, prm),
             "decode launch"))
         return s;
-    // query rows a chunk can have: all its G * max_q_len rows, up to one tile
-    const int row_slots = (int)std::min<int64_t>(shape.rows_per_tile,
-                                                 (int64_t)(a.num_heads / a.num_kv_heads) *
-                                                     a.max_q_len);
-    const int64_t rctas = pa::sched::reduce_ctas(a.num_seqs, a.num_kv_heads, shape.max_chunks,
-                                                 row_slots);
-    if (rctas > 0x7fffffff) return pa::fail(PA_ERR_UNSUPPORTED, "reduce grid too large");
-    return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<T, D>,
-                                          dim3((unsigned)rctas), dim3(128), 0, a.stream, prm,
-                                          (int)shape.max_chunks, row_slots),
+    const int row_slots = (int)std::min<int64_t>(shape.rows_per_tile, (int64_t)(a.num_heads / a.num_kv_heads) *
+                                                          a.max_q_len);
+    return pa::cuda_status(pa::sched::launch_segment_reduce<T, D>(prm, (int)shape.max_chunks,
+                                                                    row_slots, a.stream),
                            "segment reduce launch");
 }
 
@@ -1188,15 +1194,10 @@ pa_status launch_rows(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUte
                            mk, mv, prm),
             "decode launch"))
         return s;
-    const int row_slots = (int)std::min<int64_t>(kRowsTile,
-                                                 (int64_t)(a.num_heads / a.num_kv_heads) *
-                                                     a.max_q_len);
-    const int64_t rctas = pa::sched::reduce_ctas(a.num_seqs, a.num_kv_heads, shape.max_chunks,
-                                                 row_slots);
-    if (rctas > 0x7fffffff) return pa::fail(PA_ERR_UNSUPPORTED, "reduce grid too large");
-    return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<T, D>,
-                                          dim3((unsigned)rctas), dim3(128), 0, a.stream, prm,
-                                          (int)shape.max_chunks, row_slots),
+    const int row_slots = (int)std::min<int64_t>(kRowsTile, (int64_t)(a.num_heads / a.num_kv_heads) *
+                                                          a.max_q_len);
+    return pa::cuda_status(pa::sched::launch_segment_reduce<T, D>(prm, (int)shape.max_chunks,
+                                                                    row_slots, a.stream),
                            "segment reduce launch");
 }
 

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     const int64_t f0 = share_start(wid, B, p.workers);
     const int64_t f1 = share_start(wid + 1, B, p.workers);
     const int n = (int)(f1 - f0);
+    if (lane == 0) write_merge_record(p, wid, 0, 0, 0);   // none unless set at the end
     if (n <= 0) return;
 
     uint64_t pol_once = 0, pol_again = 0;
@@ -421,7 +422,12 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         if (seg_done || k == n - 1) {
             finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
                            min((sb + cur.b) * kBS, L));
-            if (k == n - 1) break;
+            if (k == n - 1) {
+                if (lane == 0)
+                    record_last_segment(p, wid, f1, B, seg_done, seg_b0,
+                                        cur.nbs - cur.b, seg_first, q0, rows);
+                break;
+            }
             next_segment(p, cur, cum, chunks);
             seg_b0 = 0;
             seg_first = false;
@@ -472,12 +478,8 @@ pa_status launch_fp8(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUten
         return s;
     const int row_slots = (int)std::min<int64_t>(kBS, (int64_t)(a.num_heads / a.num_kv_heads) *
                                                           a.max_q_len);
-    const int64_t rctas = pa::sched::reduce_ctas(a.num_seqs, a.num_kv_heads, shape.max_chunks,
-                                                 row_slots);
-    if (rctas > 0x7fffffff) return pa::fail(PA_ERR_UNSUPPORTED, "reduce grid too large");
-    return pa::cuda_status(pa::launch_pdl(pa::sched::segment_reduce_kernel<TQ, D>,
-                                          dim3((unsigned)rctas), dim3(128), 0, a.stream, prm,
-                                          (int)shape.max_chunks, row_slots),
+    return pa::cuda_status(pa::sched::launch_segment_reduce<TQ, D>(prm, (int)shape.max_chunks,
+                                                                    row_slots, a.stream),
                            "segment reduce launch");
 }
 
