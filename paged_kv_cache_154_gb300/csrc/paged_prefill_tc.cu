@@ -10,18 +10,20 @@
 // table by TMA):
 //
 //   S = Q K^T          tcgen05.mma M128 N64, A = Q, B = K (both K-major in
-//                      shared memory, 128-byte swizzle), S in TMEM;
+//                      shared memory, 128-byte swizzle), S in TMEM (two
+//                      buffers, so the product of tile t + 1 runs while the
+//                      softmax works on tile t);
 //   P = softmax(S)     four warps, one thread per row: S read from TMEM, fp32
 //                      online softmax with a running max moved only when a
 //                      tile raises it by more than 2^8 (O is then rescaled in
 //                      TMEM), P written as two 16-bit parts P_hi + P_lo so the
-//                      weights keep ~16 mantissa bits;
+//                      weights keep ~16 mantissa bits (two P buffers);
 //   O += P V           tcgen05.mma M128 N128, A = P (K-major), B = V
 //                      (MN-major: V's rows are tokens, the contraction index),
 //                      O in TMEM for the whole key range;
 //   out = O / l        read from TMEM at the end.
 //
-// Roles: warp 0 streams K/V blocks into a 2-stage ring (TMA), lane 0 of warp 1
+// Roles: warp 0 streams K/V blocks into a 4-stage ring (TMA), lane 0 of warp 1
 // issues the MMAs and commits them to mbarriers, warps 2-5 do the softmax and
 // the epilogue. Every wait is bounded; a wait that gives up stops the tile
 // loop of every role, and the MMA thread waits for its own operations to
@@ -52,21 +54,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyMax = 8.f;
 
 // shared memory (offsets from a 1024-byte aligned base)
+constexpr int kStages = 4;                      // K/V ring
 constexpr int kQOff = 0;                        // [2 sub][128 rows][128 B]
-constexpr int kKVOff = 32 * 1024;               // 2 stages x (K 16 KB, V 16 KB)
+constexpr int kKVOff = 32 * 1024;               // kStages x (K 16 KB, V 16 KB)
 constexpr int kKVStage = 32 * 1024;
 constexpr int kKBytes = 16 * 1024;              // [2 sub][64 rows][128 B]
 constexpr int kSubKV = 8 * 1024;                // one 64-dim half of a K (or V) tile
-constexpr int kPOff = kKVOff + 2 * kKVStage;    // P_hi [128 rows][128 B], then P_lo
+constexpr int kPOff = kKVOff + kStages * kKVStage;   // 2 buffers x (P_hi, P_lo) [128 rows][128 B]
 constexpr int kPBytes = 16 * 1024;
-constexpr int kBarOff = kPOff + 2 * kPBytes;    // mbarriers and flags
-constexpr int kSmem = kBarOff + 128 + 1024;     // + alignment slack
-// barrier slots
-constexpr int kBarKVFull = 0, kBarKVEmpty = 2, kBarSFull = 4, kBarPFull = 5, kBarODone = 6,
-              kBarFin = 7;
-// TMEM columns
+constexpr int kPBuf = 2 * kPBytes;
+constexpr int kBarOff = kPOff + 2 * kPBuf;      // mbarriers and flags
+constexpr int kSmem = kBarOff + 256 + 1024;     // + alignment slack
+// barrier slots: K/V full and empty per stage; S full, P full, O done per buffer
+constexpr int kBarKVFull = 0, kBarKVEmpty = kStages, kBarSFull = 2 * kStages,
+              kBarPFull = 2 * kStages + 2, kBarODone = 2 * kStages + 4, kBarFin = 2 * kStages + 6;
+constexpr int kNumBars = 2 * kStages + 7;
+// TMEM columns: S in two buffers of 64, O in 128
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSCol = 0, kOCol = 128;
+constexpr uint32_t kOCol = 128;
 
 struct PrefillParams {
     void* out;
@@ -140,8 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* const smem = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bars = base + kBarOff;
-    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(smem + kBarOff + 64);
-    volatile int* const abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 72);
+    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * kNumBars);
+    volatile int* const abort_flag =
+        reinterpret_cast<volatile int*>(smem + kBarOff + 8 * kNumBars + 8);
 
     pa::grid_dependents_launch();
     pa::grid_dependency_wait();
@@ -170,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         // P-ready takes one arrival from each of the four softmax warps
-        for (int i = 0; i < 8; ++i) pa::mbar_init(bars + 8 * i, i == kBarPFull ? 4 : 1);
+        for (int i = 0; i < kNumBars; ++i)
+            pa::mbar_init(bars + 8 * i, (i == kBarPFull || i == kBarPFull + 1) ? 4 : 1);
         *abort_flag = 0;
         pa::fence_barrier_init();
         pa::prefetch_tensormap(&tmap_k);
@@ -205,11 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- producer: K/V blocks of each tile ----------------
         int issued = 0;
         for (int t = 0; t < tiles; ++t) {
-            const int st = t & 1;
-            if (t >= 2) {
+            const int st = t % kStages;
+            if (t >= kStages) {   // the stage is free once the P V product of tile t - kStages is done
                 const bool ok = __all_sync(
-                    0xffffffffu, pa::mbar_wait(bars + 8 * (kBarKVEmpty + st), ((t >> 1) - 1) & 1,
-                                               p.err, pa::ERR_WAIT_EMPTY));
+                    0xffffffffu,
+                    pa::mbar_wait(bars + 8 * (kBarKVEmpty + st), ((t / kStages) - 1) & 1, p.err,
+                                  pa::ERR_WAIT_EMPTY));
                 if (!ok || *abort_flag) {
                     if (lane == 0) *abort_flag = 1;
                     break;
@@ -225,15 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 row = (blk * p.num_kv_heads + g) * kBS;
             }
-            if (lane == 0) {
-                const uint32_t bar = bars + 8 * (kBarKVFull + st);
-                pa::mbar_arrive_expect_tx(bar, nblk * 4 * (kBS * 128));
-            }
+            const uint32_t bar = bars + 8 * (kBarKVFull + st);
+            if (lane == 0) pa::mbar_arrive_expect_tx(bar, nblk * 4 * (kBS * 128));
+            const uint32_t kst = base + kKVOff + st * kKVStage;
             for (int j = 0; j < nblk; ++j) {
                 const int rj = __shfl_sync(0xffffffffu, row, j);
                 if (lane == 0) {
-                    const uint32_t bar = bars + 8 * (kBarKVFull + st);
-                    const uint32_t kst = base + kKVOff + st * kKVStage;
 #pragma unroll
                     for (int sub = 0; sub < 2; ++sub) {
                         pa::tma_load_2d(kst + sub * kSubKV + j * (kBS * 128), &tmap_k, sub * 64, rj,
@@ -245,29 +250,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             issued = t + 1;
         }
-        // drain: no copy may be in flight when the CTA ends; every issued stage
-        // is waited once more (it completes whether or not it was consumed)
+        // drain: no copy may be in flight when the CTA ends; the last kStages
+        // issued tiles are waited once more (each completes whether or not it
+        // was consumed; earlier ones were consumed before their stage was reused)
         if (lane == 0)
-            for (int t = issued >= 2 ? issued - 2 : 0; t < issued; ++t)
-                if (!pa::mbar_wait(bars + 8 * (kBarKVFull + (t & 1)), (t >> 1) & 1, nullptr, 0)) {
+            for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
+                if (!pa::mbar_wait(bars + 8 * (kBarKVFull + t % kStages), (t / kStages) & 1,
+                                   nullptr, 0)) {
                     if (p.err) atomicOr(p.err, pa::ERR_WAIT_DRAIN);
                     break;
                 }
     } else if (warp == 1) {
         // ---------------- MMA issue (one thread) ----------------
+        // order on the tensor pipe: QK(0), then per tile t: QK(t + 1), PV(t)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = pa::tc::idesc_f16(C::kBF16, false, false, kRows, kTok);
             constexpr uint32_t idesc_pv = pa::tc::idesc_f16(C::kBF16, false, true, kRows, D);
-            for (int t = 0; t < tiles; ++t) {
-                const int st = t & 1;
-                bool ok = pa::mbar_wait(bars + 8 * (kBarKVFull + st), (t >> 1) & 1, p.err,
+            auto issue_qk = [&](int t) -> bool {   // S[t & 1] = Q K(t)^T
+                const int st = t % kStages;
+                bool ok = pa::mbar_wait(bars + 8 * (kBarKVFull + st), (t / kStages) & 1, p.err,
                                         pa::ERR_WAIT_FULL);
-                if (ok && t >= 1)   // S is free once the softmax of tile t - 1 is done
-                    ok = pa::mbar_wait(bars + 8 * kBarPFull, (t - 1) & 1, p.err, pa::ERR_WAIT_FULL);
-                if (!ok || *abort_flag) {
-                    *abort_flag = 1;
-                    break;
-                }
+                if (ok && t >= 2)   // S[t & 1] is free once the softmax of tile t - 2 is done
+                    ok = pa::mbar_wait(bars + 8 * (kBarPFull + (t & 1)), ((t >> 1) - 1) & 1, p.err,
+                                       pa::ERR_WAIT_FULL);
+                if (!ok || *abort_flag) return false;
                 pa::tc::fence_after_sync();
                 const uint32_t kst = base + kKVOff + st * kKVStage;
 #pragma unroll
@@ -276,30 +282,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                         base + kQOff + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = pa::tc::smem_desc_sw128(
                         kst + (kk >> 2) * kSubKV + (kk & 3) * 32, 16, 1024);
-                    pa::tc::mma_f16_ss(tmem + kSCol, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+                    pa::tc::mma_f16_ss(tmem + 64 * (t & 1), a, b, idesc_qk, kk > 0 ? 1u : 0u);
                 }
-                pa::tc::commit(bars + 8 * kBarSFull);
-                ok = pa::mbar_wait(bars + 8 * kBarPFull, t & 1, p.err, pa::ERR_WAIT_FULL);
+                pa::tc::commit(bars + 8 * (kBarSFull + (t & 1)));
+                return true;
+            };
+            bool ok = issue_qk(0);
+            for (int t = 0; ok && t < tiles; ++t) {
+                if (t + 1 < tiles && !issue_qk(t + 1)) {
+                    ok = false;
+                    break;
+                }
+                ok = pa::mbar_wait(bars + 8 * (kBarPFull + (t & 1)), (t >> 1) & 1, p.err,
+                                   pa::ERR_WAIT_FULL);
                 if (!ok || *abort_flag) {
-                    *abort_flag = 1;
+                    ok = false;
                     break;
                 }
                 pa::tc::fence_after_sync();
+                const int st = t % kStages;
+                const uint32_t kst = base + kKVOff + st * kKVStage;
+                const uint32_t pbuf = base + kPOff + (t & 1) * kPBuf;
                 const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
                 for (int kb = 0; kb < nblk; ++kb) {
                     const uint64_t bv = pa::tc::smem_desc_sw128(
                         kst + kKBytes + kb * (kBS * 128), kSubKV, 1024);
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
-                        const uint64_t a = pa::tc::smem_desc_sw128(
-                            base + kPOff + part * kPBytes + kb * 32, 16, 1024);
+                        const uint64_t a =
+                            pa::tc::smem_desc_sw128(pbuf + part * kPBytes + kb * 32, 16, 1024);
                         pa::tc::mma_f16_ss(tmem + kOCol, a, bv, idesc_pv,
                                            (t > 0 || kb > 0 || part > 0) ? 1u : 0u);
                     }
                 }
-                pa::tc::commit(bars + 8 * kBarODone);
+                pa::tc::commit(bars + 8 * (kBarODone + (t & 1)));
                 pa::tc::commit(bars + 8 * (kBarKVEmpty + st));
             }
+            if (!ok) *abort_flag = 1;
             // every MMA this thread issued has finished before TMEM is freed
             pa::tc::commit(bars + 8 * kBarFin);
             if (!pa::mbar_wait(bars + 8 * kBarFin, 0, nullptr, 0) && p.err)
@@ -319,17 +338,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sm_tid = threadIdx.x - 64;                 // 0..127
         int done = 0;
         for (int t = 0; t < tiles; ++t) {
-            const int st = t & 1;
-            const bool ok = __all_sync(0xffffffffu, pa::mbar_wait(bars + 8 * kBarSFull, t & 1,
-                                                                  p.err, pa::ERR_WAIT_FULL));
+            const bool ok = __all_sync(
+                0xffffffffu, pa::mbar_wait(bars + 8 * (kBarSFull + (t & 1)), (t >> 1) & 1, p.err,
+                                           pa::ERR_WAIT_FULL));
             if (!ok || *abort_flag) {
                 if (lane == 0) *abort_flag = 1;
                 break;
             }
             pa::tc::fence_after_sync();
             float sv[kTok];
-            pa::tc::ld_32cols(trow + kSCol, *reinterpret_cast<float(*)[32]>(sv));
-            pa::tc::ld_32cols(trow + kSCol + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+            const uint32_t scol = 64 * (t & 1);
+            pa::tc::ld_32cols(trow + scol, *reinterpret_cast<float(*)[32]>(sv));
+            pa::tc::ld_32cols(trow + scol + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
             const int tok0 = t * kTok;
             float mx = -INFINITY;
 #pragma unroll
@@ -354,17 +374,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sum += sv[j];
             }
             l_run = l_run * alpha + sum;
-            // P and O may be touched once the P V product of tile t - 1 is done
-            if (t >= 1) {
+            // P buffer t & 1 is free once the P V product of tile t - 2 is done
+            if (t >= 2) {
                 const bool ok2 = __all_sync(
-                    0xffffffffu,
-                    pa::mbar_wait(bars + 8 * kBarODone, (t - 1) & 1, p.err, pa::ERR_WAIT_FULL));
+                    0xffffffffu, pa::mbar_wait(bars + 8 * (kBarODone + (t & 1)),
+                                               ((t >> 1) - 1) & 1, p.err, pa::ERR_WAIT_FULL));
                 if (!ok2 || *abort_flag) {
                     if (lane == 0) *abort_flag = 1;
                     break;
                 }
+            }
+            // O may be rescaled once the P V product of tile t - 1 is done
+            if (t >= 1 && __any_sync(0xffffffffu, moved)) {
+                const bool ok3 = __all_sync(
+                    0xffffffffu, pa::mbar_wait(bars + 8 * (kBarODone + ((t - 1) & 1)),
+                                               ((t - 1) >> 1) & 1, p.err, pa::ERR_WAIT_FULL));
+                if (!ok3 || *abort_flag) {
+                    if (lane == 0) *abort_flag = 1;
+                    break;
+                }
                 pa::tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, moved)) {
+                {
                     // rescale this warp's rows of O in TMEM (alpha = 1 for the others)
 #pragma unroll
                     for (int q = 0; q < D / 32; ++q) {
@@ -386,12 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     hi[u] = C::pack(sv[8 * ch + 2 * u], sv[8 * ch + 2 * u + 1], ra, rb);
                     lo[u] = C::pack(ra, rb);
                 }
-                const uint32_t off = sw128(row, ch);
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(base + kPOff + off),
-                             "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
+                const uint32_t off = base + kPOff + (t & 1) * kPBuf + sw128(row, ch);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(off), "r"(hi[0]),
+                             "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
                              : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                                 base + kPOff + kPBytes + off),
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(off + kPBytes),
                              "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
                              : "memory");
             }
@@ -403,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int z0 = L - tok0, zrows = tok_end - L;      // local token rows to zero
                 for (int e = sm_tid; e < zrows * 16; e += 128) {
                     const int lr = z0 + e / 16, ch = e % 16;
-                    const uint32_t dst = base + kKVOff + st * kKVStage + kKBytes +
+                    const uint32_t dst = base + kKVOff + (t % kStages) * kKVStage + kKBytes +
                                          (ch >> 3) * kSubKV + lr * 128 + ((ch & 7) << 4);
                     asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u)
                                  : "memory");
@@ -413,14 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             pa::tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) pa::mbar_arrive(bars + 8 * kBarPFull);
+            if (lane == 0) pa::mbar_arrive(bars + 8 * (kBarPFull + (t & 1)));
             done = t + 1;
         }
         // epilogue: O / l for this row
         if (done == tiles && tiles > 0) {
-            const bool ok = __all_sync(0xffffffffu,
-                                       pa::mbar_wait(bars + 8 * kBarODone, (tiles - 1) & 1, p.err,
-                                                     pa::ERR_WAIT_FULL));
+            const bool ok = __all_sync(
+                0xffffffffu, pa::mbar_wait(bars + 8 * (kBarODone + ((tiles - 1) & 1)),
+                                           ((tiles - 1) >> 1) & 1, p.err, pa::ERR_WAIT_FULL));
             if (ok) {
                 pa::tc::fence_after_sync();
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
