@@ -4,28 +4,30 @@
 // chunked prefill) turns attention over the paged cache into a dense
 // contraction: per KV head, G q heads x r query tokens against the
 // sequence's keys, causally masked ("cs336 lecture 10": query i of a run of
-// r at position L - r + i sees keys 0 .. L - r + i). This kernel computes it
-// per 128-row tile (the rows of one (sequence, kv head) in chunks of 128) over
-// key tiles of 64 tokens (four 16-token blocks, gathered through the block
-// table by TMA):
+// r at position L - r + i sees keys 0 .. L - r + i). A CTA takes 256 rows of
+// one (sequence, kv head) as two Q tiles of 128 and streams the key range in
+// tiles of 64 tokens (four 16-token blocks, gathered through the block table
+// by TMA); per Q tile x:
 //
-//   S = Q K^T          tcgen05.mma M128 N64, A = Q, B = K (both K-major in
-//                      shared memory, 128-byte swizzle), S in TMEM (two
-//                      buffers, so the product of tile t + 1 runs while the
-//                      softmax works on tile t);
-//   P = softmax(S)     four warps, one thread per row: S read from TMEM, fp32
-//                      online softmax with a running max moved only when a
-//                      tile raises it by more than 2^8 (O is then rescaled in
-//                      TMEM), P written as two 16-bit parts P_hi + P_lo so the
-//                      weights keep ~16 mantissa bits (two P buffers);
-//   O += P V           tcgen05.mma M128 N128, A = P (K-major), B = V
-//                      (MN-major: V's rows are tokens, the contraction index),
-//                      O in TMEM for the whole key range;
-//   out = O / l        read from TMEM at the end.
+//   S_x = Q_x K^T      tcgen05.mma M128 N64, A = Q_x, B = K (both K-major in
+//                      shared memory, 128-byte swizzle), S_x in TMEM;
+//   P_x = softmax(S_x) one warpgroup per Q tile, one thread per row: S read
+//                      from TMEM into registers (after which the next product
+//                      may overwrite it), fp32 online softmax with a running
+//                      max moved only when a tile raises it by more than 2^8
+//                      (O_x is then rescaled in TMEM), P written back to TMEM
+//                      as two 16-bit parts P_hi + P_lo so the weights keep
+//                      ~16 mantissa bits;
+//   O_x += P_x V       tcgen05.mma M128 N128 with A = P_x read from TMEM and
+//                      B = V (MN-major in shared memory: V's rows are tokens,
+//                      the contraction index), O_x in TMEM for the whole range;
+//   out = O_x / l      read from TMEM at the end.
 //
-// Roles: warp 0 streams K/V blocks into a 4-stage ring (TMA), lane 0 of warp 1
-// issues the MMAs and commits them to mbarriers, warps 2-5 do the softmax and
-// the epilogue. Every wait is bounded; a wait that gives up stops the tile
+// The two warpgroups alternate on the tensor pipe (QK_0, PV_0, QK_1, PV_1 per
+// key tile), so one group's softmax runs while the other's products do.
+// Roles: warp 0 streams K/V tiles into a 4-stage ring (TMA), lane 0 of warp 1
+// issues the MMAs and commits them to mbarriers, warps 2-5 and 6-9 are the
+// softmax groups. Every wait is bounded; a wait that gives up stops the tile
 // loop of every role, and the MMA thread waits for its own operations to
 // finish before TMEM is freed.
 #include <cuda.h>
@@ -46,32 +48,35 @@ namespace {
 
 constexpr int kBS = 16;
 constexpr int D = 128;
-constexpr int kRows = 128;              // query rows per tile (MMA M)
-constexpr int kTok = 64;                // keys per tile (S columns)
+constexpr int kRows = 128;              // query rows per Q tile (MMA M)
+constexpr int kQTiles = 2;              // Q tiles per CTA, one softmax warpgroup each
+constexpr int kTaskRows = kRows * kQTiles;
+constexpr int kTok = 64;                // keys per K/V tile (S columns)
 constexpr int kTileBlocks = kTok / kBS; // 4
-constexpr int kThreads = 192;           // 6 warps
+constexpr int kThreads = 64 + 128 * kQTiles;   // producer, MMA, 2 softmax warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyMax = 8.f;
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int kStages = 4;                      // K/V ring
-constexpr int kQOff = 0;                        // [2 sub][128 rows][128 B]
-constexpr int kKVOff = 32 * 1024;               // kStages x (K 16 KB, V 16 KB)
+constexpr int kQBytes = 32 * 1024;              // one Q tile: [2 sub][128 rows][128 B]
+constexpr int kQOff = 0;
+constexpr int kKVOff = kQTiles * kQBytes;       // kStages x (K 16 KB, V 16 KB)
 constexpr int kKVStage = 32 * 1024;
 constexpr int kKBytes = 16 * 1024;              // [2 sub][64 rows][128 B]
 constexpr int kSubKV = 8 * 1024;                // one 64-dim half of a K (or V) tile
-constexpr int kPOff = kKVOff + kStages * kKVStage;   // 2 buffers x (P_hi, P_lo) [128 rows][128 B]
-constexpr int kPBytes = 16 * 1024;
-constexpr int kPBuf = 2 * kPBytes;
-constexpr int kBarOff = kPOff + 2 * kPBuf;      // mbarriers and flags
+constexpr int kBarOff = kKVOff + kStages * kKVStage;   // mbarriers and flags
 constexpr int kSmem = kBarOff + 256 + 1024;     // + alignment slack
-// barrier slots: K/V full and empty per stage; S full, P full, O done per buffer
+// barrier slots: K/V full and empty per stage; per Q tile: S full, S free
+// (S read into registers), P full, O done; and the final drain
 constexpr int kBarKVFull = 0, kBarKVEmpty = kStages, kBarSFull = 2 * kStages,
-              kBarPFull = 2 * kStages + 2, kBarODone = 2 * kStages + 4, kBarFin = 2 * kStages + 6;
-constexpr int kNumBars = 2 * kStages + 7;
-// TMEM columns: S in two buffers of 64, O in 128
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kOCol = 128;
+              kBarSFree = 2 * kStages + 2, kBarPFull = 2 * kStages + 4,
+              kBarODone = 2 * kStages + 6, kBarFin = 2 * kStages + 8;
+constexpr int kNumBars = 2 * kStages + 9;
+// TMEM columns (512): O of Q tile x at 128x, S at 256 + 64x, P at 384 + 64x
+// (P_hi in the first 32 columns, P_lo in the next 32, two 16-bit values each)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 256, kPCol = 384;
 
 struct PrefillParams {
     void* out;
@@ -86,7 +91,7 @@ struct PrefillParams {
     int group;
     int num_seqs;
     int num_blocks;
-    int max_chunks;
+    int max_tasks;      // 256-row tasks per (sequence, kv head)
     float scale_log2;
     int out_f32;
 };
@@ -97,20 +102,48 @@ __device__ __forceinline__ uint32_t sw128(int row, int c) {
     return row * 128 + ((c ^ (row & 7)) << 4);
 }
 
+// packed two-lane fp32 arithmetic (one instruction for two values)
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 template <typename T>
 struct Cvt;
 template <>
 struct Cvt<__nv_bfloat16> {
     static constexpr bool kBF16 = true;
-    __device__ static uint32_t pack(float a, float b, float& ra, float& rb) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-        ra = a - __low2float(v);
-        rb = b - __high2float(v);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
-    __device__ static uint32_t pack(float a, float b) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&v);
+    // a, b -> hi = bf16(a, b), lo = bf16 of the remainders (a - hi_a, b - hi_b)
+    __device__ static void split(float a, float b, uint32_t& hi, uint32_t& lo) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        hi = *reinterpret_cast<uint32_t*>(&h);
+        float ra, rb;
+        sub2(ra, rb, a, b, __uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+        __nv_bfloat162 l = __floats2bfloat162_rn(ra, rb);
+        lo = *reinterpret_cast<uint32_t*>(&l);
     }
     __device__ static void store2(void* p, float a, float b) {
         *static_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
@@ -119,15 +152,13 @@ struct Cvt<__nv_bfloat16> {
 template <>
 struct Cvt<__half> {
     static constexpr bool kBF16 = false;
-    __device__ static uint32_t pack(float a, float b, float& ra, float& rb) {
-        __half2 v = __floats2half2_rn(a, b);
-        ra = a - __low2float(v);
-        rb = b - __high2float(v);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
-    __device__ static uint32_t pack(float a, float b) {
-        __half2 v = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&v);
+    __device__ static void split(float a, float b, uint32_t& hi, uint32_t& lo) {
+        __half2 h = __floats2half2_rn(a, b);
+        hi = *reinterpret_cast<uint32_t*>(&h);
+        float ra, rb;
+        sub2(ra, rb, a, b, __low2float(h), __high2float(h));
+        __half2 l = __floats2half2_rn(ra, rb);
+        lo = *reinterpret_cast<uint32_t*>(&l);
     }
     __device__ static void store2(void* p, float a, float b) {
         *static_cast<__half2*>(p) = __floats2half2_rn(a, b);
@@ -152,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     pa::grid_dependents_launch();
     pa::grid_dependency_wait();
 
-    // task: (chunk, sequence, kv head), later chunks (longer key ranges) first
+    // task: (256-row chunk, sequence, kv head), later chunks (longer key ranges) first
     const int sh = p.num_seqs * p.num_kv_heads;
-    const int c = p.max_chunks - 1 - (int)(blockIdx.x / sh);
+    const int c = p.max_tasks - 1 - (int)(blockIdx.x / sh);
     const int s = (int)(blockIdx.x % sh) / p.num_kv_heads;
     const int g = (int)(blockIdx.x % sh) % p.num_kv_heads;
     const int L = __ldg(p.context_lens + s);
@@ -167,17 +198,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         r = 1;
     }
     const int G = p.group;
-    const int row_off = c * kRows;
-    const int rows = min(kRows, G * r - row_off);
-    if (rows <= 0) return;                                       // uniform over the CTA
-    const int jmax = min(r - 1, (row_off + rows - 1) / G);
+    const int task_off = c * kTaskRows;
+    const int task_rows = min(kTaskRows, G * r - task_off);
+    if (task_rows <= 0) return;                                  // uniform over the CTA
+    const int nq = task_rows > kRows ? 2 : 1;                    // Q tiles with rows
+    const int jmax = min(r - 1, (task_off + task_rows - 1) / G);
     const int end_blocks = min((L + kBS - 1) / kBS, (L - r + jmax) / kBS + 1);
     const int tiles = (end_blocks + kTileBlocks - 1) / kTileBlocks;
 
     if (threadIdx.x == 0) {
-        // P-ready takes one arrival from each of the four softmax warps
+        // S free and P full take one arrival from each of the four warps of a softmax group
         for (int i = 0; i < kNumBars; ++i)
-            pa::mbar_init(bars + 8 * i, (i == kBarPFull || i == kBarPFull + 1) ? 4 : 1);
+            pa::mbar_init(bars + 8 * i, (i >= kBarSFree && i < kBarODone) ? 4 : 1);
         *abort_flag = 0;
         pa::fence_barrier_init();
         pa::prefetch_tensormap(&tmap_k);
@@ -187,17 +219,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         pa::tc::tmem_alloc(pa::smem_addr(tmem_holder), kTmemCols);
         pa::tc::tmem_relinquish();
     }
-    // Q tile: 128 rows x 128 dims, 128-byte swizzled K-major (two 64-dim halves)
-    for (int e = threadIdx.x; e < kRows * 16; e += kThreads) {
-        const int row = e >> 4, ch = e & 15;
+    // Q tiles: 128 rows x 128 dims each, 128-byte swizzled K-major (two 64-dim halves)
+    for (int e = threadIdx.x; e < nq * kRows * 16; e += kThreads) {
+        const int trow = e >> 4, ch = e & 15;          // task row 0..255
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < rows) {
-            const int gr = row_off + row;
+        if (trow < task_rows) {
+            const int gr = task_off + trow;
             const T* src = static_cast<const T*>(p.q) +
                            ((int64_t)(q0 + gr / G) * p.num_heads + g * G + gr % G) * D;
             v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
         }
-        const uint32_t dst = base + kQOff + (ch >> 3) * (kRows * 128) + sw128(row, ch & 7);
+        const int x = trow / kRows, row = trow % kRows;
+        const uint32_t dst =
+            base + kQOff + x * kQBytes + (ch >> 3) * (kRows * 128) + sw128(row, ch & 7);
         asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y),
                      "r"(v.z), "r"(v.w)
                      : "memory");
@@ -213,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued = 0;
         for (int t = 0; t < tiles; ++t) {
             const int st = t % kStages;
-            if (t >= kStages) {   // the stage is free once the P V product of tile t - kStages is done
+            if (t >= kStages) {   // the stage is free once every product reading tile t - kStages is done
                 const bool ok = __all_sync(
                     0xffffffffu,
                     pa::mbar_wait(bars + 8 * (kBarKVEmpty + st), ((t / kStages) - 1) & 1, p.err,
@@ -262,61 +296,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
     } else if (warp == 1) {
         // ---------------- MMA issue (one thread) ----------------
-        // order on the tensor pipe: QK(0), then per tile t: QK(t + 1), PV(t)
+        // per key tile t: QK_0(t + 1), PV_0(t), QK_1(t + 1), PV_1(t); a Q tile's
+        // next product of S starts as soon as its softmax has read S into registers
         if (lane == 0) {
             constexpr uint32_t idesc_qk = pa::tc::idesc_f16(C::kBF16, false, false, kRows, kTok);
             constexpr uint32_t idesc_pv = pa::tc::idesc_f16(C::kBF16, false, true, kRows, D);
-            auto issue_qk = [&](int t) -> bool {   // S[t & 1] = Q K(t)^T
-                const int st = t % kStages;
-                bool ok = pa::mbar_wait(bars + 8 * (kBarKVFull + st), (t / kStages) & 1, p.err,
-                                        pa::ERR_WAIT_FULL);
-                if (ok && t >= 2)   // S[t & 1] is free once the softmax of tile t - 2 is done
-                    ok = pa::mbar_wait(bars + 8 * (kBarPFull + (t & 1)), ((t >> 1) - 1) & 1, p.err,
+            auto issue_qk = [&](int x, int t) -> bool {   // S_x = Q_x K(t)^T
+                bool ok = true;
+                if (t >= 1)   // S_x is free once its softmax has read tile t - 1
+                    ok = pa::mbar_wait(bars + 8 * (kBarSFree + x), (t - 1) & 1, p.err,
                                        pa::ERR_WAIT_FULL);
                 if (!ok || *abort_flag) return false;
                 pa::tc::fence_after_sync();
-                const uint32_t kst = base + kKVOff + st * kKVStage;
+                const uint32_t kst = base + kKVOff + (t % kStages) * kKVStage;
+                const uint32_t qb = base + kQOff + x * kQBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = pa::tc::smem_desc_sw128(
-                        base + kQOff + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t a =
+                        pa::tc::smem_desc_sw128(qb + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = pa::tc::smem_desc_sw128(
                         kst + (kk >> 2) * kSubKV + (kk & 3) * 32, 16, 1024);
-                    pa::tc::mma_f16_ss(tmem + 64 * (t & 1), a, b, idesc_qk, kk > 0 ? 1u : 0u);
+                    pa::tc::mma_f16_ss(tmem + kSCol + 64 * x, a, b, idesc_qk, kk > 0 ? 1u : 0u);
                 }
-                pa::tc::commit(bars + 8 * (kBarSFull + (t & 1)));
+                pa::tc::commit(bars + 8 * (kBarSFull + x));
                 return true;
             };
-            bool ok = issue_qk(0);
-            for (int t = 0; ok && t < tiles; ++t) {
-                if (t + 1 < tiles && !issue_qk(t + 1)) {
-                    ok = false;
-                    break;
-                }
-                ok = pa::mbar_wait(bars + 8 * (kBarPFull + (t & 1)), (t >> 1) & 1, p.err,
-                                   pa::ERR_WAIT_FULL);
-                if (!ok || *abort_flag) {
-                    ok = false;
-                    break;
-                }
+            auto issue_pv = [&](int x, int t) -> bool {   // O_x += P_x V(t)
+                const bool ok = pa::mbar_wait(bars + 8 * (kBarPFull + x), t & 1, p.err,
+                                              pa::ERR_WAIT_FULL);
+                if (!ok || *abort_flag) return false;
                 pa::tc::fence_after_sync();
-                const int st = t % kStages;
-                const uint32_t kst = base + kKVOff + st * kKVStage;
-                const uint32_t pbuf = base + kPOff + (t & 1) * kPBuf;
+                const uint32_t kst = base + kKVOff + (t % kStages) * kKVStage;
                 const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
                 for (int kb = 0; kb < nblk; ++kb) {
                     const uint64_t bv = pa::tc::smem_desc_sw128(
                         kst + kKBytes + kb * (kBS * 128), kSubKV, 1024);
 #pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        const uint64_t a =
-                            pa::tc::smem_desc_sw128(pbuf + part * kPBytes + kb * 32, 16, 1024);
-                        pa::tc::mma_f16_ss(tmem + kOCol, a, bv, idesc_pv,
-                                           (t > 0 || kb > 0 || part > 0) ? 1u : 0u);
-                    }
+                    for (int part = 0; part < 2; ++part)
+                        pa::tc::mma_f16_ts(tmem + 128 * x, tmem + kPCol + 64 * x + 32 * part + 8 * kb,
+                                           bv, idesc_pv, (t > 0 || kb > 0 || part > 0) ? 1u : 0u);
                 }
-                pa::tc::commit(bars + 8 * (kBarODone + (t & 1)));
-                pa::tc::commit(bars + 8 * (kBarKVEmpty + st));
+                pa::tc::commit(bars + 8 * (kBarODone + x));
+                return true;
+            };
+            auto kv_ready = [&](int t) {
+                return pa::mbar_wait(bars + 8 * (kBarKVFull + t % kStages), (t / kStages) & 1,
+                                     p.err, pa::ERR_WAIT_FULL);
+            };
+            bool ok = tiles > 0 && kv_ready(0) && issue_qk(0, 0) && (nq < 2 || issue_qk(1, 0));
+            for (int t = 0; ok && t < tiles; ++t) {
+                const bool more = t + 1 < tiles;
+                if (more && !(kv_ready(t + 1) && issue_qk(0, t + 1))) ok = false;
+                if (ok && !issue_pv(0, t)) ok = false;
+                if (ok && nq > 1) {
+                    if (more && !issue_qk(1, t + 1)) ok = false;
+                    if (ok && !issue_pv(1, t)) ok = false;
+                }
+                if (ok) pa::tc::commit(bars + 8 * (kBarKVEmpty + t % kStages));
             }
             if (!ok) *abort_flag = 1;
             // every MMA this thread issued has finished before TMEM is freed
@@ -325,40 +361,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(p.err, pa::ERR_WAIT_DRAIN);
         }
         __syncwarp();
-    } else {
-        // ---------------- softmax and epilogue: one thread per row ----------------
+    } else if ((warp - 2) / 4 < nq) {
+        // ---------------- softmax and epilogue: one thread per row of Q tile x ----------------
+        const int x = (warp - 2) / 4;
         const int lane_base = 32 * (warp & 3);
         const int row = lane_base + lane;                    // tile row = TMEM lane
+        const int row_off = task_off + x * kRows;
+        const int rows = min(kRows, task_rows - x * kRows);
         const int gr = row_off + row;
         const bool valid = row < rows;
         const int jq = valid ? gr / G : 0;
-        const int bound = valid ? min(L - r + jq, L - 1) : -1;
+        // keys past a row's bound are masked; padding rows (Q = 0) need no mask
+        const int bound = valid ? min(L - r + jq, L - 1) : 0x7fffffff;
+        // the smallest bound of the tile's rows: tiles ending at or before it need no mask
+        const int bound_min = min(L - r + row_off / G, L - 1);
         const uint32_t trow = tmem + ((uint32_t)lane_base << 16);
+        const uint32_t s_tm = trow + kSCol + 64 * x, p_tm = trow + kPCol + 64 * x,
+                       o_tm = trow + 128 * x;
+        const uint32_t bar_sfull = bars + 8 * (kBarSFull + x), bar_sfree = bars + 8 * (kBarSFree + x),
+                       bar_pfull = bars + 8 * (kBarPFull + x), bar_odone = bars + 8 * (kBarODone + x);
+        const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
-        const int sm_tid = threadIdx.x - 64;                 // 0..127
+        const int grp_tid = (warp - 2 - 4 * x) * 32 + lane;  // 0..127 within the group
         int done = 0;
         for (int t = 0; t < tiles; ++t) {
-            const bool ok = __all_sync(
-                0xffffffffu, pa::mbar_wait(bars + 8 * (kBarSFull + (t & 1)), (t >> 1) & 1, p.err,
-                                           pa::ERR_WAIT_FULL));
+            bool ok = __all_sync(0xffffffffu,
+                                 pa::mbar_wait(bar_sfull, t & 1, p.err, pa::ERR_WAIT_FULL));
             if (!ok || *abort_flag) {
                 if (lane == 0) *abort_flag = 1;
                 break;
             }
             pa::tc::fence_after_sync();
             float sv[kTok];
-            const uint32_t scol = 64 * (t & 1);
-            pa::tc::ld_32cols(trow + scol, *reinterpret_cast<float(*)[32]>(sv));
-            pa::tc::ld_32cols(trow + scol + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+            pa::tc::ld_64cols(s_tm, *reinterpret_cast<uint32_t(*)[64]>(sv));
+            // S is in registers: the next product may overwrite it
+            pa::tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(bar_sfree);
             const int tok0 = t * kTok;
-            float mx = -INFINITY;
+            if (tok0 + kTok - 1 > bound_min) {               // a tile some row must not see all of
 #pragma unroll
-            for (int j = 0; j < kTok; ++j) {
-                float v = sv[j] * p.scale_log2;
-                if (tok0 + j > bound) v = -INFINITY;
-                sv[j] = v;
-                mx = fmaxf(mx, v);
+                for (int j = 0; j < kTok; ++j)
+                    if (tok0 + j > bound) sv[j] = -INFINITY;
             }
+            float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+            for (int j = 4; j < kTok; j += 8)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) m4[u] = max3(m4[u], sv[j + 2 * u], sv[j + 2 * u + 1]);
+            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            mx = mx == -INFINITY ? mx : mx * sl2;            // the scale is positive
             float alpha = 1.f;
             bool moved = false;
             if (mx > m_run + kLazyMax) {
@@ -366,90 +418,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run = mx;
                 moved = true;
             }
-            const float m_use = m_run == -INFINITY ? 0.f : m_run;
-            float sum = 0.f;
+            const float nm = m_run == -INFINITY ? 0.f : -m_run;
 #pragma unroll
-            for (int j = 0; j < kTok; ++j) {
-                sv[j] = pa::ex2(sv[j] - m_use);
-                sum += sv[j];
+            for (int j = 0; j < kTok; j += 2) {
+                fma2(sv[j], sv[j + 1], sv[j], sv[j + 1], sl2, sl2, nm, nm);
+                sv[j] = pa::ex2(sv[j]);
+                sv[j + 1] = pa::ex2(sv[j + 1]);
             }
-            l_run = l_run * alpha + sum;
-            // P buffer t & 1 is free once the P V product of tile t - 2 is done
-            if (t >= 2) {
-                const bool ok2 = __all_sync(
-                    0xffffffffu, pa::mbar_wait(bars + 8 * (kBarODone + (t & 1)),
-                                               ((t >> 1) - 1) & 1, p.err, pa::ERR_WAIT_FULL));
-                if (!ok2 || *abort_flag) {
-                    if (lane == 0) *abort_flag = 1;
-                    break;
-                }
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < kTok; j += 4) {
+                add2(s4[0], s4[1], s4[0], s4[1], sv[j], sv[j + 1]);
+                add2(s4[2], s4[3], s4[2], s4[3], sv[j + 2], sv[j + 3]);
             }
-            // O may be rescaled once the P V product of tile t - 1 is done
-            if (t >= 1 && __any_sync(0xffffffffu, moved)) {
-                const bool ok3 = __all_sync(
-                    0xffffffffu, pa::mbar_wait(bars + 8 * (kBarODone + ((t - 1) & 1)),
-                                               ((t - 1) >> 1) & 1, p.err, pa::ERR_WAIT_FULL));
-                if (!ok3 || *abort_flag) {
+            l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+            uint32_t pk[64];
+#pragma unroll
+            for (int j = 0; j < kTok / 2; ++j) C::split(sv[2 * j], sv[2 * j + 1], pk[j], pk[32 + j]);
+            // P_x and O_x are free once the P V product of tile t - 1 is done
+            if (t >= 1) {
+                ok = __all_sync(0xffffffffu,
+                                pa::mbar_wait(bar_odone, (t - 1) & 1, p.err, pa::ERR_WAIT_FULL));
+                if (!ok || *abort_flag) {
                     if (lane == 0) *abort_flag = 1;
                     break;
                 }
                 pa::tc::fence_after_sync();
-                {
+                if (__any_sync(0xffffffffu, moved)) {
                     // rescale this warp's rows of O in TMEM (alpha = 1 for the others)
 #pragma unroll
                     for (int q = 0; q < D / 32; ++q) {
                         float ov[32];
-                        pa::tc::ld_32cols(trow + kOCol + 32 * q, ov);
+                        pa::tc::ld_32cols(o_tm + 32 * q, ov);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                        pa::tc::st_32cols(trow + kOCol + 32 * q, ov);
+                        for (int i = 0; i < 32; i += 2) fma2(ov[i], ov[i + 1], ov[i], ov[i + 1], alpha, alpha, 0.f, 0.f);
+                        pa::tc::st_32cols(o_tm + 32 * q, ov);
                     }
                 }
             }
-            // P_hi and P_lo of this row: 64 keys = 8 chunks of 16 bytes each
-#pragma unroll
-            for (int ch = 0; ch < kTok / 8; ++ch) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float ra, rb;
-                    hi[u] = C::pack(sv[8 * ch + 2 * u], sv[8 * ch + 2 * u + 1], ra, rb);
-                    lo[u] = C::pack(ra, rb);
-                }
-                const uint32_t off = base + kPOff + (t & 1) * kPBuf + sw128(row, ch);
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(off), "r"(hi[0]),
-                             "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
-                             : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(off + kPBytes),
-                             "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
-                             : "memory");
-            }
+            pa::tc::st_64cols(p_tm, pk);
             // V rows past the context (in the sequence's last block) may hold
-            // anything: zero them so that P = 0 never meets a NaN
+            // anything: zero them so that P = 0 never meets a NaN (Q tile 0's
+            // group does it; both products of the tile run after its P is ready)
             const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
             const int tok_end = tok0 + nblk * kBS;
-            if (L < tok_end) {
+            if (x == 0 && L < tok_end) {
                 const int z0 = L - tok0, zrows = tok_end - L;      // local token rows to zero
-                for (int e = sm_tid; e < zrows * 16; e += 128) {
+                for (int e = grp_tid; e < zrows * 16; e += 128) {
                     const int lr = z0 + e / 16, ch = e % 16;
                     const uint32_t dst = base + kKVOff + (t % kStages) * kKVStage + kKBytes +
                                          (ch >> 3) * kSubKV + lr * 128 + ((ch & 7) << 4);
                     asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u)
                                  : "memory");
                 }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-            // each warp releases its part (no CTA-wide barrier a stalled warp could hold)
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // each warp releases its part (no group-wide barrier a stalled warp could hold)
             pa::tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) pa::mbar_arrive(bars + 8 * (kBarPFull + (t & 1)));
+            if (lane == 0) pa::mbar_arrive(bar_pfull);
             done = t + 1;
         }
         // epilogue: O / l for this row
         if (done == tiles && tiles > 0) {
             const bool ok = __all_sync(
-                0xffffffffu, pa::mbar_wait(bars + 8 * (kBarODone + ((tiles - 1) & 1)),
-                                           ((tiles - 1) >> 1) & 1, p.err, pa::ERR_WAIT_FULL));
+                0xffffffffu, pa::mbar_wait(bar_odone, (tiles - 1) & 1, p.err, pa::ERR_WAIT_FULL));
             if (ok) {
                 pa::tc::fence_after_sync();
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -458,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int qd = 0; qd < D / 32; ++qd) {
                     float ov[32];
-                    pa::tc::ld_32cols(trow + kOCol + 32 * qd, ov);
+                    pa::tc::ld_32cols(o_tm + 32 * qd, ov);
                     if (valid) {
                         if (p.out_f32) {
                             float* dst = static_cast<float*>(p.out) + orow * D + 32 * qd;
@@ -517,8 +550,8 @@ bool prefill_tc_applies(const DecodeArgs& a) {
 
 pa_status launch_prefill_tc(const DecodeArgs& a) {
     const int G = a.num_heads / a.num_kv_heads;
-    const int64_t max_chunks = ((int64_t)G * a.max_q_len + kRows - 1) / kRows;
-    const int64_t grid = max_chunks * a.num_seqs * a.num_kv_heads;
+    const int64_t max_tasks = ((int64_t)G * a.max_q_len + kTaskRows - 1) / kTaskRows;
+    const int64_t grid = max_tasks * a.num_seqs * a.num_kv_heads;
     if (grid > 0x7fffffff) return fail(PA_ERR_UNSUPPORTED, "prefill grid too large");
     CUtensorMap mk, mv;
     if (pa_status s = cache_tensor_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
@@ -538,7 +571,7 @@ pa_status launch_prefill_tc(const DecodeArgs& a) {
     prm.group = G;
     prm.num_seqs = a.num_seqs;
     prm.num_blocks = a.num_blocks;
-    prm.max_chunks = (int)max_chunks;
+    prm.max_tasks = (int)max_tasks;
     prm.scale_log2 = a.scale * kLog2e;
     prm.out_f32 = a.out_dtype == PA_F32;
     if (a.kv_dtype == PA_BF16) return launch<__nv_bfloat16>(a, mk, mv, prm, grid);
