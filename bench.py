@@ -328,6 +328,11 @@ def run_ours(args, rank, world, local):
     alg_bytes = nbytes.get("decode_unique", nbytes["decode"])
     achieved = alg_bytes / dec_avg_s / 1e9
     roof_unit, bound, alg_units = "GB/s", "hbm", alg_bytes
+    # the library sends long query runs over a 16-bit cache with head_dim 128
+    # to the tensor-core prefill kernel
+    prefill_tc = (is_prefill(wl) and wl.kv_dtype in ("bf16", "f16") and wl.head_dim == 128
+                  and args.partition_size == 0 and si.shared is None
+                  and "PA_PREFILL_MMA_SYNC" not in os.environ)
     if is_prefill(wl):
         # long query runs: a contraction on the tensor cores, not a KV stream
         flops = attention_flops(wl)
@@ -365,7 +370,10 @@ def run_ours(args, rank, world, local):
                                    if world > 1 else "1 GPU")},
         "seq_steps_per_s": round(seq_steps, 1),
         "pct_of_hbm_peak": round(100 * value / hbm_peak, 2),
-        "roofline": {"kernel": ("pa_decode_shared_prefix (prefix_prep_kernel, "
+        "roofline": {"kernel": ("pa_decode (paged_prefill_tc_kernel: Q K^T and P V on the "
+                                "tcgen05 tensor cores, accumulators in TMEM)"
+                                if prefill_tc else
+                                "pa_decode_shared_prefix (prefix_prep_kernel, "
                                 "paged_decode_balanced_kernel + segment_reduce_kernel for the "
                                 "prefixes and for the suffixes, prefix_merge_kernel)"
                                 if si.shared is not None else
@@ -380,7 +388,8 @@ def run_ours(args, rank, world, local):
                      "peak_kind": peak_kind, "unit": roof_unit,
                      "frac": round(achieved / peak, 4),
                      "traffic": (recorded_traffic(kernel_family(wl.kv_dtype))
-                                 if args.partition_size == 0 and si.shared is None else None),
+                                 if args.partition_size == 0 and si.shared is None
+                                 and not is_prefill(wl) else None),
                      ("algorithmic_flops_per_launch" if bound == "tensor"
                       else "algorithmic_bytes_per_launch"): alg_units,
                      "decode_ms_avg": round(dec_avg_s * 1e3, 5),

@@ -23,11 +23,11 @@
 //                      the contraction index), O_x in TMEM for the whole range;
 //   out = O_x / l      read from TMEM at the end.
 //
-// The two warpgroups alternate on the tensor pipe (QK_0, PV_0, QK_1, PV_1 per
-// key tile), so one group's softmax runs while the other's products do.
-// Roles: warp 0 streams K/V tiles into a 4-stage ring (TMA), lane 0 of warp 1
-// issues the MMAs and commits them to mbarriers, warps 2-5 and 6-9 are the
-// softmax groups. Every wait is bounded; a wait that gives up stops the tile
+// The MMA warp issues whichever product of either Q tile is ready (products
+// of S first), so one group's softmax runs while the other's products do.
+// Roles: warp 0 streams K/V tiles into a 4-stage ring (TMA), warps 1 and 10
+// issue the MMAs of Q tile 0 and 1 (one elected lane each) and commit them to
+// mbarriers, warps 2-5 and 6-9 are the softmax groups. Every wait is bounded; a wait that gives up stops the tile
 // loop of every role, and the MMA thread waits for its own operations to
 // finish before TMEM is freed.
 #include <cuda.h>
@@ -53,7 +53,7 @@ constexpr int kQTiles = 2;              // Q tiles per CTA, one softmax warpgrou
 constexpr int kTaskRows = kRows * kQTiles;
 constexpr int kTok = 64;                // keys per K/V tile (S columns)
 constexpr int kTileBlocks = kTok / kBS; // 4
-constexpr int kThreads = 64 + 128 * kQTiles;   // producer, MMA, 2 softmax warpgroups
+constexpr int kThreads = 96 + 128 * kQTiles;   // producer, 2 MMA warps, 2 softmax warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyMax = 8.f;
 
@@ -67,16 +67,20 @@ constexpr int kKBytes = 16 * 1024;              // [2 sub][64 rows][128 B]
 constexpr int kSubKV = 8 * 1024;                // one 64-dim half of a K (or V) tile
 constexpr int kBarOff = kKVOff + kStages * kKVStage;   // mbarriers and flags
 constexpr int kSmem = kBarOff + 256 + 1024;     // + alignment slack
-// barrier slots: K/V full and empty per stage; per Q tile: S full, S free
-// (S read into registers), P full, O done; and the final drain
+// barrier slots: K/V full and empty per stage; per (Q tile x, S buffer b):
+// S full and P full (index 2x + b); per Q tile: O done and the final drain of
+// its MMA warp; V rows past the context zeroed (single use)
 constexpr int kBarKVFull = 0, kBarKVEmpty = kStages, kBarSFull = 2 * kStages,
-              kBarSFree = 2 * kStages + 2, kBarPFull = 2 * kStages + 4,
-              kBarODone = 2 * kStages + 6, kBarFin = 2 * kStages + 8;
-constexpr int kNumBars = 2 * kStages + 9;
-// TMEM columns (512): O of Q tile x at 128x, S at 256 + 64x, P at 384 + 64x
-// (P_hi in the first 32 columns, P_lo in the next 32, two 16-bit values each)
+              kBarPFull = 2 * kStages + 4, kBarODone = 2 * kStages + 8, kBarFin = 2 * kStages + 10,
+              kBarVZero = 2 * kStages + 12;
+constexpr int kNumBars = 2 * kStages + 13;
+// TMEM columns (512): O of Q tile x at 128x; two S buffers per Q tile at
+// 256 + 128x + 64b. P of a tile is written over the S buffer it came from
+// (P_hi in its first 32 columns, P_lo in the next 32, two 16-bit values per
+// column), so the product of S for tile t + 1 runs while the softmax of tile
+// t works, and the softmax never waits for a P V product to write P.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 256, kPCol = 384;
+constexpr uint32_t kSCol = 256;
 
 struct PrefillParams {
     void* out;
@@ -207,9 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tiles = (end_blocks + kTileBlocks - 1) / kTileBlocks;
 
     if (threadIdx.x == 0) {
-        // S free and P full take one arrival from each of the four warps of a softmax group
+        // P full and V zeroed take one arrival from each of the four warps of
+        // a softmax group; K/V empty one commit from each Q tile's MMA warp
         for (int i = 0; i < kNumBars; ++i)
-            pa::mbar_init(bars + 8 * i, (i >= kBarSFree && i < kBarODone) ? 4 : 1);
+            pa::mbar_init(bars + 8 * i, ((i >= kBarPFull && i < kBarODone) || i == kBarVZero) ? 4
+                                        : (i >= kBarKVEmpty && i < kBarKVEmpty + kStages) ? nq
+                                                                                            : 1);
         *abort_flag = 0;
         pa::fence_barrier_init();
         pa::prefetch_tensormap(&tmap_k);
@@ -244,9 +251,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ---------------- producer: K/V blocks of each tile ----------------
+        // lane j handles block j of a tile; the block ids of the next tile are
+        // fetched before waiting for the stage
+        auto block_row = [&](int t) {
+            const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
+            if (t >= tiles || lane >= nblk) return -1;
+            int blk = __ldg(p.block_tables + (int64_t)s * p.max_blocks + t * kTileBlocks + lane);
+            if (blk < 0 || blk >= p.num_blocks) {
+                if (p.err) atomicOr(p.err, pa::ERR_BAD_BLOCK);
+                blk = 0;
+            }
+            return (blk * p.num_kv_heads + g) * kBS;
+        };
         int issued = 0;
+        int row = block_row(0);
         for (int t = 0; t < tiles; ++t) {
             const int st = t % kStages;
+            const int next_row = block_row(t + 1);
             if (t >= kStages) {   // the stage is free once every product reading tile t - kStages is done
                 const bool ok = __all_sync(
                     0xffffffffu,
@@ -258,30 +279,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
-            int row = 0;
-            if (lane < nblk) {
-                int blk = __ldg(p.block_tables + (int64_t)s * p.max_blocks + t * kTileBlocks + lane);
-                if (blk < 0 || blk >= p.num_blocks) {
-                    if (p.err) atomicOr(p.err, pa::ERR_BAD_BLOCK);
-                    blk = 0;
-                }
-                row = (blk * p.num_kv_heads + g) * kBS;
-            }
             const uint32_t bar = bars + 8 * (kBarKVFull + st);
             if (lane == 0) pa::mbar_arrive_expect_tx(bar, nblk * 4 * (kBS * 128));
-            const uint32_t kst = base + kKVOff + st * kKVStage;
-            for (int j = 0; j < nblk; ++j) {
-                const int rj = __shfl_sync(0xffffffffu, row, j);
-                if (lane == 0) {
+            __syncwarp();
+            if (lane < nblk) {
+                const uint32_t kst = base + kKVOff + st * kKVStage + lane * (kBS * 128);
 #pragma unroll
-                    for (int sub = 0; sub < 2; ++sub) {
-                        pa::tma_load_2d(kst + sub * kSubKV + j * (kBS * 128), &tmap_k, sub * 64, rj,
-                                        bar);
-                        pa::tma_load_2d(kst + kKBytes + sub * kSubKV + j * (kBS * 128), &tmap_v,
-                                        sub * 64, rj, bar);
-                    }
+                for (int sub = 0; sub < 2; ++sub) {
+                    pa::tma_load_2d(kst + sub * kSubKV, &tmap_k, sub * 64, row, bar);
+                    pa::tma_load_2d(kst + kKBytes + sub * kSubKV, &tmap_v, sub * 64, row, bar);
                 }
             }
+            row = next_row;
             issued = t + 1;
         }
         // drain: no copy may be in flight when the CTA ends; the last kStages
@@ -294,73 +303,91 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.err) atomicOr(p.err, pa::ERR_WAIT_DRAIN);
                     break;
                 }
-    } else if (warp == 1) {
-        // ---------------- MMA issue (one thread) ----------------
-        // per key tile t: QK_0(t + 1), PV_0(t), QK_1(t + 1), PV_1(t); a Q tile's
-        // next product of S starts as soon as its softmax has read S into registers
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = pa::tc::idesc_f16(C::kBF16, false, false, kRows, kTok);
-            constexpr uint32_t idesc_pv = pa::tc::idesc_f16(C::kBF16, false, true, kRows, D);
-            auto issue_qk = [&](int x, int t) -> bool {   // S_x = Q_x K(t)^T
-                bool ok = true;
-                if (t >= 1)   // S_x is free once its softmax has read tile t - 1
-                    ok = pa::mbar_wait(bars + 8 * (kBarSFree + x), (t - 1) & 1, p.err,
-                                       pa::ERR_WAIT_FULL);
-                if (!ok || *abort_flag) return false;
-                pa::tc::fence_after_sync();
-                const uint32_t kst = base + kKVOff + (t % kStages) * kKVStage;
-                const uint32_t qb = base + kQOff + x * kQBytes;
+    } else if (warp == 1 || warp == 2 + 4 * kQTiles) {
+        // ---------------- MMA issue: one warp per Q tile (one elected lane issues) ----------------
+        // S is double-buffered: QK_x(t) writes buffer t & 1 once PV_x(t - 2),
+        // which read P_x(t - 2) from it, has completed. Order per key tile t:
+        // PV_x(t), then QK_x(t + 2). Each Q tile has its own issuing warp, so the
+        // waits and bookkeeping of one overlap the products of the other on
+        // the shared tensor pipe. Operands are made warp-uniform (read from
+        // lane 0) so the issue stays a converged, uniform instruction stream.
+        const int x = warp == 1 ? 0 : 1;
+        const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+        const uint32_t sb = __shfl_sync(0xffffffffu, base, 0);
+        const uint32_t bb = sb + kBarOff;
+        constexpr uint32_t idesc_qk = pa::tc::idesc_f16(C::kBF16, false, false, kRows, kTok);
+        constexpr uint32_t idesc_pv = pa::tc::idesc_f16(C::kBF16, false, true, kRows, D);
+        auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+            if (__all_sync(0xffffffffu, pa::mbar_try_wait(bar, parity))) return true;
+            const bool ok = __all_sync(0xffffffffu, pa::mbar_wait(bar, parity, p.err, pa::ERR_WAIT_FULL));
+            return ok && __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+        };
+        // descriptors of every operand start: a descriptor of address a + o is
+        // the one of a plus o >> 4 (the 14-bit address field does not overflow
+        // inside shared memory)
+        const uint64_t dq = pa::tc::smem_desc_sw128(sb + kQOff + x * kQBytes, 16, 1024);
+        const uint64_t dk = pa::tc::smem_desc_sw128(sb + kKVOff, 16, 1024);
+        const uint64_t dv = pa::tc::smem_desc_sw128(sb + kKVOff + kKBytes, kSubKV, 1024);
+        const uint32_t s_col = tm + kSCol + 128 * x, o_col = tm + 128 * x;
+        auto issue_qk = [&](int t) {   // S_x[t & 1] = Q_x K(t)^T
+            pa::tc::fence_after_sync();
+            const uint64_t b0 = dk + (uint64_t)(((t % kStages) * kKVStage) >> 4);
+            const uint32_t d = s_col + 64 * (t & 1);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a =
-                        pa::tc::smem_desc_sw128(qb + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = pa::tc::smem_desc_sw128(
-                        kst + (kk >> 2) * kSubKV + (kk & 3) * 32, 16, 1024);
-                    pa::tc::mma_f16_ss(tmem + kSCol + 64 * x, a, b, idesc_qk, kk > 0 ? 1u : 0u);
-                }
-                pa::tc::commit(bars + 8 * (kBarSFull + x));
-                return true;
-            };
-            auto issue_pv = [&](int x, int t) -> bool {   // O_x += P_x V(t)
-                const bool ok = pa::mbar_wait(bars + 8 * (kBarPFull + x), t & 1, p.err,
-                                              pa::ERR_WAIT_FULL);
-                if (!ok || *abort_flag) return false;
-                pa::tc::fence_after_sync();
-                const uint32_t kst = base + kKVOff + (t % kStages) * kKVStage;
-                const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
-                for (int kb = 0; kb < nblk; ++kb) {
-                    const uint64_t bv = pa::tc::smem_desc_sw128(
-                        kst + kKBytes + kb * (kBS * 128), kSubKV, 1024);
-#pragma unroll
-                    for (int part = 0; part < 2; ++part)
-                        pa::tc::mma_f16_ts(tmem + 128 * x, tmem + kPCol + 64 * x + 32 * part + 8 * kb,
-                                           bv, idesc_pv, (t > 0 || kb > 0 || part > 0) ? 1u : 0u);
-                }
-                pa::tc::commit(bars + 8 * (kBarODone + x));
-                return true;
-            };
-            auto kv_ready = [&](int t) {
-                return pa::mbar_wait(bars + 8 * (kBarKVFull + t % kStages), (t / kStages) & 1,
-                                     p.err, pa::ERR_WAIT_FULL);
-            };
-            bool ok = tiles > 0 && kv_ready(0) && issue_qk(0, 0) && (nq < 2 || issue_qk(1, 0));
-            for (int t = 0; ok && t < tiles; ++t) {
-                const bool more = t + 1 < tiles;
-                if (more && !(kv_ready(t + 1) && issue_qk(0, t + 1))) ok = false;
-                if (ok && !issue_pv(0, t)) ok = false;
-                if (ok && nq > 1) {
-                    if (more && !issue_qk(1, t + 1)) ok = false;
-                    if (ok && !issue_pv(1, t)) ok = false;
-                }
-                if (ok) pa::tc::commit(bars + 8 * (kBarKVEmpty + t % kStages));
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t qa = ((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4;
+                const uint32_t kb = ((kk >> 2) * kSubKV + (kk & 3) * 32) >> 4;
+                pa::tc::mma_f16_ss_warp(d, dq + qa, b0 + kb, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            if (!ok) *abort_flag = 1;
-            // every MMA this thread issued has finished before TMEM is freed
-            pa::tc::commit(bars + 8 * kBarFin);
-            if (!pa::mbar_wait(bars + 8 * kBarFin, 0, nullptr, 0) && p.err)
+            pa::tc::commit_warp(bb + 8 * (kBarSFull + 2 * x + (t & 1)));
+        };
+        auto issue_pv = [&](int t) {   // O_x += P_x(t) V(t)
+            pa::tc::fence_after_sync();
+            const uint64_t v0 = dv + (uint64_t)(((t % kStages) * kKVStage) >> 4);
+            const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
+            const uint32_t pc = s_col + 64 * (t & 1);
+            const uint32_t acc0 = t > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kb = 0; kb < kTileBlocks; ++kb) {
+                if (kb < nblk) {
+                    const uint64_t bv = v0 + (uint64_t)((kb * (kBS * 128)) >> 4);
+                    pa::tc::mma_f16_ts_warp(o_col, pc + 8 * kb, bv, idesc_pv, kb > 0 ? 1u : acc0);
+                    pa::tc::mma_f16_ts_warp(o_col, pc + 32 + 8 * kb, bv, idesc_pv, 1u);
+                }
+            }
+            pa::tc::commit_warp(bb + 8 * (kBarODone + x));
+        };
+        auto kv_ready = [&](int t) { return wait(bb + 8 * (kBarKVFull + t % kStages), (t / kStages) & 1); };
+        // the last tile may hold V rows past the context, which Q tile 0's
+        // softmax zeroes before its P of that tile is ready
+        const int zero_tile = end_blocks * kBS > L ? tiles - 1 : -1;
+        bool ok = x < nq;
+        if (ok) {
+            // both S buffers start free: the products of S for tiles 0 and 1
+            for (int t = 0; ok && t < min(tiles, 2); ++t) {
+                ok = kv_ready(t);
+                if (ok) issue_qk(t);
+            }
+            for (int t = 0; ok && t < tiles; ++t) {
+                ok = wait(bb + 8 * (kBarPFull + 2 * x + (t & 1)), (t >> 1) & 1);
+                if (ok && x == 1 && t == zero_tile) ok = wait(bb + 8 * kBarVZero, 0);
+                if (!ok) break;
+                issue_pv(t);
+                // every product of this Q tile reading K/V tile t has been issued
+                pa::tc::commit_warp(bb + 8 * (kBarKVEmpty + t % kStages));
+                if (t + 2 < tiles) {
+                    // PV_x(t) read S_x[t & 1]
+                    ok = kv_ready(t + 2) && wait(bb + 8 * (kBarODone + x), t & 1);
+                    if (ok) issue_qk(t + 2);
+                }
+            }
+            if (!ok && lane == 0) *abort_flag = 1;
+            // every MMA this warp issued has finished before TMEM is freed
+            pa::tc::commit_warp(bb + 8 * (kBarFin + x));
+            if (!__all_sync(0xffffffffu, pa::mbar_wait(bb + 8 * (kBarFin + x), 0, nullptr, 0)) &&
+                lane == 0 && p.err)
                 atomicOr(p.err, pa::ERR_WAIT_DRAIN);
         }
-        __syncwarp();
     } else if ((warp - 2) / 4 < nq) {
         // ---------------- softmax and epilogue: one thread per row of Q tile x ----------------
         const int x = (warp - 2) / 4;
@@ -376,28 +403,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the smallest bound of the tile's rows: tiles ending at or before it need no mask
         const int bound_min = min(L - r + row_off / G, L - 1);
         const uint32_t trow = tmem + ((uint32_t)lane_base << 16);
-        const uint32_t s_tm = trow + kSCol + 64 * x, p_tm = trow + kPCol + 64 * x,
-                       o_tm = trow + 128 * x;
-        const uint32_t bar_sfull = bars + 8 * (kBarSFull + x), bar_sfree = bars + 8 * (kBarSFree + x),
-                       bar_pfull = bars + 8 * (kBarPFull + x), bar_odone = bars + 8 * (kBarODone + x);
+        const uint32_t s_tm = trow + kSCol + 128 * x, o_tm = trow + 128 * x;
+        const uint32_t bar_odone = bars + 8 * (kBarODone + x);
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         const int grp_tid = (warp - 2 - 4 * x) * 32 + lane;  // 0..127 within the group
         int done = 0;
         for (int t = 0; t < tiles; ++t) {
-            bool ok = __all_sync(0xffffffffu,
-                                 pa::mbar_wait(bar_sfull, t & 1, p.err, pa::ERR_WAIT_FULL));
+            const int b = t & 1;                               // S / P buffer of this tile
+            bool ok = __all_sync(0xffffffffu, pa::mbar_wait(bars + 8 * (kBarSFull + 2 * x + b),
+                                                            (t >> 1) & 1, p.err, pa::ERR_WAIT_FULL));
             if (!ok || *abort_flag) {
                 if (lane == 0) *abort_flag = 1;
                 break;
             }
             pa::tc::fence_after_sync();
             float sv[kTok];
-            pa::tc::ld_64cols(s_tm, *reinterpret_cast<uint32_t(*)[64]>(sv));
-            // S is in registers: the next product may overwrite it
-            pa::tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) pa::mbar_arrive(bar_sfree);
+            pa::tc::ld_64cols(s_tm + 64 * b, *reinterpret_cast<uint32_t(*)[64]>(sv));
             const int tok0 = t * kTok;
             if (tok0 + kTok - 1 > bound_min) {               // a tile some row must not see all of
 #pragma unroll
@@ -435,8 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[64];
 #pragma unroll
             for (int j = 0; j < kTok / 2; ++j) C::split(sv[2 * j], sv[2 * j + 1], pk[j], pk[32 + j]);
-            // P_x and O_x are free once the P V product of tile t - 1 is done
-            if (t >= 1) {
+            // O_x may be rescaled once the P V product of tile t - 1 is done
+            // (rare: the running max moves by more than 2^8 after the first tile)
+            if (t >= 1 && __any_sync(0xffffffffu, moved)) {
                 ok = __all_sync(0xffffffffu,
                                 pa::mbar_wait(bar_odone, (t - 1) & 1, p.err, pa::ERR_WAIT_FULL));
                 if (!ok || *abort_flag) {
@@ -444,22 +467,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 pa::tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, moved)) {
-                    // rescale this warp's rows of O in TMEM (alpha = 1 for the others)
+                // rescale this warp's rows of O in TMEM (alpha = 1 for the others)
+#pragma unroll 1
+                for (int q = 0; q < D / 16; ++q) {
+                    uint32_t ov[16];
+                    pa::tc::ld_16cols(o_tm + 16 * q, ov);
 #pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        float ov[32];
-                        pa::tc::ld_32cols(o_tm + 32 * q, ov);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) fma2(ov[i], ov[i + 1], ov[i], ov[i + 1], alpha, alpha, 0.f, 0.f);
-                        pa::tc::st_32cols(o_tm + 32 * q, ov);
-                    }
+                    for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    pa::tc::st_16cols(o_tm + 16 * q, ov);
                 }
             }
-            pa::tc::st_64cols(p_tm, pk);
+            // P over the S buffer it came from (this thread's row only)
+            pa::tc::st_64cols(s_tm + 64 * b, pk);
             // V rows past the context (in the sequence's last block) may hold
             // anything: zero them so that P = 0 never meets a NaN (Q tile 0's
-            // group does it; both products of the tile run after its P is ready)
+            // group does it and signals Q tile 1's MMA warp)
             const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
             const int tok_end = tok0 + nblk * kBS;
             if (x == 0 && L < tok_end) {
@@ -476,13 +498,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             // each warp releases its part (no group-wide barrier a stalled warp could hold)
             pa::tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) pa::mbar_arrive(bar_pfull);
+            if (lane == 0) {
+                pa::mbar_arrive(bars + 8 * (kBarPFull + 2 * x + b));
+                // Q tile 1's product of this tile reads the zeroed rows
+                if (x == 0 && L < tok_end) pa::mbar_arrive(bars + 8 * kBarVZero);
+            }
             done = t + 1;
         }
         // epilogue: O / l for this row
         if (done == tiles && tiles > 0) {
-            const bool ok = __all_sync(
-                0xffffffffu, pa::mbar_wait(bar_odone, (tiles - 1) & 1, p.err, pa::ERR_WAIT_FULL));
+            // the last two P V products, in order (a parity wait tells apart
+            // only neighbouring phases of the barrier)
+            bool ok = true;
+            for (int t = tiles >= 2 ? tiles - 2 : 0; ok && t < tiles; ++t)
+                ok = __all_sync(0xffffffffu,
+                                pa::mbar_wait(bar_odone, t & 1, p.err, pa::ERR_WAIT_FULL));
             if (ok) {
                 pa::tc::fence_after_sync();
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
