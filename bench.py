@@ -232,12 +232,14 @@ def unique_kv_bytes(wl, group_start, prefix_len):
     return toks * per_tok
 
 
-def launches_per_step(si, partition_size):
+def launches_per_step(si, partition_size, prefill_tc=False):
     n = 1                                               # append
     if si.pairs is not None:
         n += 1                                          # copy_blocks
     if si.shared is not None:
         return n + 6                                    # prep, 2 x (decode + reduce), merge
+    if prefill_tc:
+        return n + 2                                    # task order, tensor-core prefill
     n += 1                                              # decode
     if partition_size == 0 or si.max_context_len > partition_size:
         n += 1                                          # partial-result reduce
@@ -395,7 +397,7 @@ def run_ours(args, rank, world, local):
                      "decode_ms_avg": round(dec_avg_s * 1e3, 5),
                      "decode_ms_p50": round(statistics.median(dec_ms), 5)},
         "e2e": e2e,
-        "gpu_launches": launches_per_step(si, args.partition_size) * K,
+        "gpu_launches": launches_per_step(si, args.partition_size, prefill_tc) * K,
         "clocks": sampler.summary(),
         "wall_s_timed": round(wall1 - wall0, 3),
     }

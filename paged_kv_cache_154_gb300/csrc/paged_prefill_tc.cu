@@ -98,7 +98,88 @@ struct PrefillParams {
     int max_tasks;      // 256-row tasks per (sequence, kv head)
     float scale_log2;
     int out_f32;
+    const int32_t* order;   // task of each CTA, longest first (null: natural order)
 };
+
+// A task: rows task_off .. task_off + task_rows - 1 of (sequence s, kv head g)
+// (row = query token x G + q head within the group), over key tiles 0 .. tiles - 1.
+struct Task {
+    int c, s, g;
+    int L, q0, r;
+    int task_off, task_rows;
+    int end_blocks, tiles;
+};
+
+// Natural task index i: 256-row chunk c = i / (S x H_kv), then sequence, then kv head.
+__device__ __forceinline__ Task task_of(const PrefillParams& p, int i) {
+    Task k;
+    const int sh = p.num_seqs * p.num_kv_heads;
+    k.c = i / sh;
+    k.s = (i % sh) / p.num_kv_heads;
+    k.g = (i % sh) % p.num_kv_heads;
+    k.L = __ldg(p.context_lens + k.s);
+    if (p.qsl) {
+        k.q0 = __ldg(p.qsl + k.s);
+        k.r = __ldg(p.qsl + k.s + 1) - k.q0;
+    } else {
+        k.q0 = k.s;
+        k.r = 1;
+    }
+    const int G = p.group;
+    k.task_off = k.c * kTaskRows;
+    k.task_rows = min(kTaskRows, G * k.r - k.task_off);
+    if (k.task_rows <= 0) {
+        k.end_blocks = k.tiles = 0;
+        return k;
+    }
+    // the last row of the task sees keys up to L - r + jmax (causal)
+    const int jmax = min(k.r - 1, (k.task_off + k.task_rows - 1) / G);
+    k.end_blocks = min((k.L + kBS - 1) / kBS, (k.L - k.r + jmax) / kBS + 1);
+    k.tiles = (k.end_blocks + kTileBlocks - 1) / kTileBlocks;
+    return k;
+}
+
+// Longest-first order of the tasks (a counting sort on the key-tile count,
+// clamped to kOrderKeys - 1), so that the block scheduler starts the long
+// tasks first and the short ones fill the tail. One CTA.
+constexpr int kOrderKeys = 4096;
+constexpr int kOrderThreads = 1024;
+
+__global__ void __launch_bounds__(kOrderThreads)
+    prefill_order_kernel(const PrefillParams p, int num_tasks, int32_t* order) {
+    __shared__ int hist[kOrderKeys];
+    pa::grid_dependency_wait();
+    pa::grid_dependents_launch();
+    for (int k = threadIdx.x; k < kOrderKeys; k += kOrderThreads) hist[k] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < num_tasks; i += kOrderThreads)
+        atomicAdd(&hist[min(task_of(p, i).tiles, kOrderKeys - 1)], 1);
+    __syncthreads();
+    // start of each key's run, keys in descending order: a scan of 4 keys
+    // per thread, then of the per-thread sums
+    constexpr int kPer = kOrderKeys / kOrderThreads;
+    __shared__ int part[kOrderThreads];
+    const int k0 = kOrderKeys - kPer * (threadIdx.x + 1);          // this thread's keys, high first
+    int sum = 0;
+    for (int j = kPer - 1; j >= 0; --j) sum += hist[k0 + j];
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    for (int off = 1; off < kOrderThreads; off <<= 1) {            // inclusive scan
+        const int v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int run = part[threadIdx.x] - sum;                             // exclusive
+    for (int j = kPer - 1; j >= 0; --j) {
+        const int h = hist[k0 + j];
+        hist[k0 + j] = run;
+        run += h;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < num_tasks; i += kOrderThreads)
+        order[atomicAdd(&hist[min(task_of(p, i).tiles, kOrderKeys - 1)], 1)] = i;
+}
 
 // byte offset of 16-byte chunk c (0..7) of row `row` inside a 128-byte-wide,
 // 128-byte-swizzled matrix (8-row atoms of 1024 bytes)
@@ -187,28 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     pa::grid_dependents_launch();
     pa::grid_dependency_wait();
 
-    // task: (256-row chunk, sequence, kv head), later chunks (longer key ranges) first
-    const int sh = p.num_seqs * p.num_kv_heads;
-    const int c = p.max_tasks - 1 - (int)(blockIdx.x / sh);
-    const int s = (int)(blockIdx.x % sh) / p.num_kv_heads;
-    const int g = (int)(blockIdx.x % sh) % p.num_kv_heads;
-    const int L = __ldg(p.context_lens + s);
-    int q0, r;
-    if (p.qsl) {
-        q0 = __ldg(p.qsl + s);
-        r = __ldg(p.qsl + s + 1) - q0;
-    } else {
-        q0 = s;
-        r = 1;
-    }
+    // task of this CTA: longest first when ordered, else later chunks (longer
+    // key ranges) first
+    const int ntask = p.max_tasks * p.num_seqs * p.num_kv_heads;
+    const Task tk = task_of(p, p.order ? __ldg(p.order + blockIdx.x) : ntask - 1 - (int)blockIdx.x);
+    const int s = tk.s, g = tk.g, L = tk.L, q0 = tk.q0, r = tk.r;
     const int G = p.group;
-    const int task_off = c * kTaskRows;
-    const int task_rows = min(kTaskRows, G * r - task_off);
+    const int task_off = tk.task_off, task_rows = tk.task_rows;
     if (task_rows <= 0) return;                                  // uniform over the CTA
     const int nq = task_rows > kRows ? 2 : 1;                    // Q tiles with rows
-    const int jmax = min(r - 1, (task_off + task_rows - 1) / G);
-    const int end_blocks = min((L + kBS - 1) / kBS, (L - r + jmax) / kBS + 1);
-    const int tiles = (end_blocks + kTileBlocks - 1) / kTileBlocks;
+    const int end_blocks = tk.end_blocks, tiles = tk.tiles;
 
     if (threadIdx.x == 0) {
         // P full and V zeroed take one arrival from each of the four warps of
@@ -604,6 +673,18 @@ pa_status launch_prefill_tc(const DecodeArgs& a) {
     prm.max_tasks = (int)max_tasks;
     prm.scale_log2 = a.scale * kLog2e;
     prm.out_f32 = a.out_dtype == PA_F32;
+    // the task order goes to the start of the balanced schedule's workspace
+    // (the caller sized it with pa_decode_workspace_size, 256-byte aligned)
+    const BalancedShape ws = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim,
+                                            a.max_q_len, a.max_context_len);
+    if (a.slots && grid * 4 <= ws.workspace_bytes) {
+        prm.order = static_cast<int32_t*>(a.slots);
+        if (pa_status s = pa::cuda_status(
+                pa::launch_pdl(prefill_order_kernel, dim3(1), dim3(kOrderThreads), 0, a.stream,
+                               prm, (int)grid, static_cast<int32_t*>(a.slots)),
+                "prefill order launch"))
+            return s;
+    }
     if (a.kv_dtype == PA_BF16) return launch<__nv_bfloat16>(a, mk, mv, prm, grid);
     return launch<__half>(a, mk, mv, prm, grid);
 }
