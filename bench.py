@@ -34,6 +34,8 @@ PROFILES = {
     "16bit": ("paged_decode_llama3_8b.md", ("paged_decode.cu", "balanced.cuh", "ptx.cuh")),
     "int8": ("paged_decode_int8_mixed.md", ("paged_decode_int8.cu", "balanced.cuh", "ptx.cuh")),
     "fp8": ("paged_decode_fp8_llama3_8b.md", ("paged_decode_fp8.cu", "balanced.cuh", "ptx.cuh")),
+    "prefill": ("paged_prefill_tc_llama3_8b_chunked.md",
+                ("paged_prefill_tc.cu", "tcgen05.cuh", "ptx.cuh")),
 }
 
 
@@ -389,7 +391,8 @@ def run_ours(args, rank, world, local):
                      "bound": bound, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": roof_unit,
                      "frac": round(achieved / peak, 4),
-                     "traffic": (recorded_traffic(kernel_family(wl.kv_dtype))
+                     "traffic": (recorded_traffic("prefill") if prefill_tc else
+                                 recorded_traffic(kernel_family(wl.kv_dtype))
                                  if args.partition_size == 0 and si.shared is None
                                  and not is_prefill(wl) else None),
                      ("algorithmic_flops_per_launch" if bound == "tensor"
