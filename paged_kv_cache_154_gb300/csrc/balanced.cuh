@@ -550,15 +550,17 @@ __global__ void __launch_bounds__(128) segment_reduce_rows_kernel(const Params p
 }
 
 // Launch the reduce for a balanced decode call (PDL, after the decode kernel).
-// One warp per (sequence, kv head, chunk, row) item while there are at most
-// 64K items (every item merges its own row, in parallel); past that (prefill:
-// thousands of rows per sequence, nearly all of them in segments held whole)
-// one CTA per worker, so only the owners of cut segments do any work.
+// One CTA per worker by default: only the owners of cut segments do any work,
+// reading the merge records the decode kernel left. The phases of a read-once
+// shared-prefix call (the ones that write log-sum-exp rows) merge long
+// fork-group prefixes cut into many pieces with up to G x forks rows each;
+// there one warp per (sequence, kv head, chunk, row) item merges its own row
+// in parallel, while there are at most 64K items.
 template <typename T, int D>
 cudaError_t launch_segment_reduce(const Params& prm, int max_chunks, int row_slots,
                                   cudaStream_t stream) {
     const int64_t items = (int64_t)prm.num_seqs * prm.num_kv_heads * max_chunks * row_slots;
-    if (items <= (1 << 16))
+    if (prm.lse_out && items <= (1 << 16))
         return pa::launch_pdl(segment_reduce_rows_kernel<T, D>, dim3((unsigned)((items + 3) / 4)),
                               dim3(128), 0, stream, prm, max_chunks, row_slots);
     return pa::launch_pdl(segment_reduce_kernel<T, D>, dim3((unsigned)prm.workers),

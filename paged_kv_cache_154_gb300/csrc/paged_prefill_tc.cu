@@ -139,46 +139,56 @@ __device__ __forceinline__ Task task_of(const PrefillParams& p, int i) {
     return k;
 }
 
-// Longest-first order of the tasks (a counting sort on the key-tile count,
-// clamped to kOrderKeys - 1), so that the block scheduler starts the long
-// tasks first and the short ones fill the tail. One CTA.
-constexpr int kOrderKeys = 4096;
+// Longest-first order of the tasks: a counting sort on the key-tile count
+// (clamped to kOrderThreads - 1), so that the block scheduler starts the long
+// tasks first and the short ones fill the tail. One CTA; thread k owns key
+// bucket kOrderThreads - 1 - k, so bucket starts are an exclusive scan in
+// thread order.
 constexpr int kOrderThreads = 1024;
+constexpr int kOrderCached = 16384;   // task keys kept in shared memory
 
 __global__ void __launch_bounds__(kOrderThreads)
     prefill_order_kernel(const PrefillParams p, int num_tasks, int32_t* order) {
-    __shared__ int hist[kOrderKeys];
+    __shared__ int hist[kOrderThreads];
+    __shared__ int warp_sum[kOrderThreads / 32];
+    __shared__ uint16_t keys[kOrderCached];
     pa::grid_dependency_wait();
     pa::grid_dependents_launch();
-    for (int k = threadIdx.x; k < kOrderKeys; k += kOrderThreads) hist[k] = 0;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    auto key_of = [&](int i) {
+        return (i < kOrderCached) ? (int)keys[i] : min(task_of(p, i).tiles, kOrderThreads - 1);
+    };
+    hist[tid] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < num_tasks; i += kOrderThreads)
-        atomicAdd(&hist[min(task_of(p, i).tiles, kOrderKeys - 1)], 1);
-    __syncthreads();
-    // start of each key's run, keys in descending order: a scan of 4 keys
-    // per thread, then of the per-thread sums
-    constexpr int kPer = kOrderKeys / kOrderThreads;
-    __shared__ int part[kOrderThreads];
-    const int k0 = kOrderKeys - kPer * (threadIdx.x + 1);          // this thread's keys, high first
-    int sum = 0;
-    for (int j = kPer - 1; j >= 0; --j) sum += hist[k0 + j];
-    part[threadIdx.x] = sum;
-    __syncthreads();
-    for (int off = 1; off < kOrderThreads; off <<= 1) {            // inclusive scan
-        const int v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
-    }
-    int run = part[threadIdx.x] - sum;                             // exclusive
-    for (int j = kPer - 1; j >= 0; --j) {
-        const int h = hist[k0 + j];
-        hist[k0 + j] = run;
-        run += h;
+    for (int i = tid; i < num_tasks; i += kOrderThreads) {
+        const int k = min(task_of(p, i).tiles, kOrderThreads - 1);
+        if (i < kOrderCached) keys[i] = (uint16_t)k;
+        atomicAdd(&hist[k], 1);
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < num_tasks; i += kOrderThreads)
-        order[atomicAdd(&hist[min(task_of(p, i).tiles, kOrderKeys - 1)], 1)] = i;
+    // exclusive scan of the counts in descending key order
+    const int cnt = hist[kOrderThreads - 1 - tid];
+    int inc = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += v;
+    }
+    if (lane == 31) warp_sum[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        int w = warp_sum[lane], wi = w;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += v;
+        }
+        warp_sum[lane] = wi - w;                     // exclusive over warps
+    }
+    __syncthreads();
+    hist[kOrderThreads - 1 - tid] = warp_sum[wid] + inc - cnt;
+    __syncthreads();
+    for (int i = tid; i < num_tasks; i += kOrderThreads) order[atomicAdd(&hist[key_of(i)], 1)] = i;
 }
 
 // byte offset of 16-byte chunk c (0..7) of row `row` inside a 128-byte-wide,
