@@ -254,6 +254,12 @@ INT8_SMALL = [
      torch.bfloat16),
     ("int8_d64_f16q", [33, 700, 64, 129], [1, 2, 1, 3], 8, 2, 64, torch.float16),
     ("int8_mha", [200, 31], [1, 1], 4, 4, 128, torch.bfloat16),
+    # at least 32 query rows per KV head at d = 128 (also run through the
+    # opt-in tensor-core kernel below): contexts of 1 and 2 tokens, partial
+    # tiles, a long sequence cut across many shares, fp16 q
+    ("int8_mqa_tc_f16q", [1, 2, 17, 64, 65, 4097, 333, 16], [1, 1, 2, 1, 5, 1, 4, 1], 32, 1,
+     128, torch.float16),
+    ("int8_gqa8_verify_tc", [900, 45, 3000, 7], [4, 5, 3, 1], 32, 4, 128, torch.bfloat16),
 ]
 
 
@@ -269,11 +275,32 @@ def test_int8_small_shapes(case):
     check_out(ref, out, "int8")
 
 
-def test_int8_output_in_q_dtype():
-    wl = W.simple("int8_out16", 77, [300, 1000], [2, 1], 32, 1, 128, "int8",
-                  q_dtype=torch.bfloat16)
-    ref, cache, si, out = run_both(wl, out_dtype=torch.bfloat16)
-    check_out(ref, out, "int8", torch.bfloat16)
+@pytest.mark.parametrize("case", [c for c in INT8_SMALL if c[3] // c[4] * max(c[2]) >= 32
+                                  and c[5] == 128], ids=lambda c: c[0] + "_tc")
+def test_int8_tensor_core_kernel(case, monkeypatch):
+    """The opt-in tcgen05 INT8 kernel (PA_INT8_TC): 128-row chunks, fp16
+    (code - zp) operands built once per block, against the oracle."""
+    monkeypatch.setenv("PA_INT8_TC", "1")
+    name, lens, qlens, H, Hkv, d, qdt = case
+    wl = W.simple(name, 500 + len(name), lens, qlens, H, Hkv, d, "int8", q_dtype=qdt,
+                  key_row_boost=4.0, boost_fraction=0.02)
+    ref, cache, si, out = run_both(wl)
+    check_cache_bits(ref, cache)
+    check_out(ref, out, "int8")
+
+
+def test_mixed_int8_config_tensor_core_kernel(monkeypatch):
+    monkeypatch.setenv("PA_INT8_TC", "1")
+    wl = W.mixed_int8()
+    ref, cache, si, out = run_both(wl)
+    check_out(ref, out, "int8")
+
+
+@pytest.mark.parametrize("qdt", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+def test_int8_output_in_q_dtype(qdt):
+    wl = W.simple("int8_out16", 77, [300, 1000], [2, 1], 32, 1, 128, "int8", q_dtype=qdt)
+    ref, cache, si, out = run_both(wl, out_dtype=qdt)
+    check_out(ref, out, "int8", qdt)
 
 
 def test_mixed_int8_config():
@@ -284,14 +311,15 @@ def test_mixed_int8_config():
     check_out(ref, out, "int8")
 
 
-def test_int8_wide_value_range():
+@pytest.mark.parametrize("heads", [(16, 2), (32, 1)], ids=["gqa8", "mqa32"])
+def test_int8_wide_value_range(heads):
     """K/V rows scaled by 2^-6 .. 2^0 (per token and head) and q rows by
     2^-6 .. 2^6: the running power-of-two V reference must keep the small
     rows, and the per-row power-of-two q scaling must make the fp16
     conversion of q exact. (Outputs stay of order one, the regime the 1e-2
     tolerance is stated for; the fp16 weights carry 2^-11 relative error, below
     the INT8 quantisation step of 1/255 of a row's range.)"""
-    wl = W.simple("int8_range", 91, [800, 1200, 50], [1, 3, 1], 16, 2, 128, "int8",
+    wl = W.simple("int8_range", 91, [800, 1200, 50], [1, 3, 1], heads[0], heads[1], 128, "int8",
                   q_dtype=torch.bfloat16)
     rng = np.random.default_rng(0)
     for op in wl.phases[0] + wl.step:
