@@ -300,25 +300,28 @@ __device__ __forceinline__ void record_last_segment(const Params& p, int64_t wid
     }
 }
 
-// Merges the pieces of every cut segment: one CTA of eight warps per worker,
-// reading the worker's two slot headers in one round; a non-owner returns at
-// once. The owner's segment is merged row by row; when it has fewer than
-// eight rows the warps of a row split its pieces (warp j folds pieces j,
-// j + wpr, ...) and meet in shared memory. A lane owns D / 32 columns. Pieces
-// are read four at a time (independent loads) and folded into an online
-// log-sum-exp: out = sum 2^(m - M) O / sum 2^(m - M) l. At most 64 registers
-// a thread, so four CTAs fit on an SM.
+// Merges the pieces of every cut segment: CTAs of eight warps over (worker,
+// group of eight rows), reading the worker's two slot headers in one round;
+// a non-owner (or a row group past the segment's rows) returns at once. A
+// row with its own warp (or, with fewer than eight rows, wpr warps that
+// split its pieces and meet in shared memory) is merged in two passes: the
+// lanes take the pieces' (m, l) 32 at a time for the row's largest m and the
+// denominator sum 2^(m - M) l; then, the weights known, every lane adds its
+// D / 32 columns of every piece with independent loads (no chain through
+// the running maximum): out = sum 2^(m - M) O / sum 2^(m - M) l.
 constexpr int kReduceWarps = 8;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(32 * kReduceWarps, 4) segment_reduce_kernel(const Params p) {
+__global__ void __launch_bounds__(32 * kReduceWarps, 4) segment_reduce_kernel(const Params p,
+                                                                               int row_groups) {
     constexpr int EPL = D / 32;
-    constexpr int kBatch = 4;
+    constexpr int kUnroll = 4;                      // pieces whose loads are in flight together
     __shared__ int32_t hdr[17];                     // slot 0 words 0..7, slot 1 words 0..7, B
     __shared__ float part[kReduceWarps][D + 2];
     pa::grid_dependency_wait();     // the decode kernel's partials must be complete
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t w = blockIdx.x;
+    const int64_t w = blockIdx.x / row_groups;
+    const int rg = (int)(blockIdx.x % row_groups);
     if (w >= p.workers) return;
     if (threadIdx.x < 16)
         hdr[threadIdx.x] = __ldg(reinterpret_cast<const int32_t*>(
@@ -333,39 +336,55 @@ __global__ void __launch_bounds__(32 * kReduceWarps, 4) segment_reduce_kernel(co
     const int first_slot = hdr[8 + 7];
     const int32_t* piece = hdr + 8 * first_slot;
     const int g = piece[1], c = piece[2];
-    const int q0 = hdr[5], rows = hdr[6];
+    const int q0 = hdr[5], rows_all = hdr[6];
+    const int row0 = rg * kReduceWarps;
+    if (row0 >= rows_all) return;
+    const int rows = min(kReduceWarps, rows_all - row0);
     const int RT = p.rows_per_tile, G = p.group;
     const int64_t W = p.workers;
     const int64_t B = hdr[16];
     const bool may_be_empty = B < W;                 // only then can a share hold no block
-    // warps per row: 1 with eight rows or more, else up to 8 / rows
-    const int wpr = rows >= 8 ? 1 : (rows >= 4 ? 2 : (rows >= 2 ? 4 : 8));
-    const int rows_per_round = kReduceWarps / wpr;
-    for (int row0 = 0; row0 < rows; row0 += rows_per_round) {
-        const int row = row0 + warp / wpr, sub = warp % wpr;
-        const bool active = row < rows;
-        float M = -INFINITY, den = 0.f, acc[EPL];
+    // warps per row: the largest power of two with wpr x rows <= 8 (one round)
+    const int wpr = rows > 4 ? 1 : (rows > 2 ? 2 : (rows > 1 ? 4 : 8));
+    const int row = row0 + warp / wpr, sub = warp % wpr;
+    const bool active = warp / wpr < rows;
+    const int64_t np = wb - w + 1;                    // pieces of the segment (shares w .. wb)
+    auto slot_of = [&](int64_t x) {                   // the piece of share w + x, or null
+        const int64_t sh = w + x;
+        if (may_be_empty && sh != w && share_start(sh, B, W) == share_start(sh + 1, B, W))
+            return (uint8_t*)nullptr;
+        // later shares start inside the segment: their piece is in slot 0
+        return p.slots + (2 * sh + (sh == w ? first_slot : 0)) * (int64_t)p.slot_bytes;
+    };
+    float M = -INFINITY, den = 0.f, acc[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-        if (active) {
-            for (int64_t w0 = w + sub; w0 <= wb; w0 += (int64_t)kBatch * wpr) {
-                float lv[kBatch], mv[kBatch], ov[kBatch][EPL];
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    if (active) {
+        // pass 1: the row's largest m over this warp's pieces (sub, sub + wpr, ...)
+        for (int64_t x = sub + (int64_t)wpr * lane; x < np; x += (int64_t)wpr * 32) {
+            const uint8_t* sp = slot_of(x);
+            if (!sp) continue;
+            Slot sl(const_cast<uint8_t*>(sp), RT);
+            if (__ldg(sl.l + row) > 0.f) M = fmaxf(M, __ldg(sl.m + row));
+        }
 #pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int64_t x = w0 + (int64_t)j * wpr;
-                    bool ok = x <= wb;
-                    if (ok && may_be_empty && x != w)
-                        ok = share_start(x, B, W) != share_start(x + 1, B, W);
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        // pass 2: weights 2^(m - M), the denominator and the columns
+        if (M != -INFINITY) {
+            for (int64_t x0 = sub; x0 < np; x0 += (int64_t)wpr * kUnroll) {
+                float wv[kUnroll], lv[kUnroll], ov[kUnroll][EPL];
+#pragma unroll
+                for (int j = 0; j < kUnroll; ++j) {
+                    const int64_t x = x0 + (int64_t)j * wpr;
+                    wv[j] = 0.f;
                     lv[j] = 0.f;
-                    mv[j] = -INFINITY;
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) ov[j][e] = 0.f;
-                    if (ok) {
-                        // later shares start inside the segment: their piece is in slot 0
-                        const int slot = x == w ? first_slot : 0;
-                        Slot sl(p.slots + (2 * x + slot) * (int64_t)p.slot_bytes, RT);
+                    const uint8_t* sp = x < np ? slot_of(x) : nullptr;
+                    if (sp) {
+                        Slot sl(const_cast<uint8_t*>(sp), RT);
                         lv[j] = __ldg(sl.l + row);
-                        mv[j] = __ldg(sl.m + row);
+                        wv[j] = __ldg(sl.m + row);
                         const float* src = sl.o + (int64_t)row * D + lane * EPL;
                         if constexpr (EPL == 4) {
                             const float4 t = __ldg(reinterpret_cast<const float4*>(src));
@@ -376,69 +395,57 @@ __global__ void __launch_bounds__(32 * kReduceWarps, 4) segment_reduce_kernel(co
                         }
                     }
                 }
-                float Mb = M;
 #pragma unroll
-                for (int j = 0; j < kBatch; ++j)
-                    if (lv[j] > 0.f) Mb = fmaxf(Mb, mv[j]);
-                if (Mb == -INFINITY) continue;             // no piece of this batch saw a key
-                const float a = exp2f(M - Mb);
-                den *= a;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[e] *= a;
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const float wgt = lv[j] > 0.f ? exp2f(mv[j] - Mb) : 0.f;
+                for (int j = 0; j < kUnroll; ++j) {
+                    const float wgt = lv[j] > 0.f ? exp2f(wv[j] - M) : 0.f;
                     den += wgt * lv[j];
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) acc[e] += wgt * ov[j][e];
                 }
-                M = Mb;
             }
         }
-        if (wpr > 1) {
-            // the row's warps meet in shared memory; the first of them folds
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) part[warp][lane * EPL + e] = acc[e];
-            if (lane == 0) {
-                part[warp][D] = M;
-                part[warp][D + 1] = den;
-            }
-            __syncthreads();
-            if (active && sub == 0) {
-                float Mt = -INFINITY;
-                for (int j = 0; j < wpr; ++j)
-                    if (part[warp + j][D + 1] > 0.f) Mt = fmaxf(Mt, part[warp + j][D]);
-                float dt = 0.f;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-                for (int j = 0; j < wpr; ++j) {
-                    const float wgt =
-                        part[warp + j][D + 1] > 0.f ? exp2f(part[warp + j][D] - Mt) : 0.f;
-                    dt += wgt * part[warp + j][D + 1];
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) acc[e] += wgt * part[warp + j][lane * EPL + e];
-                }
-                M = Mt;
-                den = dt;
-            }
-            __syncthreads();                         // part is reused by the next round
-        }
-        if (!active || sub != 0) continue;
-        const int grow = c * RT + row;
-        const int64_t orow = (int64_t)(q0 + grow / G) * p.num_heads + g * G + grow % G;
-        const int64_t base = orow * D + lane * EPL;
-        const float inv = 1.f / den;
-        if (p.lse_out && lane == 0) p.lse_out[orow] = M + log2f(den);
-        if constexpr (EPL == 4) {
-            if (p.out_f32) {
-                *reinterpret_cast<float4*>(static_cast<float*>(p.out) + base) =
-                    make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-                continue;
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) store_out<T>(p.out, base + e, acc[e] * inv, p.out_f32);
     }
+    if (wpr > 1) {
+        // the row's warps meet in shared memory; the first of them folds
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) part[warp][lane * EPL + e] = acc[e];
+        if (lane == 0) {
+            part[warp][D] = M;
+            part[warp][D + 1] = den;
+        }
+        __syncthreads();
+        if (active && sub == 0) {
+            float Mt = -INFINITY;
+            for (int j = 0; j < wpr; ++j)
+                if (part[warp + j][D + 1] > 0.f) Mt = fmaxf(Mt, part[warp + j][D]);
+            float dt = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+            for (int j = 0; j < wpr; ++j) {
+                const float wgt = part[warp + j][D + 1] > 0.f ? exp2f(part[warp + j][D] - Mt) : 0.f;
+                dt += wgt * part[warp + j][D + 1];
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] += wgt * part[warp + j][lane * EPL + e];
+            }
+            M = Mt;
+            den = dt;
+        }
+    }
+    if (!active || sub != 0) return;
+    const int grow = c * RT + row;
+    const int64_t orow = (int64_t)(q0 + grow / G) * p.num_heads + g * G + grow % G;
+    const int64_t base = orow * D + lane * EPL;
+    const float inv = 1.f / den;
+    if (p.lse_out && lane == 0) p.lse_out[orow] = M + log2f(den);
+    if constexpr (EPL == 4) {
+        if (p.out_f32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + base) =
+                make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+            return;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) store_out<T>(p.out, base + e, acc[e] * inv, p.out_f32);
 }
 
 // Merges the pieces of every cut segment, one warp per (sequence, kv head,
@@ -563,8 +570,10 @@ cudaError_t launch_segment_reduce(const Params& prm, int max_chunks, int row_slo
     if (prm.lse_out && items <= (1 << 16))
         return pa::launch_pdl(segment_reduce_rows_kernel<T, D>, dim3((unsigned)((items + 3) / 4)),
                               dim3(128), 0, stream, prm, max_chunks, row_slots);
-    return pa::launch_pdl(segment_reduce_kernel<T, D>, dim3((unsigned)prm.workers),
-                          dim3(32 * kReduceWarps), 0, stream, prm);
+    // CTAs over (worker, group of eight rows) of the most rows a chunk holds
+    const int row_groups = (row_slots + kReduceWarps - 1) / kReduceWarps;
+    return pa::launch_pdl(segment_reduce_kernel<T, D>, dim3((unsigned)(prm.workers * row_groups)),
+                          dim3(32 * kReduceWarps), 0, stream, prm, row_groups);
 }
 
 }  // namespace sched
