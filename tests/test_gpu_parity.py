@@ -358,6 +358,9 @@ PREFILL = [
     ("prefill_over_context", [164, 900, 1000], [64, 200, 128], 32, 8, 128, "bf16"),
     ("prefill_mha_d64_f16", [300, 90], [150, 90], 8, 8, 64, "f16"),
     ("prefill_mqa", [400, 333], [96, 33], 32, 1, 128, "bf16"),
+    # the tensor-core kernel over an fp16 cache; task rows not a multiple of
+    # 128 (a half-empty second Q tile), a context ending mid-block
+    ("prefill_tc_f16_ragged", [517, 70, 1234], [77, 70, 300], 16, 4, 128, "f16"),
 ]
 
 
@@ -370,6 +373,24 @@ def test_paged_prefill_matches_oracle(case):
     ref, cache, si, out = run_both(wl)
     check_cache_bits(ref, cache)
     check_out(ref, out, dt)
+
+
+def test_paged_prefill_peaked_softmax():
+    """2% of the key rows scaled by 8: peaked softmaxes whose running max moves
+    by more than 2^8 mid-stream (the tensor-core kernel rescales O in TMEM)."""
+    wl = W.simple("prefill_peaked", 621, [1500, 640], [320, 256], 32, 8, 128, "bf16",
+                  key_row_boost=8.0, boost_fraction=0.02)
+    ref, cache, si, out = run_both(wl)
+    check_out(ref, out, "bf16")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_paged_prefill_output_in_cache_dtype(dt):
+    """The tensor-core prefill kernel writing 16-bit outputs."""
+    qdt = torch.bfloat16 if dt == "bf16" else torch.float16
+    wl = W.simple("prefill_out16_" + dt, 620, [700, 300], [256, 100], 32, 8, 128, dt)
+    ref, cache, si, out = run_both(wl, out_dtype=qdt)
+    check_out(ref, out, dt, qdt)
 
 
 @pytest.mark.parametrize("kv", ["int8", "fp8"])
