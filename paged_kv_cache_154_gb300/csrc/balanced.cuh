@@ -300,20 +300,18 @@ __device__ __forceinline__ void record_last_segment(const Params& p, int64_t wid
     }
 }
 
-// Merges the pieces of every cut segment: CTAs of eight warps over (worker,
-// group of eight rows), reading the worker's two slot headers in one round;
-// a non-owner (or a row group past the segment's rows) returns at once. A
-// row with its own warp (or, with fewer than eight rows, wpr warps that
-// split its pieces and meet in shared memory) is merged in two passes: the
+// Merges the pieces of every cut segment: CTAs of kReduceWarps warps over
+// (worker, group of kReduceWarps rows), reading the worker's two slot headers
+// in one round; a non-owner (or a row group past the segment's rows) returns
+// at once. A row with its own warp (or, with fewer rows than warps, wpr warps
+// that split its pieces and meet in shared memory) is merged in two passes: the
 // lanes take the pieces' (m, l) 32 at a time for the row's largest m and the
 // denominator sum 2^(m - M) l; then, the weights known, every lane adds its
 // D / 32 columns of every piece with independent loads (no chain through
 // the running maximum): out = sum 2^(m - M) O / sum 2^(m - M) l.
-constexpr int kReduceWarps = 8;
-
-template <typename T, int D>
-__global__ void __launch_bounds__(32 * kReduceWarps, 4) segment_reduce_kernel(const Params p,
-                                                                               int row_groups) {
+template <typename T, int D, int kReduceWarps>
+__global__ void __launch_bounds__(32 * kReduceWarps, 32 / kReduceWarps) segment_reduce_kernel(
+    const Params p, int row_groups) {
     constexpr int EPL = D / 32;
     constexpr int kUnroll = 4;                      // pieces whose loads are in flight together
     __shared__ int32_t hdr[17];                     // slot 0 words 0..7, slot 1 words 0..7, B
@@ -344,8 +342,9 @@ __global__ void __launch_bounds__(32 * kReduceWarps, 4) segment_reduce_kernel(co
     const int64_t W = p.workers;
     const int64_t B = hdr[16];
     const bool may_be_empty = B < W;                 // only then can a share hold no block
-    // warps per row: the largest power of two with wpr x rows <= 8 (one round)
-    const int wpr = rows > 4 ? 1 : (rows > 2 ? 2 : (rows > 1 ? 4 : 8));
+    // warps per row: the largest power of two with wpr x rows <= kReduceWarps (one round)
+    int wpr = 1;
+    while (2 * wpr * rows <= kReduceWarps) wpr *= 2;
     const int row = row0 + warp / wpr, sub = warp % wpr;
     const bool active = warp / wpr < rows;
     const int64_t np = wb - w + 1;                    // pieces of the segment (shares w .. wb)
@@ -570,10 +569,19 @@ cudaError_t launch_segment_reduce(const Params& prm, int max_chunks, int row_slo
     if (prm.lse_out && items <= (1 << 16))
         return pa::launch_pdl(segment_reduce_rows_kernel<T, D>, dim3((unsigned)((items + 3) / 4)),
                               dim3(128), 0, stream, prm, max_chunks, row_slots);
-    // CTAs over (worker, group of eight rows) of the most rows a chunk holds
-    const int row_groups = (row_slots + kReduceWarps - 1) / kReduceWarps;
-    return pa::launch_pdl(segment_reduce_kernel<T, D>, dim3((unsigned)(prm.workers * row_groups)),
-                          dim3(32 * kReduceWarps), 0, stream, prm, row_groups);
+    // CTAs over (worker, group of rows) of the most rows a chunk holds: four
+    // warps (and rows) a CTA when segments are cut into few pieces (workers
+    // per segment, on average, at most 8); eight when few long segments are
+    // each cut into many pieces, which the warps of a row then share.
+    const int64_t segments = (int64_t)prm.num_seqs * prm.num_kv_heads * max_chunks;
+    if (prm.workers <= 8 * segments) {
+        const int row_groups = (row_slots + 3) / 4;
+        return pa::launch_pdl(segment_reduce_kernel<T, D, 4>, dim3((unsigned)(prm.workers * row_groups)),
+                              dim3(128), 0, stream, prm, row_groups);
+    }
+    const int row_groups = (row_slots + 7) / 8;
+    return pa::launch_pdl(segment_reduce_kernel<T, D, 8>, dim3((unsigned)(prm.workers * row_groups)),
+                          dim3(256), 0, stream, prm, row_groups);
 }
 
 }  // namespace sched
