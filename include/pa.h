@@ -237,11 +237,13 @@ pa_status pa_append_kv(const void* key, const void* value, pa_dtype src_dtype,
                        int32_t block_size, void* stream);
 
 /* Bytes of workspace pa_decode needs for these sizes (0 if none). With
- * partition_size 0 (the balanced schedule) this is 2 x min(2048,
- * num_seqs x num_kv_heads x ceil(max_context_len/16)) partial slots of
- * 16 + 4 x R x (head_dim + 2) bytes (rounded up to 16), R = (num_heads /
- * num_kv_heads) x max_q_len; with partition_size > 0 see pa_decode. Returns
- * 0 for invalid sizes. Host-only: needs no GPU. */
+ * partition_size 0 (the balanced schedule) this is 24576 bytes of arrival
+ * counters, the per-sequence prefix sums (4 x (num_seqs + 1) bytes rounded
+ * up to 256) and 2 x min(2048, num_seqs x num_kv_heads x
+ * ceil(max_context_len/16)) partial slots of 32 + 4 x R x (head_dim + 2)
+ * bytes (rounded up to 16), R = (num_heads / num_kv_heads) x max_q_len
+ * (at least 64 rows once R > 16); with partition_size > 0 see pa_decode.
+ * Returns 0 for invalid sizes. Host-only: needs no GPU. */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_tokens,
                                 int32_t num_heads, int32_t num_kv_heads,
                                 int32_t head_dim, int32_t max_q_len,
@@ -269,12 +271,25 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_tokens,
  *                  of all (sequence, KV head, block) work; a share that
  *                  covers a (sequence, KV head) whole writes its output, and
  *                  where share boundaries cut one, the pieces' partials
- *                  (m, l, O) are merged by a log-sum-exp reduce. A multiple
+ *                  (m, l, O) are merged with the log-sum-exp rule (by the
+ *                  decode kernel itself for F16/BF16 caches with at most 16
+ *                  query rows per KV head, else by a reduce kernel). A multiple
  *                  of 16 up to 4096 selects fixed split-KV partitions of that
  *                  many tokens (one CTA per partition, KV head and sequence).
  *   workspace      device memory of pa_decode_workspace_size() bytes,
- *                  256-byte aligned (NULL allowed if that size is 0); its
- *                  contents need no initialisation. Layout with
+ *                  256-byte aligned (NULL allowed if that size is 0). Its
+ *                  first 24576 bytes are 6144 uint32 arrival counters: they
+ *                  must be ZERO before the first call that uses the buffer
+ *                  (cudaMemset once, at allocation), and every call leaves
+ *                  them zero, so one buffer serves any sequence of calls of
+ *                  any sizes on one stream. With partition_size 0 the
+ *                  decode kernel counts the blocks of each cut (sequence,
+ *                  KV head) as its pieces finish, and the piece that
+ *                  completes the count merges them; a counter found
+ *                  non-zero sets PA_DEVERR_WORKSPACE in the device error
+ *                  word. After a call whose device error word is non-zero,
+ *                  zero the counters again. The rest needs no
+ *                  initialisation. Layout after the counters with
  *                  partition_size > 0 and P = ceil(max_context_len /
  *                  partition_size):
  *                    o_part fp32 [num_q_tokens][num_heads][P][head_dim]
@@ -323,9 +338,10 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents.
- *     Nothing in it needs to start at zero (each call writes every entry it
- *     reads), but calls whose work overlaps on the GPU (different streams,
- *     or different host threads) race on it and must be serialised. */
+ *     It starts zeroed (a static device array), and each call leaves its
+ *     arrival counters zero as pa_decode describes; calls whose work
+ *     overlaps on the GPU (different streams, or different host threads)
+ *     race on it and must be serialised. */
 pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
                              pa_dtype q_dtype, const void* k_cache,
                              const void* v_cache, pa_dtype kv_dtype,
@@ -373,7 +389,9 @@ size_t pa_decode_shared_prefix_workspace_size(
  *   max_group_q_len host: the largest number of query tokens in one group
  *   max_prefix_len  host: the largest prefix_len
  *   workspace     pa_decode_shared_prefix_workspace_size() bytes, 256-byte
- *                 aligned, no initialisation needed.
+ *                 aligned. Its first 24576 bytes are arrival counters with
+ *                 pa_decode's rule: zero before the first call, left zero
+ *                 by every call; the rest needs no initialisation.
  * Other arguments as pa_decode. Under PA_VALIDATE=1 the group arrays are
  * also checked against the block tables (PA_ERR_VALIDATION). INT8 caches
  * return PA_ERR_UNSUPPORTED. */
@@ -389,6 +407,15 @@ pa_status pa_decode_shared_prefix(
     const int32_t* prefix_len, int32_t num_groups, int32_t max_group_q_len,
     int32_t max_prefix_len, void* workspace, size_t workspace_bytes,
     void* stream);
+
+/* Device error word bits. */
+#define PA_DEVERR_WAIT_FULL  (1u << 0) /* a consumer gave up waiting for a staged tile */
+#define PA_DEVERR_WAIT_EMPTY (1u << 1) /* a producer gave up waiting for a free stage */
+#define PA_DEVERR_WAIT_DRAIN (1u << 2) /* the exit drain gave up on an in-flight copy */
+#define PA_DEVERR_BAD_BLOCK  (1u << 3) /* a block-table entry outside the pool */
+#define PA_DEVERR_BAD_SLOT   (1u << 4) /* a slot_mapping entry outside the pool */
+#define PA_DEVERR_BAD_GROUP  (1u << 5) /* a shared-prefix group range or prefix length */
+#define PA_DEVERR_WORKSPACE  (1u << 6) /* a workspace arrival counter was not zero */
 
 /* Read and clear the device error word that kernels set instead of
  * trapping (a bounded wait that gave up, an index a kernel refused).

@@ -57,6 +57,8 @@ struct Params {
     float* lse_out;                // may be null; else [num_q_tokens][num_heads] base-2 log-sum-exp
                                    // of each output row, in scale * log2(e) units
     int unmasked;                  // 1: every query row sees every key < L (no causal offset)
+    unsigned int* arrivals;        // may be null; else one counter per worker, zero on entry
+                                   // and on exit: the decode kernel merges cut segments itself
 };
 
 // First block a sequence attends (0 unless ctx_start is given).
@@ -298,6 +300,303 @@ __device__ __forceinline__ void record_last_segment(const Params& p, int64_t wid
         const int64_t fb = f1 + blocks_left;                 // one past the segment's end
         write_merge_record(p, wid, 1, (fb * p.workers - 1) / B, seg_first ? 0 : 1, q0, rows);
     }
+}
+
+// The share holding virtual block f: the largest w with share_start(w) <= f.
+__host__ __device__ __forceinline__ int64_t share_of(int64_t f, int64_t B, int64_t W) {
+    return ((f + 1) * W - 1) / B;
+}
+
+// In-kernel merge of cut segments. The pieces of a cut segment are merged by
+// whichever piece finishes last, so no reduce kernel runs after the decode
+// kernel and merges overlap other warps' streaming. After writing its slot,
+// a piece's warp adds its block count to a counter; the warp whose addition
+// completes the count knows that every piece it covers is written, merges
+// them, and resets the counter to zero for the next call. A segment of at
+// most kMergeFanIn shares is merged in one level (counter: by the share
+// where the segment starts). A longer one -- a long sequence cut by many
+// shares -- in two: the shares are grouped kMergeFanIn at a time, the last
+// piece of a group folds the group into one partial (m, l, O) written over
+// the slot of the group's first piece, and the last group to finish merges
+// the group partials. Counters live in three regions of kBalancedMaxWorkers
+// each, so no two levels or segments share one: group 0 (or a whole short
+// segment) by the segment's first share, groups 1.. by their first share (a
+// middle share of the segment, which no other segment's group can start
+// at), and the second level by the segment's first share.
+constexpr int kMergeFanIn = 8;
+constexpr int kCounterRegion = pa::kBalancedMaxWorkers;   // counters per region
+
+// Release: the warp barrier orders every lane's stores before lane 0's
+// acq_rel atomic (cumulative, as a CTA barrier before a thread's release);
+// acquire: the same atomic, then a warp barrier before the lanes read the
+// pieces (through L2, ld.global.cg). A count past the total means the
+// counters were not zero on entry.
+__device__ __forceinline__ bool arrive(const Params& p, unsigned int* cnt, int add, int total,
+                                       int lane) {
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        unsigned int old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                     : "=r"(old)
+                     : "l"(cnt), "r"((unsigned int)add)
+                     : "memory");
+        const unsigned int now = old + (unsigned int)add;
+        if (now > (unsigned int)total && p.err) atomicOr(p.err, pa::ERR_WORKSPACE);
+        last = now == (unsigned int)total;
+        if (last) atomicExch(cnt, 0u);   // no other piece counts here in this launch
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    __syncwarp();
+    return last != 0;
+}
+
+// Blocks of segment [fs, fs + nbs) held by shares sh .. min(sh + span - 1, wb).
+__device__ __forceinline__ int64_t blocks_in(int64_t B, int64_t W, int64_t fs, int nbs,
+                                             int64_t wb, int64_t sh, int span) {
+    const int64_t b0 = max(fs, share_start(sh, B, W));
+    const int64_t b1 = min(fs + nbs, share_start(min(sh + span - 1, wb) + 1, B, W));
+    return max((int64_t)0, b1 - b0);
+}
+
+// Partials staged in shared memory at a time by fold_partials, and the
+// shared memory it needs for them (four rows of D fp32 each).
+constexpr int kFoldBatch = 8;
+__host__ __device__ constexpr int fold_stage_bytes(int d) { return kFoldBatch * 4 * d * 4; }
+
+// Folds, row by row, the partials at shares s0, s0 + step, .. <= s1 of the
+// segment of nbs blocks from virtual block fs, held by shares wa .. wb (the
+// piece in wa in slot first_slot, the others in slot 0); with step 1 the
+// pieces themselves, with step kMergeFanIn the group partials. A share (or
+// group) holding no block of the segment wrote nothing and is skipped. Four
+// rows at a time: the rows of kFoldBatch partials are copied at once into
+// the warp's free staging buffer (cp.async, one round trip for the batch),
+// then every lane folds its D / 8 columns of one row with the log-sum-exp
+// rule. The result goes to slot `part` as a partial (m = M, l = sum
+// 2^(m_i - M) l_i, O = sum 2^(m_i - M) O_i) with the header of a piece
+// covering the shares s0 .. s1, or, with part null, to the output as O / l
+// (row j of the tile is query row c * RT + j of sequence s, first query
+// token q0, kv head g).
+template <typename T, int D>
+__device__ __forceinline__ void fold_partials(const Params& p, int64_t B, int64_t fs, int nbs,
+                                              int64_t wa, int64_t wb, int first_slot, int64_t s0,
+                                              int64_t s1, int step, int rows, uint8_t* part, int s,
+                                              int g, int c, int q0, uint32_t stage, int lane) {
+    constexpr int EPL = D / 8;
+    constexpr int kRowBytes = D * 4;
+    constexpr int kPerLane = 4 * kRowBytes / 16 / 32;   // 16-byte chunks a lane copies per partial
+    const int64_t W = p.workers;
+    const int RT = p.rows_per_tile, G = p.group;
+    const int cp = lane & 7;
+    // with at least as many blocks as shares every share holds one: no
+    // share (nor group) of the segment is empty, and no division is needed
+    const bool may_be_empty = B < W;
+    if (part && lane == 0) {
+        // tokens of the blocks of the segment in shares s0 .. s1
+        const int64_t b0 = max(fs, share_start(s0, B, W));
+        const int64_t b1 = min(fs + nbs, share_start(s1 + 1, B, W));
+        const int sb = first_block(p, s);
+        int32_t* hdr = reinterpret_cast<int32_t*>(part);
+        hdr[0] = s;
+        hdr[1] = g;
+        hdr[2] = c;
+        hdr[3] = (sb + (int)(b0 - fs)) * kBS;
+        hdr[4] = min((sb + (int)(b1 - fs)) * kBS, __ldg(p.context_lens + s));
+    }
+    // the staging buffer was last written by the tensor-copy engine
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    for (int r0 = 0; r0 < rows; r0 += 4) {
+        const int row = r0 + (lane >> 3);
+        const bool on = row < rows;
+        float M = -INFINITY, den = 0.f, acc[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+        for (int64_t x0 = s0; x0 <= s1; x0 += (int64_t)step * kFoldBatch) {
+            float mv[kFoldBatch], lv[kFoldBatch];
+            __syncwarp();   // every lane is done with the previous batch in the buffer
+#pragma unroll
+            for (int j = 0; j < kFoldBatch; ++j) {
+                const int64_t sh = x0 + (int64_t)j * step;
+                lv[j] = 0.f;
+                mv[j] = -INFINITY;
+                if (sh > s1 || (may_be_empty && blocks_in(B, W, fs, nbs, wb, sh, step) == 0))
+                    continue;                                               // warp-uniform
+                Slot sl(p.slots + (2 * sh + (sh == wa ? first_slot : 0)) * (int64_t)p.slot_bytes, RT);
+                if (on) {
+                    lv[j] = __ldcg(sl.l + row);
+                    mv[j] = __ldcg(sl.m + row);
+                }
+                // rows r0 .. r0 + 3 of the partial (r0 + 4 <= RT: in the slot)
+                const char* src = reinterpret_cast<const char*>(sl.o + (int64_t)r0 * D);
+#pragma unroll
+                for (int i = 0; i < kPerLane; ++i) {
+                    const int ch = lane + 32 * i;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                     stage + (uint32_t)(j * 4 * kRowBytes + ch * 16)),
+                                 "l"(src + ch * 16)
+                                 : "memory");
+                }
+            }
+            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < kFoldBatch; ++j) {
+                if (!(lv[j] > 0.f)) continue;          // no partial, or no visible key in it
+                const float Mn = fmaxf(M, mv[j]);
+                const float a = exp2f(M - Mn), b = exp2f(mv[j] - Mn);
+                den = den * a + b * lv[j];
+                const uint32_t at = stage + (uint32_t)(j * 4 * kRowBytes + (row - r0) * kRowBytes +
+                                                       cp * EPL * 4);
+#pragma unroll
+                for (int e = 0; e < EPL / 4; ++e) {
+                    float x, y, z, w;
+                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(x), "=f"(y), "=f"(z), "=f"(w)
+                                 : "r"(at + 16 * e));
+                    acc[4 * e + 0] = acc[4 * e + 0] * a + b * x;
+                    acc[4 * e + 1] = acc[4 * e + 1] * a + b * y;
+                    acc[4 * e + 2] = acc[4 * e + 2] * a + b * z;
+                    acc[4 * e + 3] = acc[4 * e + 3] * a + b * w;
+                }
+                M = Mn;
+            }
+        }
+        if (part) {
+            if (on) {
+                Slot sl(part, RT);
+                if (cp == 0) {
+                    sl.m[row] = M;
+                    sl.l[row] = den;
+                }
+                float4* dst = reinterpret_cast<float4*>(sl.o + (int64_t)row * D + cp * EPL);
+#pragma unroll
+                for (int e = 0; e < EPL / 4; ++e)
+                    dst[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+            }
+            continue;
+        }
+        if (!on) continue;
+        const int grow = c * RT + row;
+        const int64_t orow = (int64_t)(q0 + grow / G) * p.num_heads + g * G + grow % G;
+        const int64_t base = orow * D + cp * EPL;
+        const float inv = 1.f / den;
+        if (p.lse_out && cp == 0) p.lse_out[orow] = M + log2f(den);
+        if (p.out_f32) {
+#pragma unroll
+            for (int e = 0; e < EPL / 4; ++e)
+                reinterpret_cast<float4*>(static_cast<float*>(p.out) + base)[e] =
+                    make_float4(acc[4 * e] * inv, acc[4 * e + 1] * inv, acc[4 * e + 2] * inv,
+                                acc[4 * e + 3] * inv);
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) store_out<T>(p.out, base + e, acc[e] * inv, 0);
+        }
+    }
+}
+
+// A piece of a cut segment, as the warp that wrote it sees it: pb of the
+// segment's nbs blocks (from virtual block fs, held by shares wa .. wb, its
+// first piece in slot first_slot of share wa) of (sequence s, kv head g, row
+// chunk c; first query token q0, rows rows of the tile); the counter it
+// counts its blocks into and the total that completes that counter; for a
+// segment of more than kMergeFanIn shares, the group g0 .. g1 it belongs to.
+struct CutPiece {
+    int64_t fs, wa, wb, g0, g1;
+    unsigned int* cnt;
+    int pb, nbs, s, g, c, q0, rows, first_slot, total;
+    bool two_level;
+};
+
+// wa_known / wb_known: the first / last share of the segment when the caller
+// knows it (-1 otherwise), which spares a 64-bit division each; f_wa: the
+// first block of share wa when wa_known.
+__device__ __forceinline__ CutPiece cut_piece(const Params& p, int64_t B, int64_t wme, int64_t fs,
+                                              int pb, int nbs, int s, int g, int c, int q0,
+                                              int rows, int64_t wa_known, int64_t f_wa,
+                                              int64_t wb_known) {
+    const int64_t W = p.workers;
+    CutPiece x;
+    x.fs = fs;
+    x.pb = pb;
+    x.nbs = nbs;
+    x.s = s;
+    x.g = g;
+    x.c = c;
+    x.q0 = q0;
+    x.rows = rows;
+    x.wa = wa_known >= 0 ? wa_known : share_of(fs, B, W);
+    x.wb = wb_known >= 0 ? wb_known : share_of(fs + nbs - 1, B, W);
+    x.first_slot = (wa_known >= 0 ? f_wa : share_start(x.wa, B, W)) == fs ? 0 : 1;
+    x.two_level = x.wb - x.wa + 1 > kMergeFanIn;
+    if (!x.two_level) {
+        x.g0 = x.wa;
+        x.g1 = x.wb;
+        x.cnt = p.arrivals + x.wa;
+        x.total = nbs;
+    } else {
+        const int64_t j = (wme - x.wa) / kMergeFanIn;
+        x.g0 = x.wa + j * kMergeFanIn;
+        x.g1 = min(x.g0 + kMergeFanIn - 1, x.wb);
+        x.cnt = j == 0 ? p.arrivals + x.wa : p.arrivals + kCounterRegion + x.g0;
+        x.total = (int)blocks_in(B, W, fs, nbs, x.wb, x.g0, kMergeFanIn);
+    }
+    return x;
+}
+
+// Counts up to two pieces of a warp in at once (lane 0 the first, lane 1 the
+// second: one round trip for both); bit 0 / bit 1 of the result: that piece
+// completed its counter. Ordering as in arrive().
+__device__ __forceinline__ int arrive_pair(const Params& p, const CutPiece& a, bool has_a,
+                                           const CutPiece& b, bool has_b, int lane) {
+    __syncwarp();
+    int last = 0;
+    if ((lane == 0 && has_a) || (lane == 1 && has_b)) {
+        unsigned int* cnt = lane == 0 ? a.cnt : b.cnt;
+        const int add = lane == 0 ? a.pb : b.pb, total = lane == 0 ? a.total : b.total;
+        unsigned int old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                     : "=r"(old)
+                     : "l"(cnt), "r"((unsigned int)add)
+                     : "memory");
+        const unsigned int now = old + (unsigned int)add;
+        if (now > (unsigned int)total && p.err) atomicOr(p.err, pa::ERR_WORKSPACE);
+        last = now == (unsigned int)total;
+        if (last) atomicExch(cnt, 0u);   // no other piece counts here in this launch
+    }
+    const int la = __shfl_sync(0xffffffffu, last, 0), lb = __shfl_sync(0xffffffffu, last, 1);
+    __syncwarp();
+    return la | (lb << 1);
+}
+
+// After x completed its counter: merge the segment (one level), or fold the
+// group into its partial and, if that completes the segment's groups, merge
+// the group partials (stage: fold_stage_bytes(D) bytes of this warp's
+// shared memory, free).
+template <typename T, int D>
+__device__ __forceinline__ void merge_cut(const Params& p, int64_t B, const CutPiece& x,
+                                          uint32_t stage, int lane) {
+    const int64_t W = p.workers;
+    if (!x.two_level) {
+        fold_partials<T, D>(p, B, x.fs, x.nbs, x.wa, x.wb, x.first_slot, x.wa, x.wb, 1, x.rows,
+                            nullptr, x.s, x.g, x.c, x.q0, stage, lane);
+        return;
+    }
+    uint8_t* part =
+        p.slots + (2 * x.g0 + (x.g0 == x.wa ? x.first_slot : 0)) * (int64_t)p.slot_bytes;
+    fold_partials<T, D>(p, B, x.fs, x.nbs, x.wa, x.wb, x.first_slot, x.g0, x.g1, 1, x.rows, part,
+                        x.s, x.g, x.c, x.q0, stage, lane);
+    // groups that hold blocks (with more shares than blocks, whole groups can be empty)
+    const int64_t np = x.wb - x.wa + 1;
+    int groups = (int)((np + kMergeFanIn - 1) / kMergeFanIn);
+    if (B < W) {
+        groups = 0;
+        for (int64_t y = x.wa + (int64_t)lane * kMergeFanIn; y <= x.wb; y += 32 * kMergeFanIn)
+            groups += blocks_in(B, W, x.fs, x.nbs, x.wb, y, kMergeFanIn) > 0;
+        groups = __reduce_add_sync(0xffffffffu, groups);
+    }
+    if (arrive(p, p.arrivals + 2 * kCounterRegion + x.wa, 1, groups, lane))
+        fold_partials<T, D>(p, B, x.fs, x.nbs, x.wa, x.wb, x.first_slot, x.wa, x.wb, kMergeFanIn,
+                            x.rows, nullptr, x.s, x.g, x.c, x.q0, stage, lane);
 }
 
 // Merges the pieces of every cut segment: CTAs of kReduceWarps warps over

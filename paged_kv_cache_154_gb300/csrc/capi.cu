@@ -198,13 +198,14 @@ extern "C" size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_token
         num_heads % num_kv_heads != 0)
         return 0;
     if (partition_size == 0)
-        return (size_t)pa::balanced_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_q_len,
-                                          max_context_len)
-            .workspace_bytes;
+        return (size_t)(pa::kArrivalBytes + pa::balanced_shape(num_seqs, num_heads, num_kv_heads,
+                                                               head_dim, max_q_len, max_context_len)
+                                                .workspace_bytes);
     const int64_t parts = (max_context_len + (int64_t)partition_size - 1) / partition_size;
     if (parts <= 1) return 0;
     const size_t rows = (size_t)num_q_tokens * num_heads * parts;
-    return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float));
+    return (size_t)pa::kArrivalBytes + align256(rows * head_dim * sizeof(float)) +
+           2 * align256(rows * sizeof(float));
 }
 
 namespace pa {
@@ -355,11 +356,13 @@ extern "C" pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_
     a.max_context_len = max_context_len;
     a.partition_size = P;
     a.num_partitions = (int32_t)parts;
+    // the arrival counters first (kept zero), then this call's scratch
     if (P == 0) {
-        a.slots = workspace;
+        a.arrivals = static_cast<unsigned int*>(workspace);
+        a.slots = static_cast<char*>(workspace) + pa::kArrivalBytes;
     } else if (parts > 1) {
         const size_t rows = (size_t)num_q_tokens * num_heads * parts;
-        char* w = static_cast<char*>(workspace);
+        char* w = static_cast<char*>(workspace) + pa::kArrivalBytes;
         a.o_part = reinterpret_cast<float*>(w);
         a.m_part = reinterpret_cast<float*>(w + align256(rows * head_dim * sizeof(float)));
         a.l_part = reinterpret_cast<float*>(w + align256(rows * head_dim * sizeof(float)) +
@@ -368,6 +371,13 @@ extern "C" pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, pa_
     a.stream = st;
     return pa::launch_decode(a);
 }
+
+static_assert(PA_DEVERR_WAIT_FULL == pa::ERR_WAIT_FULL && PA_DEVERR_WAIT_EMPTY == pa::ERR_WAIT_EMPTY &&
+                  PA_DEVERR_WAIT_DRAIN == pa::ERR_WAIT_DRAIN &&
+                  PA_DEVERR_BAD_BLOCK == pa::ERR_BAD_BLOCK && PA_DEVERR_BAD_SLOT == pa::ERR_BAD_SLOT &&
+                  PA_DEVERR_BAD_GROUP == pa::ERR_BAD_GROUP &&
+                  PA_DEVERR_WORKSPACE == pa::ERR_WORKSPACE,
+              "device error bits of pa.h and the kernels agree");
 
 extern "C" pa_status pa_device_error(void* stream, uint32_t* code) {
     if (!code) return fail(PA_ERR_INVALID_ARG, "code is NULL");

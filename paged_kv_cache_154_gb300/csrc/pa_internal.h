@@ -27,6 +27,7 @@ enum : unsigned int {
     ERR_BAD_BLOCK = 1u << 3,    // a block-table entry outside the pool
     ERR_BAD_SLOT = 1u << 4,     // a slot outside the pool
     ERR_BAD_GROUP = 1u << 5,    // a shared-prefix group range or prefix length out of bounds
+    ERR_WORKSPACE = 1u << 6,    // a split-segment arrival counter was not zero at the start
 };
 
 inline int dtype_bytes(pa_dtype t) {
@@ -122,6 +123,9 @@ struct DecodeArgs {
     float* m_part;
     float* l_part;
     void* slots;             // balanced schedule (partition_size == 0)
+    unsigned int* arrivals;  // balanced schedule: 3 x kBalancedMaxWorkers counters, zero before the
+                             // call and left zero by it; null: merge cut segments in a
+                             // separate reduce kernel
     // balanced schedule of a 16-bit cache only (null / 0 otherwise):
     const int32_t* ctx_start;  // [num_seqs] first attended token, a multiple of 16
     float* lse_out;            // [num_q_tokens][num_heads] base-2 log-sum-exp per output row
@@ -157,6 +161,10 @@ pa_status validate_decode_arrays(const int32_t* block_tables, int32_t max_blocks
 // prefix sums live in shared memory).
 constexpr int kBalancedMaxWorkers = 2048;
 constexpr int kBalancedMaxSeqs = 8192;
+// The first bytes of every decode workspace: three regions of one arrival
+// counter per worker (see DecodeArgs::arrivals), at the same offset whatever
+// the call's shape so that one buffer can serve calls of different sizes.
+constexpr int64_t kArrivalBytes = 3 * 4 * kBalancedMaxWorkers;
 
 struct BalancedShape {
     int rows_per_tile;       // query rows per worker tile of this kernel family

@@ -327,7 +327,7 @@ struct BalancedLayout {
 };
 
 template <typename T, int D, int MT, int S>
-__global__ void __launch_bounds__(kWorkerWarps * 32)
+__global__ void __launch_bounds__(kWorkerWarps * 32, 3)
     paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                  const __grid_constant__ CUtensorMap tmap_v,
                                  const pa::sched::Params p) {
@@ -337,6 +337,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     constexpr int kKSteps = D / 16;
     constexpr int kNTiles = D / 8;
     constexpr int RT = 16 * MT;
+    static_assert(Lay::kRing >= fold_stage_bytes(D), "the merges stage partials in the ring");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = pa::smem_addr(smem_raw);
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     const int64_t f1 = share_start(wid + 1, B, p.workers);
     const int n = (int)(f1 - f0);
     if (lane == 0) write_merge_record(p, wid, 0, 0, 0);   // none unless set at the end
-    if (n <= 0) return;
+    if (wid >= p.workers || n <= 0) return;   // the grid's last CTA may have spare warps
 
     if (lane == 0) {
         for (int i = 0; i < S; ++i) pa::mbar_init(bars + 8 * i, 1);
@@ -402,6 +403,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
 
     // Consumer side: walk the share block by block, segment by segment.
     Pos cur = locate(p, cum, chunks, f0);
+    int64_t seg_f = f0 - cur.b;   // virtual index of the current segment's first block
     WarpAttn<T, D, MT> st;
     uint32_t qreg[MT == 1 ? kKSteps : 1][4];
     int L = 0, r = 1, q0 = 0, rows = 0, row_off = 0, seg_b0 = cur.b, sb = 0, last_q = 0;
@@ -507,23 +509,51 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         ++cur.b;
         const bool seg_done = cur.b == cur.nbs;
         if (seg_done || k == n - 1) {
-            finish_segment(seg_b0 == 0 && seg_done, seg_first ? 0 : 1,
-                           min((sb + cur.b) * kBS, L));
+            const bool whole = seg_b0 == 0 && seg_done;
+            finish_segment(whole, seg_first ? 0 : 1, min((sb + cur.b) * kBS, L));
             if (k == n - 1) {
-                if (lane == 0)
+                if (lane == 0 && !p.arrivals)
                     record_last_segment(p, wid, f1, B, seg_done, seg_b0,
                                         cur.nbs - cur.b, seg_first, q0, rows);
                 break;
             }
             next_segment(p, cur, cum, chunks);
+            seg_f = f0 + k + 1;
             seg_b0 = 0;
             seg_first = false;
             start_segment();
         }
     }
     // drain: no copy of this warp may still be in flight when it exits
+    bool drained = true;
     for (int k = consumed; k < issued; ++k)
-        if (!pa::mbar_wait(bars + 8 * (k % S), (k / S) & 1, p.err, pa::ERR_WAIT_DRAIN)) break;
+        if (!pa::mbar_wait(bars + 8 * (k % S), (k / S) & 1, p.err, pa::ERR_WAIT_DRAIN)) {
+            drained = false;
+            break;
+        }
+    // the cut segments' pieces of this share, merged by whichever piece is
+    // last (after the stream, where the accumulators are no longer live and
+    // the ring is free to stage partials in): the first segment if it began
+    // before the share and ended inside it (its position found again), and
+    // the last if the share did not hold it whole
+    if (p.arrivals && consumed == n && drained) {
+        const Pos h = locate(p, cum, chunks, f0);
+        const bool has_h = h.b > 0 && h.nbs - h.b < n;        // ends in this share: wb = wid
+        const bool has_t = !(seg_b0 == 0 && cur.b == cur.nbs);
+        CutPiece hp{}, tp{};
+        if (has_h) {
+            int hq0;
+            const int hr = query_run(p.qsl, h.s, &hq0);
+            hp = cut_piece(p, B, wid, f0 - h.b, h.nbs - h.b, h.nbs, h.s, h.g, h.c, hq0,
+                           min(RT, G * hr - h.c * RT), -1, 0, wid);
+        }
+        if (has_t)   // starts in this share (wa = wid) unless it began before it
+            tp = cut_piece(p, B, wid, seg_f, cur.b - seg_b0, cur.nbs, cur.s, cur.g, cur.c, q0,
+                           rows, seg_f >= f0 ? wid : -1, f0, -1);
+        const int done = arrive_pair(p, hp, has_h, tp, has_t, lane);
+        if (done & 1) merge_cut<T, D>(p, B, hp, ring, lane);
+        if (done & 2) merge_cut<T, D>(p, B, tp, ring, lane);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -582,7 +612,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
     const int64_t f1 = share_start(wid + 1, B, p.workers);
     const int n = (int)(f1 - f0);
     if (threadIdx.x == 0) write_merge_record(p, wid, 0, 0, 0);   // none unless set at the end
-    if (n <= 0) return;                                      // uniform over the CTA
+    if (wid >= p.workers || n <= 0) return;                  // uniform over the CTA
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -1158,6 +1188,7 @@ pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const 
             pa::launch_pdl(kern, dim3(grid), dim3(kWorkerWarps * 32), smem, a.stream, mk, mv, prm),
             "decode launch"))
         return s;
+    if (prm.arrivals) return PA_OK;   // cut segments merged by the decode kernel
     const int row_slots = (int)std::min<int64_t>(shape.rows_per_tile, (int64_t)(a.num_heads / a.num_kv_heads) *
                                                           a.max_q_len);
     return pa::cuda_status(pa::sched::launch_segment_reduce<T, D>(prm, (int)shape.max_chunks,
@@ -1189,6 +1220,7 @@ pa_status launch_rows(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUte
                                                        a.head_dim, a.max_q_len, a.max_context_len);
     const int64_t workers = std::min<int64_t>((int64_t)ctas * sms, shape.workers);
     prm.workers = (int)workers;
+    prm.arrivals = nullptr;   // this kernel leaves the merges to the reduce kernel
     if (pa_status s = pa::cuda_status(
             pa::launch_pdl(kern, dim3((unsigned)workers), dim3(kWorkerWarps * 32), smem, a.stream,
                            mk, mv, prm),
@@ -1298,6 +1330,7 @@ pa_status launch_decode(const DecodeArgs& a) {
     b.ctx_start = a.ctx_start;
     b.lse_out = a.lse_out;
     b.unmasked = a.unmasked;
+    b.arrivals = a.arrivals;
     if (a.kv_dtype == PA_BF16) return launch_dtype<__nv_bfloat16>(a, mt, mk, mv, prm, b);
     return launch_dtype<__half>(a, mt, mk, mv, prm, b);
 }

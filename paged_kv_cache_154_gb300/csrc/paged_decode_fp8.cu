@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     const int64_t f1 = share_start(wid + 1, B, p.workers);
     const int n = (int)(f1 - f0);
     if (lane == 0) write_merge_record(p, wid, 0, 0, 0);   // none unless set at the end
-    if (n <= 0) return;
+    if (wid >= p.workers || n <= 0) return;   // the grid's last CTA may have spare warps
 
     uint64_t pol_once = 0, pol_again = 0;
     if (lane == 0) {

@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
     const int64_t f1 = share_start(wid + 1, B, p.workers);
     const int n = (int)(f1 - f0);
     if (tid == 0) write_merge_record(p, wid, 0, 0, 0);   // none unless set at the end
-    if (n <= 0) return;                                // uniform over the CTA
+    if (wid >= p.workers || n <= 0) return;            // uniform over the CTA
 
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {

@@ -132,10 +132,11 @@ __global__ void __launch_bounds__(128)
     }
 }
 
-// Workspace: the two decode calls' own workspaces, the two phases' fp32 rows
-// and log-sum-exps, and the pseudo-sequence arrays.
+// Workspace: the arrival counters (kept zero; the two phases use them one
+// after the other), the two decode calls' own scratch, the two phases' fp32
+// rows and log-sum-exps, and the pseudo-sequence arrays.
 struct SpLayout {
-    size_t ws_a, ws_b, o_a, lse_a, o_b, lse_b, g_qsl, g_ctx, g_tables, ctx_start, total;
+    size_t arr, ws_a, ws_b, o_a, lse_a, o_b, lse_b, g_qsl, g_ctx, g_tables, ctx_start, total;
 };
 
 SpLayout sp_layout(int32_t num_seqs, int32_t num_q_tokens, int32_t num_heads,
@@ -154,6 +155,7 @@ SpLayout sp_layout(int32_t num_seqs, int32_t num_q_tokens, int32_t num_heads,
         at += align256(bytes);
         return here;
     };
+    l.arr = take((size_t)pa::kArrivalBytes);
     l.ws_a = take((size_t)sa.workspace_bytes);
     l.ws_b = take((size_t)sb.workspace_bytes);
     l.o_a = take(rows * head_dim * sizeof(float));
@@ -321,6 +323,7 @@ extern "C" pa_status pa_decode_shared_prefix(
     a.partition_size = 0;
     a.num_partitions = 1;
     a.slots = w + lay.ws_a;
+    a.arrivals = reinterpret_cast<unsigned int*>(w + lay.arr);
     a.lse_out = lse_a;
     a.unmasked = 1;
     a.stream = st;

@@ -161,7 +161,7 @@ class PagedKVCache:
                 group_start=torch.from_numpy(gs).to(dev), prefix_len=torch.from_numpy(pl).to(dev),
                 group_start_host=gs, prefix_len_host=pl, max_group_q_len=max(gq),
                 max_prefix_len=int(pl.max()),
-                workspace=torch.empty(sp_bytes, dtype=torch.uint8, device=dev))
+                workspace=torch.zeros(sp_bytes, dtype=torch.uint8, device=dev))
         return StepInputs(
             key=torch.cat(ks).to(dev), value=torch.cat(vs).to(dev),
             slots=torch.from_numpy(np.ascontiguousarray(slots)).to(dev),
@@ -172,7 +172,7 @@ class PagedKVCache:
             query_start_loc=torch.from_numpy(qsl).to(dev) if multi else None,
             max_q_len=max(q_lens), max_context_len=max(lens),
             out=torch.empty((nq, q.shape[1], q.shape[2]), dtype=out_dtype, device=dev),
-            workspace=(torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+            workspace=(torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
                        if ws_bytes else None),
             shared=shared)
 

@@ -139,22 +139,25 @@ def test_device_calls_reject_bad_arguments_on_the_host():
 
 
 def test_workspace_size():
+    # every workspace starts with 6144 uint32 arrival counters (24576 bytes)
+    arr = 24576
     # partitioned schedule: o, m, l per (q token, head, partition)
     assert pa.decode_workspace_size(64, 64, 32, 8, 128, 1, 512, 512) == 0
     n = pa.decode_workspace_size(4, 4, 32, 8, 128, 1, 131072, 512)
     rows = 4 * 32 * 256
-    assert n == rows * 128 * 4 + 2 * rows * 4
+    assert n == arr + rows * 128 * 4 + 2 * rows * 4
     # balanced schedule: prefix sums, then 2 slots per worker (workers capped at 2048);
     # a slot is a 32-byte header + m, l, O for a tile of 16 (or 64) query rows
     slot = 32 + 4 * 16 * (128 + 2)
-    assert pa.decode_workspace_size(64, 64, 32, 8, 128, 1, 4096, 0) == 512 + 2 * 2048 * slot
+    assert pa.decode_workspace_size(64, 64, 32, 8, 128, 1, 4096, 0) == \
+        arr + 512 + 2 * 2048 * slot
     slot64 = 32 + 4 * 16 * 66
-    assert pa.decode_workspace_size(1, 1, 8, 2, 64, 1, 17, 0) == 256 + 2 * (2 * 2) * slot64
+    assert pa.decode_workspace_size(1, 1, 8, 2, 64, 1, 17, 0) == arr + 256 + 2 * (2 * 2) * slot64
     # 32 q heads on one KV head with verify runs of 5 (160 rows): slots sized for the
     # 64-row tiles of the 16-bit kernels (the INT8 kernel's 32-row tiles fit in them)
     slot_big = 32 + 4 * 64 * 130
     assert pa.decode_workspace_size(256, 400, 32, 1, 128, 5, 16384, 0) == \
-        1280 + 2 * 2048 * slot_big
+        arr + 1280 + 2 * 2048 * slot_big
     assert pa.decode_workspace_size(1, 1, 8, 3, 64, 1, 17, 0) == 0      # heads not a multiple
 
 

@@ -13,6 +13,8 @@ import paged_kv_cache_154_gb300 as pa
 from gpu_harness import check_cache_bits, check_out, run_both, THREADS
 
 pytestmark = pytest.mark.gpu
+ARRIVAL_BYTES = 24576         # 6144 uint32 arrival counters at the start of every workspace
+DEVERR_WORKSPACE = 1 << 6     # a non-zero arrival counter seen by a decode kernel
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -72,7 +74,7 @@ def test_partials_match_oracle_partitions():
     check_out(ref, out, "bf16")
     nq, H, D = si.out.shape
     nparts = (si.max_context_len + P - 1) // P
-    ws = si.workspace
+    ws = si.workspace[ARRIVAL_BYTES:]                  # the partitions' layout follows the counters
     rows = nq * H * nparts
     o_bytes = ((rows * D * 4 + 255) // 256) * 256
     m_bytes = ((rows * 4 + 255) // 256) * 256
@@ -167,15 +169,16 @@ def test_empty_inputs_are_no_ops():
 
 def _written_slots(ws: torch.Tensor, wl, max_q_len: int):
     """Partial slots of the balanced schedule that the last call wrote (the
-    workspace was filled with 0xFF first, so unwritten headers read -1).
-    Layout: prefix sums (num_seqs + 1 int32, 256-byte aligned), then slots of
-    a 32-byte header {seq, kv head, chunk, first token, end token} and fp32
-    m[RT], l[RT], O[RT][d]."""
+    workspace past its arrival counters was filled with 0xFF first, so
+    unwritten headers read -1). Layout: 6144 uint32 arrival counters, prefix
+    sums (num_seqs + 1 int32, 256-byte aligned), then slots of a 32-byte
+    header {seq, kv head, chunk, first token, end token} and fp32 m[RT],
+    l[RT], O[RT][d]."""
     G = wl.num_heads // wl.num_kv_heads
     rt = 16 if G * max_q_len <= 16 else 64          # rows per tile of the 16-bit kernels
     slot_bytes = (32 + 4 * rt * (wl.head_dim + 2) + 15) // 16 * 16
     cum_bytes = (4 * (wl.num_seqs + 1) + 255) // 256 * 256
-    raw = ws.cpu().numpy()[cum_bytes:]
+    raw = ws.cpu().numpy()[ARRIVAL_BYTES + cum_bytes:]
     out = []
     for i in range(raw.size // slot_bytes):
         b = raw[i * slot_bytes:(i + 1) * slot_bytes]
@@ -211,10 +214,13 @@ def test_balanced_partials_match_oracle(case):
         cache.run_phase(ops, names)
     si = cache.prepare_step(wl.step, names, wl.q, torch.float32, 0)
     si.workspace.fill_(0xFF)
+    si.workspace[:ARRIVAL_BYTES].zero_()
     cache.step(si, wl.scale, 0)
     torch.cuda.synchronize()
     assert pa.device_error() == 0
     check_out(ref, si.out, "bf16")
+    # the decode kernel's merges leave every arrival counter at zero
+    assert not si.workspace[:ARRIVAL_BYTES].any()
     slots = _written_slots(si.workspace, wl, si.max_q_len)
     assert slots, "expected at least one cut segment"
     G = wl.num_heads // wl.num_kv_heads
@@ -234,6 +240,95 @@ def test_balanced_partials_match_oracle(case):
             np.testing.assert_allclose(m[j], mm[qi, h] * np.log2(np.e), rtol=1e-5, atol=1e-4)
             np.testing.assert_allclose(l[j], lm[qi, h], rtol=1e-4)
             np.testing.assert_allclose(o[j] / l[j], om[qi, h], rtol=0, atol=2e-3)
+
+
+def _balanced_state(name, lens, qlens, H, Hkv, d, seed):
+    from paged_kv_cache_154_gb300.engine import PagedKVCache
+    wl = W.simple(name, seed, lens, qlens, H, Hkv, d, "bf16")
+    cache = PagedKVCache(wl.num_blocks, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
+                         free_order=wl.free_order)
+    names = {}
+    for ops in wl.phases:
+        cache.run_phase(ops, names)
+    si = cache.prepare_step(wl.step, names, wl.q, torch.float32, 0)
+    cache.write_step(si)
+    return wl, cache, si
+
+
+def test_one_workspace_serves_calls_of_any_shape():
+    """One buffer, zeroed once, serves a run of calls of different shapes:
+    the arrival counters sit at its start whatever the shape, and every call
+    (the decode kernel that merges its own cut segments, or the 64-row
+    kernel with the reduce kernel) leaves them at zero; the rest of the
+    buffer starts as stale bytes."""
+    cases = [("ws_one_long", [20000], [1], 8, 1, 128),
+             ("ws_many_short", [1, 2, 3, 17, 31, 33, 5, 64, 100, 7] * 6, [1] * 60, 16, 4, 128),
+             ("ws_verify_rows", [3000, 777, 4100], [4, 1, 3], 32, 4, 128),
+             ("ws_d64_mha", [900, 17, 4000], [1, 1, 1], 4, 4, 64)]
+    states = [_balanced_state(*c, seed=500 + i) for i, c in enumerate(cases)]
+    refs = [oracle.run(wl, threads=THREADS) for wl, _, _ in states]
+    big = torch.zeros(max(si.workspace.numel() for _, _, si in states), dtype=torch.uint8,
+                      device="cuda")
+    big[ARRIVAL_BYTES:].fill_(0x5A)
+    for _ in range(2):
+        for (wl, cache, si), ref in zip(states, refs):
+            si.out.fill_(float("nan"))
+            pa.decode(si.out, si.q, cache.k, cache.v, si.block_tables, si.context_lens,
+                      si.max_context_len, wl.scale, si.query_start_loc, si.max_q_len,
+                      cache.num_blocks, workspace=big)
+            torch.cuda.synchronize()
+            assert pa.device_error() == 0
+            check_out(ref, si.out, "bf16")
+            assert not big[:ARRIVAL_BYTES].any()
+
+
+def test_nonzero_arrival_counters_are_reported():
+    """Counters that were not zeroed are reported in the device error word
+    (no fault, no hang); zeroed again, the next call is correct."""
+    wl, cache, si = _balanced_state("ws_dirty", [20000, 3000], [1, 1], 8, 1, 128, seed=510)
+    ref = oracle.run(wl, threads=THREADS)
+    args = (si.q, cache.k, cache.v, si.block_tables, si.context_lens, si.max_context_len,
+            wl.scale, si.query_start_loc, si.max_q_len, cache.num_blocks)
+    si.workspace[:ARRIVAL_BYTES].fill_(0x40)       # every counter 0x40404040: past any segment
+    pa.decode(si.out, *args, workspace=si.workspace)
+    torch.cuda.synchronize()
+    assert pa.device_error() & DEVERR_WORKSPACE
+    si.workspace[:ARRIVAL_BYTES].zero_()
+    si.out.fill_(float("nan"))
+    pa.decode(si.out, *args, workspace=si.workspace)
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+    check_out(ref, si.out, "bf16")
+    assert not si.workspace[:ARRIVAL_BYTES].any()
+
+
+@pytest.mark.parametrize("case", [
+    ("spare_warps_mqa", [20000], [1], 8, 1, 128),        # 1250 workers: 2 spare warps
+    ("spare_warps_d64", [1000, 77], [1, 1], 4, 1, 64),   # 2 x 63 = 126 workers, 68 blocks
+])
+def test_writes_stay_inside_workspace_and_output(case):
+    """Calls whose worker count is not a multiple of the CTA's four warps
+    (the grid's last CTA has spare warps): nothing is written past the
+    workspace the size query asked for, nor past the output, and the output
+    matches the oracle."""
+    name, lens, qlens, H, Hkv, d = case
+    wl, cache, si = _balanced_state(name, lens, qlens, H, Hkv, d, seed=520)
+    ref = oracle.run(wl, threads=THREADS)
+    need = si.workspace.numel()
+    guard = 1 << 16
+    ws = torch.full((need + guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    ws[:ARRIVAL_BYTES].zero_()
+    nq = si.out.shape[0]
+    out = torch.full((nq + 4,) + tuple(si.out.shape[1:]), float("nan"), device="cuda")
+    pa.decode(out[:nq], si.q, cache.k, cache.v, si.block_tables, si.context_lens,
+              si.max_context_len, wl.scale, si.query_start_loc, si.max_q_len, cache.num_blocks,
+              workspace=ws[:need])
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+    check_out(ref, out[:nq], "bf16")
+    assert bool((ws[need:] == 0xA5).all()), "bytes written past the workspace"
+    assert bool(out[nq:].isnan().all()), "rows written past the output"
+    assert not ws[:ARRIVAL_BYTES].any()
 
 
 def test_many_query_rows_per_kv_head_use_row_chunks():

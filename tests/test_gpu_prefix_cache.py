@@ -65,7 +65,7 @@ def test_second_request_reuses_the_system_prompt_blocks():
     bt, cl = cache.pool.block_tables([b], (L + 15) // 16)
     q = torch.randn(1, H, D, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
     out = torch.empty(1, H, D, dtype=torch.float32, device="cuda")
-    ws = torch.empty(pa.decode_workspace_size(1, 1, H, HKV, D, 1, L), dtype=torch.uint8,
+    ws = torch.zeros(pa.decode_workspace_size(1, 1, H, HKV, D, 1, L), dtype=torch.uint8,
                      device="cuda")
     pa.decode(out, q.cuda(), cache.k, cache.v, torch.from_numpy(bt).cuda(),
               torch.from_numpy(cl).cuda(), L, 1.0 / np.sqrt(D), num_blocks=cache.num_blocks,

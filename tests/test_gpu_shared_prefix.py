@@ -97,7 +97,7 @@ def test_raw_api_prefix_covering_a_whole_sequence():
     pl = np.array([64, 0], np.int32)
     dev = "cuda"
     out = torch.empty(3, wl.num_heads, wl.head_dim, dtype=torch.float32, device=dev)
-    ws = torch.empty(pa.decode_shared_prefix_workspace_size(3, 3, wl.num_heads, wl.num_kv_heads,
+    ws = torch.zeros(pa.decode_shared_prefix_workspace_size(3, 3, wl.num_heads, wl.num_kv_heads,
                                                             wl.head_dim, 1, 100, 2, 2, 64,
                                                             bt.shape[1]),
                      dtype=torch.uint8, device=dev)
@@ -119,7 +119,7 @@ def test_validate_mode_rejects_inconsistent_groups(monkeypatch):
     bt = si.block_tables
     cl = si.context_lens
     out = torch.empty_like(si.out)
-    ws = torch.empty(pa.decode_shared_prefix_workspace_size(4, 4, wl.num_heads, wl.num_kv_heads,
+    ws = torch.zeros(pa.decode_shared_prefix_workspace_size(4, 4, wl.num_heads, wl.num_kv_heads,
                                                             wl.head_dim, 1, 100, 4, 4, 96,
                                                             bt.shape[1]),
                      dtype=torch.uint8, device=dev)
