@@ -234,18 +234,51 @@ def unique_kv_bytes(wl, group_start, prefix_len):
     return toks * per_tok
 
 
-def launches_per_step(si, partition_size, prefill_tc=False):
+def launches_per_step(si, partition_size, prefill_tc=False, kv_dtype="bf16", group=1):
+    """Kernels of one step. A balanced decode over a 16-bit cache with at most
+    16 query rows per KV head merges its cut segments itself; every other
+    balanced decode launches the segment reduce after it."""
+    def decode_launches(rows, balanced=True, long_enough=True):
+        if not balanced:
+            return 1 + (1 if long_enough else 0)        # decode (+ partition reduce)
+        fused = kv_dtype in ("f16", "bf16") and rows <= 16
+        return 1 if fused else 2                        # decode (+ segment reduce)
+
     n = 1                                               # append
     if si.pairs is not None:
         n += 1                                          # copy_blocks
     if si.shared is not None:
-        return n + 6                                    # prep, 2 x (decode + reduce), merge
+        # prep, the prefix phase, the suffix phase, the merge of the two
+        return (n + 2 + decode_launches(group * si.shared.max_group_q_len)
+                + decode_launches(group * si.max_q_len))
     if prefill_tc:
         return n + 2                                    # task order, tensor-core prefill
-    n += 1                                              # decode
-    if partition_size == 0 or si.max_context_len > partition_size:
-        n += 1                                          # partial-result reduce
-    return n
+    return n + decode_launches(group * si.max_q_len, partition_size == 0,
+                               si.max_context_len > partition_size)
+
+
+def roofline_kernel(wl, si, partition_size, prefill_tc):
+    """The kernels the timed attention call launches."""
+    G = wl.num_heads // wl.num_kv_heads
+
+    def balanced16(rows):
+        return ("paged_decode_balanced_kernel (cut segments merged in-kernel)" if rows <= 16
+                else "paged_decode_rows_kernel + segment_reduce_kernel")
+
+    if prefill_tc:
+        return ("pa_decode (paged_prefill_tc_kernel: Q K^T and P V on the tcgen05 tensor "
+                "cores, accumulators in TMEM)")
+    if si.shared is not None:
+        return (f"pa_decode_shared_prefix (prefix_prep_kernel, "
+                f"{balanced16(G * si.shared.max_group_q_len)} for the prefixes, "
+                f"{balanced16(G * si.max_q_len)} for the suffixes, prefix_merge_kernel)")
+    if wl.kv_dtype == "int8":
+        return "pa_decode (paged_decode_int8_kernel + segment_reduce_kernel)"
+    if wl.kv_dtype == "fp8":
+        return "pa_decode (paged_decode_fp8_kernel + segment_reduce_kernel)"
+    if partition_size == 0:
+        return f"pa_decode ({balanced16(G * si.max_q_len)})"
+    return "pa_decode (paged_decode_kernel + split_kv_reduce_kernel)"
 
 
 def run_ours(args, rank, world, local):
@@ -374,20 +407,7 @@ def run_ours(args, rank, world, local):
                                    if world > 1 else "1 GPU")},
         "seq_steps_per_s": round(seq_steps, 1),
         "pct_of_hbm_peak": round(100 * value / hbm_peak, 2),
-        "roofline": {"kernel": ("pa_decode (paged_prefill_tc_kernel: Q K^T and P V on the "
-                                "tcgen05 tensor cores, accumulators in TMEM)"
-                                if prefill_tc else
-                                "pa_decode_shared_prefix (prefix_prep_kernel, "
-                                "paged_decode_balanced_kernel + segment_reduce_kernel for the "
-                                "prefixes and for the suffixes, prefix_merge_kernel)"
-                                if si.shared is not None else
-                                "pa_decode (paged_decode_int8_kernel + segment_reduce_kernel)"
-                                if wl.kv_dtype == "int8" else
-                                "pa_decode (paged_decode_fp8_kernel + segment_reduce_kernel)"
-                                if wl.kv_dtype == "fp8" else
-                                "pa_decode (paged_decode_balanced_kernel + segment_reduce_kernel)"
-                                if args.partition_size == 0 else
-                                "pa_decode (paged_decode_kernel + split_kv_reduce_kernel)"),
+        "roofline": {"kernel": roofline_kernel(wl, si, args.partition_size, prefill_tc),
                      "bound": bound, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": roof_unit,
                      "frac": round(achieved / peak, 4),
@@ -400,7 +420,8 @@ def run_ours(args, rank, world, local):
                      "decode_ms_avg": round(dec_avg_s * 1e3, 5),
                      "decode_ms_p50": round(statistics.median(dec_ms), 5)},
         "e2e": e2e,
-        "gpu_launches": launches_per_step(si, args.partition_size, prefill_tc) * K,
+        "gpu_launches": launches_per_step(si, args.partition_size, prefill_tc, wl.kv_dtype,
+                                          wl.num_heads // wl.num_kv_heads) * K,
         "clocks": sampler.summary(),
         "wall_s_timed": round(wall1 - wall0, 3),
     }
