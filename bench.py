@@ -119,16 +119,19 @@ def kernel_digest(family: str = "16bit"):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(family: str = "16bit"):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+def recorded_traffic(family: str = "16bit", workload: str = ""):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source and on this workload; else None."""
     try:
         text = open(os.path.join(ROOT, "profiles", PROFILES[family][0])).read()
     except OSError:
         return None
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
     if not m_sha or not m_b or m_sha.group(1) != kernel_digest(family):
+        return None
+    if not m_w or m_w.group(1) != workload:
         return None
     return float(m_b.group(1))
 
@@ -411,8 +414,8 @@ def run_ours(args, rank, world, local):
                      "bound": bound, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": roof_unit,
                      "frac": round(achieved / peak, 4),
-                     "traffic": (recorded_traffic("prefill") if prefill_tc else
-                                 recorded_traffic(kernel_family(wl.kv_dtype))
+                     "traffic": (recorded_traffic("prefill", args.workload) if prefill_tc else
+                                 recorded_traffic(kernel_family(wl.kv_dtype), args.workload)
                                  if args.partition_size == 0 and si.shared is None
                                  and not is_prefill(wl) else None),
                      ("algorithmic_flops_per_launch" if bound == "tensor"

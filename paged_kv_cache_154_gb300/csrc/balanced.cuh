@@ -139,6 +139,13 @@ __host__ __device__ __forceinline__ int64_t share_start(int64_t w, int64_t B, in
     return w * B / W;
 }
 
+// Shares the B virtual blocks are cut into: one per worker, but never more
+// than there are blocks, so that every share holds at least one block
+// (workers past the count get no share).
+__device__ __forceinline__ int64_t share_count(const Params& p, int64_t B) {
+    return max((int64_t)1, min((int64_t)p.workers, B));
+}
+
 // Shared-memory header of a balanced kernel: per-warp mbarriers, then
 // cum[num_seqs + 1] (virtual blocks before each sequence) and chunks[num_seqs].
 __host__ __device__ __forceinline__ int header_bytes(int num_seqs, int stages) {
@@ -298,7 +305,8 @@ __device__ __forceinline__ void record_last_segment(const Params& p, int64_t wid
                                                     int rows) {
     if (!seg_done && seg_b0 == 0) {
         const int64_t fb = f1 + blocks_left;                 // one past the segment's end
-        write_merge_record(p, wid, 1, (fb * p.workers - 1) / B, seg_first ? 0 : 1, q0, rows);
+        write_merge_record(p, wid, 1, (fb * share_count(p, B) - 1) / B, seg_first ? 0 : 1, q0,
+                           rows);
     }
 }
 
@@ -385,7 +393,7 @@ __device__ __forceinline__ void fold_partials(const Params& p, int64_t B, int64_
     constexpr int EPL = D / 8;
     constexpr int kRowBytes = D * 4;
     constexpr int kPerLane = 4 * kRowBytes / 16 / 32;   // 16-byte chunks a lane copies per partial
-    const int64_t W = p.workers;
+    const int64_t W = share_count(p, B);
     const int RT = p.rows_per_tile, G = p.group;
     const int cp = lane & 7;
     // with at least as many blocks as shares every share holds one: no
@@ -514,7 +522,7 @@ __device__ __forceinline__ CutPiece cut_piece(const Params& p, int64_t B, int64_
                                               int pb, int nbs, int s, int g, int c, int q0,
                                               int rows, int64_t wa_known, int64_t f_wa,
                                               int64_t wb_known) {
-    const int64_t W = p.workers;
+    const int64_t W = share_count(p, B);
     CutPiece x;
     x.fs = fs;
     x.pb = pb;
@@ -575,7 +583,7 @@ __device__ __forceinline__ int arrive_pair(const Params& p, const CutPiece& a, b
 template <typename T, int D>
 __device__ __forceinline__ void merge_cut(const Params& p, int64_t B, const CutPiece& x,
                                           uint32_t stage, int lane) {
-    const int64_t W = p.workers;
+    const int64_t W = share_count(p, B);
     if (!x.two_level) {
         fold_partials<T, D>(p, B, x.fs, x.nbs, x.wa, x.wb, x.first_slot, x.wa, x.wb, 1, x.rows,
                             nullptr, x.s, x.g, x.c, x.q0, stage, lane);
@@ -638,8 +646,8 @@ __global__ void __launch_bounds__(32 * kReduceWarps, 32 / kReduceWarps) segment_
     if (row0 >= rows_all) return;
     const int rows = min(kReduceWarps, rows_all - row0);
     const int RT = p.rows_per_tile, G = p.group;
-    const int64_t W = p.workers;
     const int64_t B = hdr[16];
+    const int64_t W = share_count(p, B);
     const bool may_be_empty = B < W;                 // only then can a share hold no block
     // warps per row: the largest power of two with wpr x rows <= kReduceWarps (one round)
     int wpr = 1;
@@ -776,7 +784,7 @@ __global__ void __launch_bounds__(128) segment_reduce_rows_kernel(const Params p
     const int nbs = chunk_blocks(p, L, r, sb, c);
     if (nbs == 0) return;                          // nothing attended: no output row
     const int64_t B = __ldg(p.cum_out + p.num_seqs);
-    const int64_t W = p.workers;
+    const int64_t W = share_count(p, B);
     int before = 0;                                // blocks of the chunks before c
     for (int cc = 0; cc < c; ++cc) before += chunk_blocks(p, L, r, sb, cc);
     const int span = (__ldg(p.cum_out + s + 1) - __ldg(p.cum_out + s)) / p.num_kv_heads;

@@ -120,11 +120,12 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
     build_prefix(cum, chunks, p);
     const int64_t B = cum[n_seqs];
     const int64_t wid = (int64_t)blockIdx.x * kWorkerWarps + warp;
-    const int64_t f0 = share_start(wid, B, p.workers);
-    const int64_t f1 = share_start(wid + 1, B, p.workers);
+    const int64_t W = share_count(p, B);
+    const int64_t f0 = share_start(wid, B, W);
+    const int64_t f1 = share_start(wid + 1, B, W);
     const int n = (int)(f1 - f0);
     if (lane == 0) write_merge_record(p, wid, 0, 0, 0);   // none unless set at the end
-    if (wid >= p.workers || n <= 0) return;   // the grid's last CTA may have spare warps
+    if (wid >= W || n <= 0) return;   // the grid's last CTA may have spare warps
 
     uint64_t pol_once = 0, pol_again = 0;
     if (lane == 0) {
