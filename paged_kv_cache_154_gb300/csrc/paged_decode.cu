@@ -1185,6 +1185,11 @@ pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const 
                                                        a.head_dim, a.max_q_len, a.max_context_len);
     const int64_t workers = std::min<int64_t>((int64_t)ctas * sms * kWorkerWarps, shape.workers);
     prm.workers = (int)workers;
+    // The in-kernel merge pays off when shares are long. When a call can
+    // hold fewer than 8 blocks per worker (a small call), the merges'
+    // round trips at the end of each short stream cost more than the
+    // reduce kernel.
+    if (shape.virtual_blocks < 8 * workers) prm.arrivals = nullptr;
     const int grid = (int)((workers + kWorkerWarps - 1) / kWorkerWarps);
     if (pa_status s = pa::cuda_status(
             pa::launch_pdl(kern, dim3(grid), dim3(kWorkerWarps * 32), smem, a.stream, mk, mv, prm),

@@ -338,6 +338,9 @@ extern "C" pa_status pa_decode_shared_prefix(
     a.max_q_len = max_q_len;
     a.max_context_len = max_context_len;
     a.slots = w + lay.ws_b;
+    // the private suffixes are short (a few blocks per share), where the
+    // reduce kernel merges faster than the decode kernel's tail
+    a.arrivals = nullptr;
     a.ctx_start = ctx_start;
     a.lse_out = lse_b;
     a.unmasked = 0;

@@ -198,6 +198,9 @@ def _written_slots(ws: torch.Tensor, wl, max_q_len: int):
     ("one_long", [20000], [1], 8, 1, 128),
     # verify runs and GQA 8: 32 rows, one 64-row tile served by two of the CTA's warps
     ("verify_long", [3000, 777, 4100], [4, 1, 3], 32, 4, 128),
+    # long GQA sequences: merged inside the decode kernel, the longest cut by
+    # far more than eight shares (two-level merge, group partials in slots)
+    ("gqa_long_in_kernel", [12000, 5000, 2000], [1, 1, 1], 32, 8, 128),
     # 96 query rows per KV head: two row chunks per (sequence, kv head)
     ("chunked_rows", [2500, 900], [3, 1], 32, 1, 128),
 ])
@@ -258,13 +261,14 @@ def _balanced_state(name, lens, qlens, H, Hkv, d, seed):
 def test_one_workspace_serves_calls_of_any_shape():
     """One buffer, zeroed once, serves a run of calls of different shapes:
     the arrival counters sit at its start whatever the shape, and every call
-    (the decode kernel that merges its own cut segments, or the 64-row
-    kernel with the reduce kernel) leaves them at zero; the rest of the
+    leaves them at zero, whether the decode kernel merged its own cut
+    segments (the two long GQA calls: one- and two-level merges) or the
+    reduce kernel did (a small call, the 64-row kernel). The rest of the
     buffer starts as stale bytes."""
-    cases = [("ws_one_long", [20000], [1], 8, 1, 128),
+    cases = [("ws_gqa_long", [12000, 5000, 2000], [1, 1, 1], 32, 8, 128),
              ("ws_many_short", [1, 2, 3, 17, 31, 33, 5, 64, 100, 7] * 6, [1] * 60, 16, 4, 128),
              ("ws_verify_rows", [3000, 777, 4100], [4, 1, 3], 32, 4, 128),
-             ("ws_d64_mha", [900, 17, 4000], [1, 1, 1], 4, 4, 64)]
+             ("ws_d64_in_kernel", [9000, 6000], [1, 1], 16, 8, 64)]
     states = [_balanced_state(*c, seed=500 + i) for i, c in enumerate(cases)]
     refs = [oracle.run(wl, threads=THREADS) for wl, _, _ in states]
     big = torch.zeros(max(si.workspace.numel() for _, _, si in states), dtype=torch.uint8,
@@ -285,7 +289,9 @@ def test_one_workspace_serves_calls_of_any_shape():
 def test_nonzero_arrival_counters_are_reported():
     """Counters that were not zeroed are reported in the device error word
     (no fault, no hang); zeroed again, the next call is correct."""
-    wl, cache, si = _balanced_state("ws_dirty", [20000, 3000], [1, 1], 8, 1, 128, seed=510)
+    # long GQA sequences: the decode kernel merges (and counts) itself
+    wl, cache, si = _balanced_state("ws_dirty", [12000, 3000, 3000], [1, 1, 1], 32, 8, 128,
+                                    seed=510)
     ref = oracle.run(wl, threads=THREADS)
     args = (si.q, cache.k, cache.v, si.block_tables, si.context_lens, si.max_context_len,
             wl.scale, si.query_start_loc, si.max_q_len, cache.num_blocks)
