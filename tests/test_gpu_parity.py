@@ -268,7 +268,7 @@ def test_one_workspace_serves_calls_of_any_shape():
     cases = [("ws_gqa_long", [12000, 5000, 2000], [1, 1, 1], 32, 8, 128),
              ("ws_many_short", [1, 2, 3, 17, 31, 33, 5, 64, 100, 7] * 6, [1] * 60, 16, 4, 128),
              ("ws_verify_rows", [3000, 777, 4100], [4, 1, 3], 32, 4, 128),
-             ("ws_d64_in_kernel", [9000, 6000], [1, 1], 16, 8, 64)]
+             ("ws_d64_in_kernel", [9000, 6000, 3000, 2000], [1, 1, 1, 1], 16, 8, 64)]
     states = [_balanced_state(*c, seed=500 + i) for i, c in enumerate(cases)]
     refs = [oracle.run(wl, threads=THREADS) for wl, _, _ in states]
     big = torch.zeros(max(si.workspace.numel() for _, _, si in states), dtype=torch.uint8,
