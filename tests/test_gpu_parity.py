@@ -228,15 +228,20 @@ def test_balanced_partials_match_oracle(case):
     assert slots, "expected at least one cut segment"
     G = wl.num_heads // wl.num_kv_heads
     qsl = wl.query_start_loc
+    per_range = {}    # the oracle over one sequence's keys [t0, t1), all heads
     for (s, g, c, t0, t1), rt, m, l, o in slots:
         L = wl.context_lens[s]
         assert 0 <= t0 < t1 <= L and t0 % 16 == 0
-        om, mm, lm = oracle.attend(ref.q64, ref.cache, ref.block_tables, ref.context_lens, qsl,
-                                   wl.num_heads, wl.scale, t0, t1)
-        r = qsl[s + 1] - qsl[s]
+        q0, q1 = int(qsl[s]), int(qsl[s + 1])
+        if (s, t0, t1) not in per_range:
+            per_range[(s, t0, t1)] = oracle.attend(
+                ref.q64[q0:q1], ref.cache, ref.block_tables[s:s + 1], ref.context_lens[s:s + 1],
+                np.array([0, q1 - q0], np.int32), wl.num_heads, wl.scale, t0, t1)
+        om, mm, lm = per_range[(s, t0, t1)]
+        r = q1 - q0
         for j in range(min(rt, G * r - c * rt)):
             row = c * rt + j
-            qi, h = qsl[s] + row // G, g * G + row % G
+            qi, h = row // G, g * G + row % G
             if lm[qi, h] == 0:
                 assert l[j] == 0 and np.isneginf(m[j])
                 continue
