@@ -341,8 +341,19 @@ def decode_no_alloc(out, q, k_cache, v_cache, block_tables, context_lens, max_co
         int(partition_size), _stream(stream)))
 
 
+# Bits of the device error word (PA_DEVERR_* in pa.h).
+DEVERR_WAIT_FULL = 1 << 0      # a consumer gave up waiting for a staged tile
+DEVERR_WAIT_EMPTY = 1 << 1     # a producer gave up waiting for a free stage
+DEVERR_WAIT_DRAIN = 1 << 2     # the exit drain gave up on an in-flight copy
+DEVERR_BAD_BLOCK = 1 << 3      # a block-table entry outside the pool
+DEVERR_BAD_SLOT = 1 << 4       # a slot_mapping entry outside the pool
+DEVERR_BAD_GROUP = 1 << 5      # a shared-prefix group range or prefix length
+DEVERR_WORKSPACE = 1 << 6      # a workspace arrival counter was not zero
+
+
 def device_error(stream=None) -> int:
-    """pa_device_error: read and clear the device error word (synchronises)."""
+    """pa_device_error: read and clear the device error word (synchronises);
+    the value is a mask of the DEVERR_* bits."""
     code = ctypes.c_uint32()
     st = lib().pa_device_error(_stream(stream), ctypes.addressof(code))
     if st not in (0, 7):

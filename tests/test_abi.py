@@ -35,6 +35,16 @@ def test_every_declared_symbol_is_exported():
     assert "sm_103a" in pa.version()
 
 
+def test_device_error_bits_match_the_header():
+    """The binding's DEVERR_* constants are the header's PA_DEVERR_* bits."""
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "pa.h")).read()
+    bits = {m.group(1): 1 << int(m.group(2)) for m in
+            re.finditer(r"#define PA_DEVERR_(\w+)\s+\(1u << (\d+)\)", hdr)}
+    assert len(bits) == 7 and len(set(bits.values())) == 7
+    for name, value in bits.items():
+        assert getattr(pa, "DEVERR_" + name) == value, name
+
+
 def test_pool_matches_oracle_model_on_random_ops():
     rng = np.random.default_rng(3)
     order = rng.permutation(300).astype(np.int32)

@@ -1,0 +1,71 @@
+"""Host-side logic of bench.py (no GPU): the kernels a step launches, the
+kernel the roofline names, and the rule that a profile's recorded DRAM
+traffic is reported only for the workload and kernel source it was captured
+on."""
+import os
+import sys
+from types import SimpleNamespace
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _si(max_q_len=1, max_context_len=4096, pairs=None, shared=None):
+    return SimpleNamespace(max_q_len=max_q_len, max_context_len=max_context_len, pairs=pairs,
+                           shared=shared)
+
+
+def _wl(kv="bf16", H=32, Hkv=8):
+    return SimpleNamespace(kv_dtype=kv, num_heads=H, num_kv_heads=Hkv)
+
+
+@pytest.mark.parametrize("kv, group, qlen, expect", [
+    ("bf16", 4, 1, 2),      # append + decode that merges its own cut segments
+    ("f16", 8, 2, 2),       # 16 rows per KV head: still the per-warp kernel
+    ("bf16", 8, 3, 3),      # 24 rows: 64-row kernel + segment reduce
+    ("int8", 4, 1, 3),      # INT8 decode + segment reduce
+    ("fp8", 4, 1, 3),       # FP8 decode + segment reduce
+])
+def test_launches_per_balanced_step(kv, group, qlen, expect):
+    assert bench.launches_per_step(_si(max_q_len=qlen), 0, False, kv, group) == expect
+
+
+def test_launches_with_copies_partitions_prefill_and_shared_prefix():
+    si = _si(pairs=object())
+    assert bench.launches_per_step(si, 0, False, "bf16", 4) == 3              # + copy_blocks
+    assert bench.launches_per_step(_si(max_context_len=4096), 512, False, "bf16", 4) == 3
+    assert bench.launches_per_step(_si(max_context_len=400), 512, False, "bf16", 4) == 2
+    assert bench.launches_per_step(_si(), 0, True, "bf16", 4) == 3            # order + prefill
+    # best-of-5 shape: 5 forks x 8 q heads per KV head in the prefix phase
+    # (64-row kernel + reduce), 8 rows in the suffix phase
+    sp = SimpleNamespace(max_group_q_len=5)
+    assert bench.launches_per_step(_si(shared=sp), 0, False, "bf16", 8) == 1 + 2 + 2 + 1
+
+
+def test_roofline_kernel_names_what_runs():
+    assert "in-kernel" in bench.roofline_kernel(_wl(), _si(), 0, False)
+    assert "rows_kernel + segment_reduce" in bench.roofline_kernel(_wl(), _si(max_q_len=5), 0,
+                                                                   False)
+    assert "int8" in bench.roofline_kernel(_wl("int8"), _si(), 0, False)
+    assert "fp8" in bench.roofline_kernel(_wl("fp8"), _si(), 0, False)
+    assert "split_kv_reduce" in bench.roofline_kernel(_wl(), _si(), 512, False)
+    assert "tcgen05" in bench.roofline_kernel(_wl(), _si(), 0, True)
+
+
+def test_recorded_traffic_only_for_the_profiled_workload():
+    import re
+    for family, workload in (("16bit", "llama3_8b"), ("int8", "mixed_int8"),
+                             ("fp8", "llama3_8b_fp8"), ("prefill", "paged_prefill")):
+        text = open(os.path.join(ROOT, "profiles", bench.PROFILES[family][0])).read()
+        assert re.search(r"^workload:\s*" + workload + r"\s*$", text, re.M), family
+        fresh = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text).group(1) == \
+            bench.kernel_digest(family)
+        t = bench.recorded_traffic(family, workload)
+        # reported exactly when the summary was taken on the current source
+        assert (t is not None and t > 0) == fresh, (family, workload)
+        assert bench.recorded_traffic(family, "tiny") is None
+        assert bench.recorded_traffic(family, "long_context") is None

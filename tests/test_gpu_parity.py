@@ -14,7 +14,6 @@ from gpu_harness import check_cache_bits, check_out, run_both, THREADS
 
 pytestmark = pytest.mark.gpu
 ARRIVAL_BYTES = 24576         # 6144 uint32 arrival counters at the start of every workspace
-DEVERR_WORKSPACE = 1 << 6     # a non-zero arrival counter seen by a decode kernel
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -131,7 +130,7 @@ def test_bad_block_id_is_reported_not_faulted():
     bt[1, 2] = wl.num_blocks + 1000               # outside the pool
     pa.decode(si.out, si.q, cache.k, cache.v, bt, si.context_lens, si.max_context_len,
               wl.scale, num_blocks=cache.num_blocks, workspace=si.workspace)
-    assert pa.device_error() & (1 << 3)            # ERR_BAD_BLOCK, no fault
+    assert pa.device_error() & pa.DEVERR_BAD_BLOCK      # reported, no fault
     assert pa.device_error() == 0                  # the word was cleared
 
 
@@ -303,7 +302,7 @@ def test_nonzero_arrival_counters_are_reported():
     si.workspace[:ARRIVAL_BYTES].fill_(0x40)       # every counter 0x40404040: past any segment
     pa.decode(si.out, *args, workspace=si.workspace)
     torch.cuda.synchronize()
-    assert pa.device_error() & DEVERR_WORKSPACE
+    assert pa.device_error() & pa.DEVERR_WORKSPACE
     si.workspace[:ARRIVAL_BYTES].zero_()
     si.out.fill_(float("nan"))
     pa.decode(si.out, *args, workspace=si.workspace)
