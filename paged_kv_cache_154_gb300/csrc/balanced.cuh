@@ -142,7 +142,7 @@ __host__ __device__ __forceinline__ int64_t share_start(int64_t w, int64_t B, in
 // Shares the B virtual blocks are cut into: one per worker, but never more
 // than there are blocks, so that every share holds at least one block
 // (workers past the count get no share).
-__device__ __forceinline__ int64_t share_count(const Params& p, int64_t B) {
+__host__ __device__ __forceinline__ int64_t share_count(const Params& p, int64_t B) {
     return max((int64_t)1, min((int64_t)p.workers, B));
 }
 
@@ -360,7 +360,7 @@ __device__ __forceinline__ bool arrive(const Params& p, unsigned int* cnt, int a
 }
 
 // Blocks of segment [fs, fs + nbs) held by shares sh .. min(sh + span - 1, wb).
-__device__ __forceinline__ int64_t blocks_in(int64_t B, int64_t W, int64_t fs, int nbs,
+__host__ __device__ __forceinline__ int64_t blocks_in(int64_t B, int64_t W, int64_t fs, int nbs,
                                              int64_t wb, int64_t sh, int span) {
     const int64_t b0 = max(fs, share_start(sh, B, W));
     const int64_t b1 = min(fs + nbs, share_start(min(sh + span - 1, wb) + 1, B, W));
@@ -518,7 +518,7 @@ struct CutPiece {
 // wa_known / wb_known: the first / last share of the segment when the caller
 // knows it (-1 otherwise), which spares a 64-bit division each; f_wa: the
 // first block of share wa when wa_known.
-__device__ __forceinline__ CutPiece cut_piece(const Params& p, int64_t B, int64_t wme, int64_t fs,
+__host__ __device__ __forceinline__ CutPiece cut_piece(const Params& p, int64_t B, int64_t wme, int64_t fs,
                                               int pb, int nbs, int s, int g, int c, int q0,
                                               int rows, int64_t wa_known, int64_t f_wa,
                                               int64_t wb_known) {
