@@ -41,6 +41,13 @@ CASES = {
     "singletons": lambda: W.best_of_n("sp_single", 74, num_groups=5, n_forks=1,
                                       prompt_len=130, shared_extra_max=15, private_max=50,
                                       num_heads=8, num_kv_heads=2, head_dim=64),
+    # long prompts, 4 forks x GQA 4 = 16 rows per KV head: the prefix phase
+    # runs the per-warp kernel with its in-kernel merge (8 blocks per worker
+    # and more), writing the base-2 log-sum-exps the final merge needs
+    "long_prefix_in_kernel": lambda: W.best_of_n("sp_long", 76, num_groups=8, n_forks=4,
+                                                 prompt_len=4096, shared_extra_max=15,
+                                                 private_max=64, num_heads=32, num_kv_heads=8,
+                                                 head_dim=128),
     # a prompt that fills its last block: forks share every prompt block
     "block_aligned_prompt": lambda: W.best_of_n("sp_aligned", 75, num_groups=2, n_forks=3,
                                                 prompt_len=255, shared_extra_max=1,
