@@ -337,8 +337,8 @@ constexpr int kCounterRegion = pa::kBalancedMaxWorkers;   // counters per region
 // Release: the warp barrier orders every lane's stores before lane 0's
 // acq_rel atomic (cumulative, as a CTA barrier before a thread's release);
 // acquire: the same atomic, then a warp barrier before the lanes read the
-// pieces (through L2, ld.global.cg). A count past the total means the
-// counters were not zero on entry.
+// pieces (through L2, ld.global.cg). A count past the total, before or
+// after the addition, means the counters were not zero on entry.
 __device__ __forceinline__ bool arrive(const Params& p, unsigned int* cnt, int add, int total,
                                        int lane) {
     __syncwarp();
@@ -350,7 +350,10 @@ __device__ __forceinline__ bool arrive(const Params& p, unsigned int* cnt, int a
                      : "l"(cnt), "r"((unsigned int)add)
                      : "memory");
         const unsigned int now = old + (unsigned int)add;
-        if (now > (unsigned int)total && p.err) atomicOr(p.err, pa::ERR_WORKSPACE);
+        // a clean counter never exceeds its total: checking the old value as
+        // well catches a dirty one that the addition wrapped around
+        if ((old > (unsigned int)total || now > (unsigned int)total) && p.err)
+            atomicOr(p.err, pa::ERR_WORKSPACE);
         last = now == (unsigned int)total;
         if (last) atomicExch(cnt, 0u);   // no other piece counts here in this launch
     }
@@ -567,7 +570,10 @@ __device__ __forceinline__ int arrive_pair(const Params& p, const CutPiece& a, b
                      : "l"(cnt), "r"((unsigned int)add)
                      : "memory");
         const unsigned int now = old + (unsigned int)add;
-        if (now > (unsigned int)total && p.err) atomicOr(p.err, pa::ERR_WORKSPACE);
+        // a clean counter never exceeds its total: checking the old value as
+        // well catches a dirty one that the addition wrapped around
+        if ((old > (unsigned int)total || now > (unsigned int)total) && p.err)
+            atomicOr(p.err, pa::ERR_WORKSPACE);
         last = now == (unsigned int)total;
         if (last) atomicExch(cnt, 0u);   // no other piece counts here in this launch
     }

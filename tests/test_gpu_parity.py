@@ -290,16 +290,18 @@ def test_one_workspace_serves_calls_of_any_shape():
             assert not big[:ARRIVAL_BYTES].any()
 
 
-def test_nonzero_arrival_counters_are_reported():
+@pytest.mark.parametrize("fill", [0x40, 0xFF])
+def test_nonzero_arrival_counters_are_reported(fill):
     """Counters that were not zeroed are reported in the device error word
-    (no fault, no hang); zeroed again, the next call is correct."""
+    (no fault, no hang), including 0xFF-poisoned ones that an addition wraps
+    around; zeroed again, the next call is correct."""
     # long GQA sequences: the decode kernel merges (and counts) itself
     wl, cache, si = _balanced_state("ws_dirty", [12000, 3000, 3000], [1, 1, 1], 32, 8, 128,
                                     seed=510)
     ref = oracle.run(wl, threads=THREADS)
     args = (si.q, cache.k, cache.v, si.block_tables, si.context_lens, si.max_context_len,
             wl.scale, si.query_start_loc, si.max_q_len, cache.num_blocks)
-    si.workspace[:ARRIVAL_BYTES].fill_(0x40)       # every counter 0x40404040: past any segment
+    si.workspace[:ARRIVAL_BYTES].fill_(fill)       # every counter past any segment's total
     pa.decode(si.out, *args, workspace=si.workspace)
     torch.cuda.synchronize()
     assert pa.device_error() & pa.DEVERR_WORKSPACE
