@@ -590,7 +590,6 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 4)
     using namespace pa::sched;
     using Lay = RowsLayout<D, S>;
     using PK = Pack<T>;
-    constexpr int kKSteps = D / 16;
     constexpr int kNTiles = D / 8;
     constexpr int RT = kRowsTile;
 
