@@ -271,6 +271,16 @@ def decode_workspace_size(num_seqs: int, num_q_tokens: int, num_heads: int, num_
                                               partition_size))
 
 
+def zeroed_workspace(nbytes: int, device="cuda"):
+    """A decode workspace of `nbytes` (from decode_workspace_size or
+    decode_shared_prefix_workspace_size): zero-filled as the arrival counters
+    at its start require, 256-byte aligned (torch's allocator), None for 0."""
+    import torch
+    if nbytes <= 0:
+        return None
+    return torch.zeros(int(nbytes), dtype=torch.uint8, device=device)
+
+
 def decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
            scale: float, query_start_loc=None, max_q_len: int = 1, num_blocks=None,
            k_scale=None, v_scale=None, k_zp=None, v_zp=None, partition_size: int = 0,

@@ -20,7 +20,8 @@ import numpy as np
 import torch
 
 from . import (BLOCK_SIZE, Pool, append_kv, copy_blocks, decode, decode_shared_prefix,
-               decode_shared_prefix_workspace_size, decode_workspace_size)
+               decode_shared_prefix_workspace_size, decode_workspace_size,
+               zeroed_workspace)
 
 KV_TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "int8": torch.int8,
             "fp8": torch.float8_e4m3fn}
@@ -161,7 +162,7 @@ class PagedKVCache:
                 group_start=torch.from_numpy(gs).to(dev), prefix_len=torch.from_numpy(pl).to(dev),
                 group_start_host=gs, prefix_len_host=pl, max_group_q_len=max(gq),
                 max_prefix_len=int(pl.max()),
-                workspace=torch.zeros(sp_bytes, dtype=torch.uint8, device=dev))
+                workspace=zeroed_workspace(sp_bytes, dev))
         return StepInputs(
             key=torch.cat(ks).to(dev), value=torch.cat(vs).to(dev),
             slots=torch.from_numpy(np.ascontiguousarray(slots)).to(dev),
@@ -172,8 +173,7 @@ class PagedKVCache:
             query_start_loc=torch.from_numpy(qsl).to(dev) if multi else None,
             max_q_len=max(q_lens), max_context_len=max(lens),
             out=torch.empty((nq, q.shape[1], q.shape[2]), dtype=out_dtype, device=dev),
-            workspace=(torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-                       if ws_bytes else None),
+            workspace=zeroed_workspace(ws_bytes, dev),
             shared=shared)
 
     def write_step(self, si: StepInputs) -> None:
