@@ -28,15 +28,36 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak); seq-steps/s at 1 GPU"
-# Committed ncu summary per decode kernel family: the summary file and the
+# Committed ncu summary per profiled workload: the summary file and the
 # sources whose digest it records (traffic is reported only while they match).
+_DEC16 = ("paged_decode.cu", "balanced.cuh", "ptx.cuh")
 PROFILES = {
-    "16bit": ("paged_decode_llama3_8b.md", ("paged_decode.cu", "balanced.cuh", "ptx.cuh")),
-    "int8": ("paged_decode_int8_mixed.md", ("paged_decode_int8.cu", "balanced.cuh", "ptx.cuh")),
-    "fp8": ("paged_decode_fp8_llama3_8b.md", ("paged_decode_fp8.cu", "balanced.cuh", "ptx.cuh")),
-    "prefill": ("paged_prefill_tc_llama3_8b_chunked.md",
-                ("paged_prefill_tc.cu", "tcgen05.cuh", "ptx.cuh")),
+    "llama3_8b": ("paged_decode_llama3_8b.md", _DEC16),
+    "llama2_70b_best_of_5": ("paged_decode_llama2_70b_best_of_5.md", _DEC16),
+    "llama2_70b_best_of_5+read_once": ("shared_prefix_llama2_70b_best_of_5.md",
+                                       _DEC16 + ("shared_prefix.cu",)),
+    "long_context": ("paged_decode_long_context.md", _DEC16),
+    "mixed_int8": ("paged_decode_int8_mixed.md", ("paged_decode_int8.cu", "balanced.cuh",
+                                                  "ptx.cuh")),
+    "llama3_8b_fp8": ("paged_decode_fp8_llama3_8b.md", ("paged_decode_fp8.cu", "balanced.cuh",
+                                                        "ptx.cuh")),
+    "paged_prefill": ("paged_prefill_tc_llama3_8b_chunked.md",
+                      ("paged_prefill_tc.cu", "tcgen05.cuh", "ptx.cuh")),
 }
+# The configurations timed beside the headline in a default run: (entry,
+# workload, read-once shared prefixes).
+CONFIG_RUNS = (
+    ("llama2_70b_best_of_5", "llama2_70b_best_of_5", False),
+    ("llama2_70b_best_of_5_read_once", "llama2_70b_best_of_5", True),
+    ("long_context", "long_context", False),
+    ("mixed_int8", "mixed_int8", False),
+    ("llama3_8b_fp8", "llama3_8b_fp8", False),
+    ("paged_prefill", "paged_prefill", False),
+)
+
+
+def profile_key(workload: str, shared_prefix: bool = False) -> str:
+    return workload + ("+read_once" if shared_prefix else "")
 
 
 def parse():
@@ -45,7 +66,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama3_8b")
+    ap.add_argument("--workload", default=None,
+                    help="one workload alone (default: llama3_8b as the headline, with every "
+                         "other configuration timed beside it under `configs`)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the headline workload only")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shared-prefix", action="store_true",
@@ -107,31 +132,30 @@ def step_bytes(wl, out_bytes_per_elem=4):
             "decode": kv_read + q_b + out_b, "step": kv_read + q_b + out_b + appended}
 
 
-def kernel_family(kv_dtype: str) -> str:
-    return kv_dtype if kv_dtype in ("int8", "fp8") else "16bit"
-
-
-def kernel_digest(family: str = "16bit"):
+def kernel_digest(key: str = "llama3_8b"):
     h = hashlib.sha256()
-    for f in PROFILES[family][1]:
+    for f in PROFILES[key][1]:
         with open(os.path.join(ROOT, "paged_kv_cache_154_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(family: str = "16bit", workload: str = ""):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source and on this workload; else None."""
+def recorded_traffic(key: str):
+    """DRAM bytes (read + write) of one attention call from the committed ncu
+    summary of this workload, if it was taken on the current kernel source;
+    else None."""
+    if key not in PROFILES:
+        return None
     try:
-        text = open(os.path.join(ROOT, "profiles", PROFILES[family][0])).read()
+        text = open(os.path.join(ROOT, "profiles", PROFILES[key][0])).read()
     except OSError:
         return None
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_b = re.search(r"dram_bytes_per_call:\s*([0-9.eE+]+)", text)
     m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
-    if not m_sha or not m_b or m_sha.group(1) != kernel_digest(family):
+    if not m_sha or not m_b or m_sha.group(1) != kernel_digest(key):
         return None
-    if not m_w or m_w.group(1) != workload:
+    if not m_w or m_w.group(1) != key:
         return None
     return float(m_b.group(1))
 
@@ -222,7 +246,7 @@ def build_state(wl, device, partition_size, shared_prefix=False):
     si = cache.prepare_step(wl.step, names, wl.q, torch.float32, partition_size,
                             shared_prefix=shared_prefix)
     torch.cuda.synchronize()
-    return cache, si
+    return cache, si, names
 
 
 def unique_kv_bytes(wl, group_start, prefix_len):
@@ -284,25 +308,29 @@ def roofline_kernel(wl, si, partition_size, prefill_tc):
     return "pa_decode (paged_decode_kernel + split_kv_reduce_kernel)"
 
 
-def run_ours(args, rank, world, local):
-    import torch
-    import workloads as W
-    import paged_kv_cache_154_gb300 as pa
+def percentile(xs, q):
+    """The q-th percentile (0..100) of xs, linear between order statistics."""
+    ys = sorted(xs)
+    if len(ys) == 1:
+        return ys[0]
+    x = (len(ys) - 1) * q / 100.0
+    i = int(x)
+    j = min(i + 1, len(ys) - 1)
+    return ys[i] + (ys[j] - ys[i]) * (x - i)
 
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-    wl = rank_workload(args.workload, rank)
-    if args.shared_prefix and args.partition_size:
+
+def time_workload(wl, device, steps, warmup, partition_size=0, shared_prefix=False, world=1,
+                  local=0, keep_state=False):
+    """Times `steps` steps of one workload on this rank: each step the cache
+    writes (copy-on-write copies, append) and the attention call, replayed
+    from two CUDA graphs, timed with CUDA events on the launching stream, L2
+    flushed before each step outside the timed window. Returns the timings
+    and, with keep_state, the device state for the end-to-end leg."""
+    import torch
+    import paged_kv_cache_154_gb300 as pa
+    if shared_prefix and partition_size:
         raise SystemExit("--shared-prefix uses the balanced schedule (partition size 0)")
-    cache, si = build_state(wl, device, args.partition_size, args.shared_prefix)
-    nbytes = step_bytes(wl)
-    if si.shared is not None:
-        nbytes["kv_read_unique"] = unique_kv_bytes(wl, si.shared.group_start_host,
-                                                   si.shared.prefix_len_host)
-        nbytes["decode_unique"] = nbytes["kv_read_unique"] + nbytes["q"] + nbytes["out"]
+    cache, si, names = build_state(wl, device, partition_size, shared_prefix)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
@@ -316,19 +344,18 @@ def run_ours(args, rank, world, local):
 
     # the step as two CUDA graphs (cache writes; attention), replayed back to back
     g_write = cache.capture(cache.write_step, si)
-    g_attend = cache.capture(cache.attend_step, si, wl.scale, args.partition_size)
+    g_attend = cache.capture(cache.attend_step, si, wl.scale, partition_size)
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         g_write.replay()
         g_attend.replay()
     torch.cuda.synchronize()
     assert pa.device_error() == 0
-
-    K = args.steps
+    K = steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     sampler = ClockSampler(local)
     time.sleep(0.15)
@@ -348,39 +375,123 @@ def run_ours(args, rank, world, local):
     time.sleep(0.1)
     sampler.stop()
     assert pa.device_error() == 0
-    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
-    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
-    tot_ms = max_over_ranks(sum(step_ms), world, device)
+    res = {"step_ms": [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)],
+           "dec_ms": [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)],
+           "clocks": sampler.summary(), "wall_s": wall1 - wall0,
+           "si_info": {"pairs": si.pairs is not None, "max_q_len": si.max_q_len,
+                       "max_context_len": si.max_context_len,
+                       "shared": (None if si.shared is None else
+                                  (si.shared.group_start_host, si.shared.prefix_len_host,
+                                   si.shared.max_group_q_len))}}
+    res["launches"] = launches_per_step(si, partition_size, prefill_tc_runs(wl, partition_size,
+                                                                            si),
+                                        wl.kv_dtype, wl.num_heads // wl.num_kv_heads)
+    res["kernel"] = roofline_kernel(wl, si, partition_size,
+                                    prefill_tc_runs(wl, partition_size, si))
+    del g_write, g_attend, flush, clean
+    if keep_state:
+        res["state"] = (cache, si, names)
+    else:
+        del cache, si
+        torch.cuda.empty_cache()
+    return res
+
+
+def prefill_tc_runs(wl, partition_size, si) -> bool:
+    """Does the library send this step's attention to the tensor-core prefill
+    kernel? (long query runs over a 16-bit cache with head_dim 128)."""
+    return (is_prefill(wl) and wl.kv_dtype in ("bf16", "f16") and wl.head_dim == 128
+            and partition_size == 0 and si.shared is None)
+
+
+def roofline_entry(wl, res, key, shared_prefix=False):
+    """The attention call's roofline: algorithmic bytes (or, for prefill,
+    flops) per call over its mean event time, against the measured peak."""
+    nbytes = step_bytes(wl)
+    sh = res["si_info"]["shared"]
+    if sh is not None:
+        nbytes["kv_read_unique"] = unique_kv_bytes(wl, sh[0], sh[1])
+        nbytes["decode_unique"] = nbytes["kv_read_unique"] + nbytes["q"] + nbytes["out"]
+    dec = res["dec_ms"]
+    dec_avg_s = statistics.mean(dec) / 1e3
+    if is_prefill(wl):
+        units = attention_flops(wl)
+        peak, kind = measured_peak("bf16_tflops")
+        achieved, unit, bound = units / dec_avg_s / 1e12, "TFLOP/s", "tensor"
+        ukey = "algorithmic_flops_per_launch"
+    else:
+        # the method's own algorithmic bytes: read-once decode reads shared blocks once
+        units = nbytes.get("decode_unique", nbytes["decode"])
+        peak, kind = measured_peak("hbm_gbs")
+        achieved, unit, bound = units / dec_avg_s / 1e9, "GB/s", "hbm"
+        ukey = "algorithmic_bytes_per_launch"
+    roof = {"kernel": res["kernel"], "bound": bound, "achieved": round(achieved, 1),
+            "peak": peak, "peak_kind": kind, "unit": unit, "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(key), ukey: units,
+            "decode_ms_avg": round(dec_avg_s * 1e3, 5),
+            "decode_ms_p50": round(statistics.median(dec), 5),
+            "decode_ms_p95": round(percentile(dec, 95), 5)}
+    if sh is not None:
+        roof["logical_bytes_per_launch"] = nbytes["decode"]
+        roof["logical_gbs"] = round(nbytes["decode"] / dec_avg_s / 1e9, 1)
+    return roof, nbytes
+
+
+def config_entry(name, workload, shared_prefix, device, steps, warmup):
+    """One configuration's timings as a `configs` entry of the bench line."""
+    import workloads as W
+    wl = W.NAMED[workload]()
+    res = time_workload(wl, device, steps, warmup, 0, shared_prefix)
+    key = profile_key(workload, shared_prefix)
+    roof, nbytes = roofline_entry(wl, res, key, shared_prefix)
+    tot_s = sum(res["step_ms"]) / 1e3
+    return {"workload": workload, "read_once_shared_prefix": shared_prefix,
+            "dtype": wl.kv_dtype, "steps": steps,
+            "value": round(steps * nbytes["step"] / tot_s / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(1e3 * tot_s / steps, 5),
+            "seq_steps_per_s": round(steps * wl.num_seqs / tot_s, 1),
+            "num_seqs": wl.num_seqs, "heads": [wl.num_heads, wl.num_kv_heads],
+            "head_dim": wl.head_dim, "context_tokens": sum(wl.context_lens),
+            "query_tokens": sum(wl.q_lens), "bytes_per_step": nbytes, "roofline": roof,
+            "gpu_launches_per_step": res["launches"], "clocks": res["clocks"]}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    workload = args.workload or "llama3_8b"
+    wl = rank_workload(workload, rank)
+    res = time_workload(wl, device, args.steps, args.warmup, args.partition_size,
+                        args.shared_prefix, world, local, keep_state=True)
+    nbytes = step_bytes(wl)
+    K = args.steps
+    tot_ms = max_over_ranks(sum(res["step_ms"]), world, device)
     job_bytes = sum_over_ranks(float(nbytes["step"]), world, device)
     job_seqs = sum_over_ranks(float(wl.num_seqs), world, device)
 
-    # end to end: host (pinned) inputs copied in, result copied out, every step
-    e2e = measure_e2e(wl, cache, si, args, (g_write, g_attend), K_e2e=min(K, 50))
+    # end to end through the public API: host pool, pinned host buffers, C-ABI calls
+    cache, si, names = res.pop("state")
+    e2e = None
+    if not args.shared_prefix and args.partition_size == 0:
+        e2e = measure_e2e(wl, cache, si, names, steps=min(K, 50))
+    del cache, si
+    torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-    peak, peak_kind = measured_peak()
-    hbm_peak = peak
-    dec_avg_s = statistics.mean(dec_ms) / 1e3
-    # the method's own algorithmic bytes: read-once decode reads shared blocks once
-    alg_bytes = nbytes.get("decode_unique", nbytes["decode"])
-    achieved = alg_bytes / dec_avg_s / 1e9
-    roof_unit, bound, alg_units = "GB/s", "hbm", alg_bytes
-    # the library sends long query runs over a 16-bit cache with head_dim 128
-    # to the tensor-core prefill kernel
-    prefill_tc = (is_prefill(wl) and wl.kv_dtype in ("bf16", "f16") and wl.head_dim == 128
-                  and args.partition_size == 0 and si.shared is None
-                  and "PA_PREFILL_MMA_SYNC" not in os.environ)
-    if is_prefill(wl):
-        # long query runs: a contraction on the tensor cores, not a KV stream
-        flops = attention_flops(wl)
-        peak, peak_kind = measured_peak("bf16_tflops")
-        achieved = flops / dec_avg_s / 1e12
-        roof_unit, bound, alg_units = "TFLOP/s", "tensor", flops
+    key = profile_key(workload, args.shared_prefix)
+    roof, nbytes = roofline_entry(wl, res, key, args.shared_prefix)
+    hbm_peak, _ = measured_peak()
     value = K * job_bytes / (tot_ms / 1e3) / 1e9
     seq_steps = K * job_seqs / (tot_ms / 1e3)
+    si_info = res["si_info"]
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -398,8 +509,8 @@ def run_ours(args, rank, world, local):
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "block_size": 16, "context_tokens": sum(wl.context_lens),
                    "schedule": ("balanced, read-once shared prefixes "
-                                f"({len(si.shared.prefix_len_host)} fork groups)"
-                                if si.shared is not None else
+                                f"({len(si_info['shared'][1])} fork groups)"
+                                if si_info["shared"] is not None else
                                 "balanced" if args.partition_size == 0
                                 else f"partitions of {args.partition_size}"),
                    "l2": "flushed between steps (2x L2 write, then a 2x L2 read so no dirty "
@@ -410,94 +521,141 @@ def run_ours(args, rank, world, local):
                                    if world > 1 else "1 GPU")},
         "seq_steps_per_s": round(seq_steps, 1),
         "pct_of_hbm_peak": round(100 * value / hbm_peak, 2),
-        "roofline": {"kernel": roofline_kernel(wl, si, args.partition_size, prefill_tc),
-                     "bound": bound, "achieved": round(achieved, 1), "peak": peak,
-                     "peak_kind": peak_kind, "unit": roof_unit,
-                     "frac": round(achieved / peak, 4),
-                     "traffic": (recorded_traffic("prefill", args.workload) if prefill_tc else
-                                 recorded_traffic(kernel_family(wl.kv_dtype), args.workload)
-                                 if args.partition_size == 0 and si.shared is None
-                                 and not is_prefill(wl) else None),
-                     ("algorithmic_flops_per_launch" if bound == "tensor"
-                      else "algorithmic_bytes_per_launch"): alg_units,
-                     "decode_ms_avg": round(dec_avg_s * 1e3, 5),
-                     "decode_ms_p50": round(statistics.median(dec_ms), 5)},
+        "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": launches_per_step(si, args.partition_size, prefill_tc, wl.kv_dtype,
-                                          wl.num_heads // wl.num_kv_heads) * K,
-        "clocks": sampler.summary(),
-        "wall_s_timed": round(wall1 - wall0, 3),
+        "gpu_launches": res["launches"] * K,
+        "clocks": res["clocks"],
+        "wall_s_timed": round(res["wall_s"], 3),
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=12.0)
+    # the other configurations, each timed on its own (default run only)
+    if world == 1 and args.workload is None and not args.no_configs:
+        line["configs"] = {}
+        for name, w, sp in CONFIG_RUNS:
+            line["configs"][name] = config_entry(name, w, sp, device, max(50, K), args.warmup)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def measure_e2e(wl, cache, si, args, graphs, K_e2e):
-    """Same metric through the public API with host buffers: per step, copy
-    q, the new K/V rows, the slots, block tables, lengths (and copy pairs)
-    from pinned host memory, run the step, copy the output back, sync."""
+def measure_e2e(wl, cache, si, names, steps):
+    """The same metric through the public API, as a user's decode loop runs
+    it, every step: the host pool reserves each sequence's new slots (its
+    copy-on-write pairs come back) and writes the block tables and lengths;
+    those, the step's q and new K/V rows are copied from pinned host memory
+    to the device; pa_copy_blocks (when there are pairs), pa_append_kv and
+    pa_decode run; the output is copied back to pinned host memory and the
+    stream synchronised. The sequences grow by their query run each step,
+    and each step's bytes are counted from its own lengths."""
+    import numpy as np
     import torch
     import paged_kv_cache_154_gb300 as pa
-    pairs = []                                   # (device input, pinned host copy)
-    for name in ("q", "key", "value", "slots", "block_tables", "context_lens", "pairs",
-                 "query_start_loc"):
-        t = getattr(si, name)
-        if t is not None:
-            pairs.append((t, t.cpu().pin_memory()))
-    if si.shared is not None:                    # the step's fork groups are inputs too
-        for t in (si.shared.group_start, si.shared.prefix_len):
-            pairs.append((t, t.cpu().pin_memory()))
+    dev = si.q.device
+    seqs = [names[op.seq] for op in wl.step]
+    q_lens = [int(op.k.shape[0]) for op in wl.step]
+    r_max = max(q_lens)
+    T = sum(q_lens)
+    warm = 3
+    cap_blocks = si.block_tables.shape[1] + ((warm + steps) * r_max + 15) // 16 + 1
+    max_len_final = si.max_context_len + (warm + steps) * r_max
+    ws_bytes = pa.decode_workspace_size(len(seqs), T, wl.num_heads, wl.num_kv_heads,
+                                        wl.head_dim, r_max, max_len_final, 0)
+    ws = pa.zeroed_workspace(ws_bytes, dev)
+    # device inputs of fixed shape; pinned host staging buffers
+    h = {"q": si.q.cpu().pin_memory(), "key": si.key.cpu().pin_memory(),
+         "value": si.value.cpu().pin_memory(),
+         "slots": torch.empty(T, dtype=torch.int64).pin_memory(),
+         "bt": torch.empty((len(seqs), cap_blocks), dtype=torch.int32).pin_memory(),
+         "cl": torch.empty(len(seqs), dtype=torch.int32).pin_memory()}
+    d = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in h.items()}
+    qsl = si.query_start_loc            # fixed: the run lengths do not change
     out_h = torch.empty(si.out.shape, dtype=si.out.dtype).pin_memory()
-    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
-    d2h = out_h.numel() * out_h.element_size()
+    out_d = torch.empty_like(si.out)
     stream = torch.cuda.current_stream()
-    times = []
-    for k in range(K_e2e + 3):
+    kv_elem = 1 if wl.kv_dtype in ("int8", "fp8") else 2
+    per_tok = 2 * wl.num_kv_heads * wl.head_dim * kv_elem + (
+        2 * wl.num_kv_heads * 5 if wl.kv_dtype == "int8" else 0)
+    fixed = T * wl.num_heads * wl.head_dim * (2 + 4) + T * per_tok
+    times, nbytes, h2d_last = [], 0, 0
+    for k in range(warm + steps):
         t0 = time.perf_counter()
-        for d, h in pairs:
-            d.copy_(h, non_blocking=True)
-        for g in graphs:
-            g.replay()
-        out_h.copy_(si.out, non_blocking=True)
+        pairs, off = [], 0
+        slots_np = h["slots"].numpy()
+        for s, r in zip(seqs, q_lens):
+            sl, pair = cache.pool.seq_append_slots(s, r)
+            slots_np[off:off + r] = sl
+            off += r
+            if pair is not None:
+                pairs.append(pair)
+        bt, cl = cache.pool.block_tables(seqs, cap_blocks)
+        h["bt"].numpy()[:] = bt
+        h["cl"].numpy()[:] = cl
+        for name in h:
+            d[name].copy_(h[name], non_blocking=True)
+        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        if pairs:
+            pr_h = torch.tensor(pairs, dtype=torch.int32).pin_memory()
+            pr = pr_h.to(dev, non_blocking=True)
+            h2d += pr_h.numel() * 4
+            pa.copy_blocks(cache.k, cache.v, pr, cache.num_blocks, cache.k_scale, cache.v_scale,
+                           cache.k_zp, cache.v_zp)
+        pa.append_kv(d["key"], d["value"], cache.k, cache.v, d["slots"], cache.num_blocks,
+                     cache.k_scale, cache.v_scale, cache.k_zp, cache.v_zp)
+        max_len = int(cl.max())
+        pa.decode(out_d, d["q"], cache.k, cache.v, d["bt"], d["cl"], max_len, wl.scale, qsl,
+                  si.max_q_len, cache.num_blocks, cache.k_scale, cache.v_scale, cache.k_zp,
+                  cache.v_zp, 0, ws)
+        out_h.copy_(out_d, non_blocking=True)
         stream.synchronize()
-        if k >= 3:
+        if k >= warm:
             times.append(time.perf_counter() - t0)
-    nbytes = step_bytes(wl)["step"]
-    return {"value": round(len(times) * nbytes / sum(times) / 1e9, 1), "unit": "GB/s",
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": round(1e3 * statistics.mean(times), 4), "steps": len(times)}
+            nbytes += int(cl.astype(np.int64).sum()) * per_tok + fixed
+            h2d_last = h2d
+    assert pa.device_error() == 0
+    d2h = out_h.numel() * out_h.element_size()
+    return {"value": round(nbytes / sum(times) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d_last), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(1e3 * statistics.mean(times), 4), "steps": len(times),
+            "path": "host pool (pa_seq_append_slots, pa_pool_block_tables) + pinned H2D + "
+                    "pa_copy_blocks/pa_append_kv/pa_decode + D2H, per step"}
 
 
 def cpu_baseline(wl, budget_s=12.0, sample_seqs=None):
     """The oracle (plain C, fp64, OpenMP over (sequence, kv head)) on a
     bounded sample of the workload's sequences, same metric (GB/s of the
-    attention's algorithmic bytes for the sampled sequences)."""
-    import numpy as np
+    attention's algorithmic bytes for the sampled sequences), with every
+    host core and with one thread."""
     import oracle
     threads = os.cpu_count() or 1
     run = oracle.run(wl, decode=False)
+
+    def timed(n, nthreads, budget):
+        qsl = wl.query_start_loc[: n + 1]
+        kv_elem = 1 if wl.kv_dtype in ("int8", "fp8") else 2
+        nbytes = sum(2 * wl.context_lens[s] * wl.num_kv_heads * wl.head_dim * kv_elem
+                     for s in range(n))
+        nq = int(qsl[-1])
+        nbytes += nq * wl.num_heads * wl.head_dim * (2 + 4)
+        reps, t_total = 0, 0.0
+        while t_total < budget and reps < 50:
+            t0 = time.perf_counter()
+            oracle.attend(run.q64[:nq], run.cache, run.block_tables[:n], run.context_lens[:n],
+                          qsl, wl.num_heads, wl.scale, threads=nthreads)
+            t_total += time.perf_counter() - t0
+            reps += 1
+        return reps * nbytes / t_total / 1e9, reps, t_total
+
     n = wl.num_seqs if sample_seqs is None else min(sample_seqs, wl.num_seqs)
-    qsl = wl.query_start_loc[: n + 1]
-    nbytes = 0
-    kv_elem = 1 if wl.kv_dtype in ("int8", "fp8") else 2
-    for s in range(n):
-        nbytes += 2 * wl.context_lens[s] * wl.num_kv_heads * wl.head_dim * kv_elem
-    nq = int(qsl[-1])
-    nbytes += nq * wl.num_heads * wl.head_dim * (2 + 4)
-    reps, t_total = 0, 0.0
-    while t_total < budget_s and reps < 50:
-        t0 = time.perf_counter()
-        oracle.attend(run.q64[:nq], run.cache, run.block_tables[:n], run.context_lens[:n],
-                      qsl, wl.num_heads, wl.scale, threads=threads)
-        t_total += time.perf_counter() - t0
-        reps += 1
-    return {"value": round(reps * nbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": threads,
-            "kind": "oracle",
+    v, reps, t = timed(n, threads, budget_s)
+    n1 = min(n, 4)
+    v1, reps1, t1 = timed(n1, 1, budget_s / 3)
+    return {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} of {wl.num_seqs} sequences (all heads), attention only, "
-                      f"{reps} repetitions in {t_total:.1f} s"}
+                      f"{reps} repetitions in {t:.1f} s",
+            "single_thread": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"{n1} of {wl.num_seqs} sequences (all heads), "
+                                        f"attention only, {reps1} repetitions in {t1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
@@ -507,7 +665,7 @@ def run_reference(args, rank, world):
         return
     import workloads as W
     import oracle
-    wl = W.NAMED[args.workload]()
+    wl = W.NAMED[args.workload or "llama3_8b"]()
     threads = os.cpu_count() or 1
     run = oracle.run(wl, decode=False)
     # bounded sample: the first sequences whose keys add up to ~1/8 of the batch

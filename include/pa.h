@@ -285,11 +285,14 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_tokens,
  *                  any sizes on one stream. With partition_size 0 the
  *                  decode kernel counts the blocks of each cut (sequence,
  *                  KV head) as its pieces finish, and the piece that
- *                  completes the count merges them; a counter found
- *                  non-zero sets PA_DEVERR_WORKSPACE in the device error
- *                  word. After a call whose device error word is non-zero,
- *                  zero the counters again. The rest needs no
- *                  initialisation. Layout after the counters with
+ *                  completes the count merges them. A counter that a call
+ *                  finds above its total sets PA_DEVERR_WORKSPACE in the
+ *                  device error word; a stale count below the total is not
+ *                  always detected (it can make a merge run before all of
+ *                  its pieces are written). So after a call whose device
+ *                  error word is non-zero (a bounded wait gave up and left
+ *                  counts short), zero the counters again before the next
+ *                  call. The rest needs no initialisation. Layout after the counters with
  *                  partition_size > 0 and P = ceil(max_context_len /
  *                  partition_size):
  *                    o_part fp32 [num_q_tokens][num_heads][P][head_dim]
@@ -318,7 +321,7 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* pa_decode without caller-provided workspace: the split-KV scratch is a
- * built-in 16 MiB device array inside this library. The pages have no
+ * built-in 40 MiB device array inside this library. The pages have no
  * counterpart to this call; it exists for callers that cannot allocate
  * device memory themselves -- for example code embedded in a host
  * application whose own allocator owns all device memory (a stray
@@ -328,20 +331,24 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
  *   - Arguments and results are exactly those of pa_decode, minus
  *     workspace/workspace_bytes. The caller still passes (and owns) every
  *     input and output buffer.
- *   - If pa_decode_workspace_size() for these arguments exceeds 16 MiB
- *     (16777216 bytes) the call returns PA_ERR_UNSUPPORTED and launches
- *     nothing; a larger partition_size lowers the need.
+ *   - If pa_decode_workspace_size() for these arguments exceeds 40 MiB
+ *     (41943040 bytes) the call returns PA_ERR_UNSUPPORTED and launches
+ *     nothing. 40 MiB covers every call with at most 16 query rows per KV
+ *     head (q heads per KV head x max_q_len), at any batch size; calls with
+ *     more rows may need a larger partition_size, or pa_decode.
  *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating
- *     library routine. Every GPU that loads the library holds the 16 MiB
+ *     library routine. Every GPU that loads the library holds the 40 MiB
  *     array until the process exits.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
- *   - All calls share the one array and it keeps the last call's contents.
- *     It starts zeroed (a static device array), and each call leaves its
- *     arrival counters zero as pa_decode describes; calls whose work
- *     overlaps on the GPU (different streams, or different host threads)
- *     race on it and must be serialised. */
+ *     that first call before any stream capture. The cached address is not
+ *     valid after cudaDeviceReset: do not use this call across a reset.
+ *   - Every call first clears the array's arrival counters with a
+ *     cudaMemsetAsync on `stream` (no allocation), so a call that gave up
+ *     (non-zero device error word) leaves no stale count for the next one.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     calls whose work overlaps on the GPU (different streams, or different
+ *     host threads) race on it and must be serialised. */
 pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
                              pa_dtype q_dtype, const void* k_cache,
                              const void* v_cache, pa_dtype kv_dtype,

@@ -330,7 +330,7 @@ def decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
         _ptr(workspace), ws_bytes, _stream(stream)))
 
 
-NO_ALLOC_WORKSPACE_BYTES = 16 << 20
+NO_ALLOC_WORKSPACE_BYTES = 40 << 20
 
 
 def decode_no_alloc(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,

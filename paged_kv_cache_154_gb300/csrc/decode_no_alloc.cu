@@ -1,6 +1,11 @@
 // pa_decode_no_alloc: pa_decode for callers that cannot allocate device
 // memory. The split-KV workspace lives in a file-scope device array of fixed
 // size instead of caller memory; everything else is pa_decode unchanged.
+//
+// Size: 40 MiB holds the largest workspace of any call with at most 16 query
+// rows per KV head (q heads per KV head x the longest query run), whatever
+// the batch: 24 KiB of arrival counters, up to 32 KiB of prefix sums and
+// 2 x 2048 partial slots of 8,352 bytes (head_dim 128) -- about 32.7 MiB.
 #include <mutex>
 #include <vector>
 
@@ -8,7 +13,7 @@
 
 namespace {
 
-constexpr size_t kStaticWorkspaceBytes = (size_t)16 << 20;   // 16 MiB per device
+constexpr size_t kStaticWorkspaceBytes = (size_t)40 << 20;   // 40 MiB per device
 
 // Held by every GPU that loads this library, for the life of the process.
 static __device__ __align__(256) unsigned char g_decode_workspace[kStaticWorkspaceBytes];
@@ -54,8 +59,17 @@ extern "C" pa_status pa_decode_no_alloc(
                         "more than the built-in %zu; use pa_decode with caller memory",
                         need, kStaticWorkspaceBytes);
     void* ws = nullptr;
-    if (need > 0)
+    if (need > 0) {
         if (pa_status s = workspace_address(&ws)) return s;
+        // The arrival counters must be zero when a call starts. A call whose
+        // bounded wait gave up can leave some part-counted, and the caller has
+        // no pointer to this array to clear them, so every call clears them
+        // itself, in stream order before its kernels (a memset, no allocation).
+        if (pa_status s = pa::cuda_status(
+                cudaMemsetAsync(ws, 0, (size_t)pa::kArrivalBytes, static_cast<cudaStream_t>(stream)),
+                "pa_decode_no_alloc: clear the arrival counters"))
+            return s;
+    }
     return pa_decode(out, out_dtype, q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale,
                      k_zp, v_zp, block_tables, max_blocks_per_seq, context_lens,
                      query_start_loc, num_seqs, num_q_tokens, max_q_len, num_heads,

@@ -653,8 +653,7 @@ namespace pa {
 bool prefill_tc_applies(const DecodeArgs& a) {
     const int64_t rows = (int64_t)(a.num_heads / a.num_kv_heads) * a.max_q_len;
     return (a.kv_dtype == PA_BF16 || a.kv_dtype == PA_F16) && a.head_dim == 128 &&
-           a.partition_size == 0 && !a.ctx_start && !a.lse_out && !a.unmasked && rows >= 256 &&
-           std::getenv("PA_PREFILL_MMA_SYNC") == nullptr;
+           a.partition_size == 0 && !a.ctx_start && !a.lse_out && !a.unmasked && rows >= 256;
 }
 
 pa_status launch_prefill_tc(const DecodeArgs& a) {

@@ -58,14 +58,30 @@ def test_roofline_kernel_names_what_runs():
 
 def test_recorded_traffic_only_for_the_profiled_workload():
     import re
-    for family, workload in (("16bit", "llama3_8b"), ("int8", "mixed_int8"),
-                             ("fp8", "llama3_8b_fp8"), ("prefill", "paged_prefill")):
-        text = open(os.path.join(ROOT, "profiles", bench.PROFILES[family][0])).read()
-        assert re.search(r"^workload:\s*" + workload + r"\s*$", text, re.M), family
+    for key, (fname, _) in bench.PROFILES.items():
+        path = os.path.join(ROOT, "profiles", fname)
+        if not os.path.exists(path):
+            assert bench.recorded_traffic(key) is None
+            continue
+        text = open(path).read()
+        assert re.search(r"^workload:\s*" + re.escape(key) + r"\s*$", text, re.M), key
         fresh = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text).group(1) == \
-            bench.kernel_digest(family)
-        t = bench.recorded_traffic(family, workload)
+            bench.kernel_digest(key)
+        t = bench.recorded_traffic(key)
         # reported exactly when the summary was taken on the current source
-        assert (t is not None and t > 0) == fresh, (family, workload)
-        assert bench.recorded_traffic(family, "tiny") is None
-        assert bench.recorded_traffic(family, "long_context") is None
+        assert (t is not None and t > 0) == fresh, key
+    assert bench.recorded_traffic("tiny") is None
+
+
+def test_percentile():
+    xs = list(range(1, 101))
+    assert bench.percentile(xs, 50) == pytest.approx(50.5)
+    assert bench.percentile(xs, 95) == pytest.approx(95.05)
+    assert bench.percentile([3.0], 95) == 3.0
+
+
+def test_every_config_run_names_a_workload_and_a_profile():
+    import workloads as W
+    for name, workload, shared in bench.CONFIG_RUNS:
+        assert workload in W.NAMED
+        assert bench.profile_key(workload, shared) in bench.PROFILES
