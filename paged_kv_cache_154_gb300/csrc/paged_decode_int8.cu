@@ -672,8 +672,6 @@ pa_status launch8_q(const pa::DecodeArgs& a, int mt, const CUtensorMap& mk,
 
 namespace pa {
 
-bool int8_tc_applies(const DecodeArgs& a);
-pa_status launch_decode_int8_tc(const DecodeArgs& a);
 
 pa_status launch_decode_int8(const DecodeArgs& a) {
     if (a.partition_size != 0)
@@ -681,9 +679,6 @@ pa_status launch_decode_int8(const DecodeArgs& a) {
     if (pa_status s = balanced_check(a)) return s;
     if (((uintptr_t)a.k_scale | (uintptr_t)a.v_scale | (uintptr_t)a.k_zp | (uintptr_t)a.v_zp) % 16)
         return fail(PA_ERR_INVALID_ARG, "k_scale, v_scale, k_zp and v_zp must be 16-byte aligned");
-    // many query rows per KV head (MQA, verify runs) at head_dim 128: the
-    // tensor-core kernel when asked for (PA_INT8_TC)
-    if (int8_tc_applies(a)) return launch_decode_int8_tc(a);
     const BalancedShape shape = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
                                                a.head_dim, a.max_q_len, a.max_context_len,
                                                kTileInt8);

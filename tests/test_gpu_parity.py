@@ -244,8 +244,12 @@ def test_balanced_partials_match_oracle(case):
             if lm[qi, h] == 0:
                 assert l[j] == 0 and np.isneginf(m[j])
                 continue
-            np.testing.assert_allclose(m[j], mm[qi, h] * np.log2(np.e), rtol=1e-5, atol=1e-4)
-            np.testing.assert_allclose(l[j], lm[qi, h], rtol=1e-4)
+            # m is the partial's reference (base 2): the row's largest logit, or,
+            # where a kernel moves it lazily, a logit at most 2^8 below it; l and
+            # O are relative to it, which is all the log-sum-exp merge uses
+            mx = mm[qi, h] * np.log2(np.e)
+            assert m[j] <= mx + 1e-4 and mx <= m[j] + 8 + 1e-4, (m[j], mx)
+            np.testing.assert_allclose(l[j] * np.exp2(m[j] - mx), lm[qi, h], rtol=1e-4)
             np.testing.assert_allclose(o[j] / l[j], om[qi, h], rtol=0, atol=2e-3)
 
 
@@ -379,27 +383,6 @@ def test_int8_small_shapes(case):
                   key_row_boost=4.0, boost_fraction=0.02)
     ref, cache, si, out = run_both(wl)
     check_cache_bits(ref, cache)
-    check_out(ref, out, "int8")
-
-
-@pytest.mark.parametrize("case", [c for c in INT8_SMALL if c[3] // c[4] * max(c[2]) >= 32
-                                  and c[5] == 128], ids=lambda c: c[0] + "_tc")
-def test_int8_tensor_core_kernel(case, monkeypatch):
-    """The opt-in tcgen05 INT8 kernel (PA_INT8_TC): 128-row chunks, fp16
-    (code - zp) operands built once per block, against the oracle."""
-    monkeypatch.setenv("PA_INT8_TC", "1")
-    name, lens, qlens, H, Hkv, d, qdt = case
-    wl = W.simple(name, 500 + len(name), lens, qlens, H, Hkv, d, "int8", q_dtype=qdt,
-                  key_row_boost=4.0, boost_fraction=0.02)
-    ref, cache, si, out = run_both(wl)
-    check_cache_bits(ref, cache)
-    check_out(ref, out, "int8")
-
-
-def test_mixed_int8_config_tensor_core_kernel(monkeypatch):
-    monkeypatch.setenv("PA_INT8_TC", "1")
-    wl = W.mixed_int8()
-    ref, cache, si, out = run_both(wl)
     check_out(ref, out, "int8")
 
 
