@@ -139,6 +139,13 @@ pa_status launch_decode(const DecodeArgs& a);
 // (tensor_maps.cu).
 pa_status cache_tensor_map(CUtensorMap* out, const void* ptr, int num_blocks, int num_kv_heads,
                            int head_dim, int elem_bytes);
+// 16-bit cache with head_dim 128 viewed in three dimensions -- 64 columns,
+// rows, the two 64-column halves of a row -- so that one box of 16 rows x 2
+// halves (4 KiB) moves a whole (block, kv head) tile in one copy, laid out in
+// shared memory as [half][16 rows][128 B] with the 128-byte swizzle (the
+// layout two 2-D boxes give).
+pa_status cache_tensor_map_tile(CUtensorMap* out, const void* ptr, int num_blocks,
+                                int num_kv_heads);
 
 // Host-side argument checks of the decode entry points (capi.cu).
 pa_status check_decode_args(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,

@@ -98,16 +98,19 @@ __device__ __forceinline__ uint32_t tile_offset(int row, int chunk) {
     return sub * (kBS * 128) + row * 128 + ((c ^ (row & 7)) << 4);
 }
 
-// Issue the K and V copies of one (block, kv head) tile into a stage.
+// Issue the K and V copies of one (block, kv head) tile into a stage: one
+// copy each (head_dim 128 through the whole-tile view, 64 through one box).
 template <int D>
 __device__ __forceinline__ void issue_tile(uint32_t stage, uint32_t bar, const CUtensorMap* mk,
                                            const CUtensorMap* mv, int row, uint64_t pol) {
     constexpr int kTile = kBS * D * 2;
     pa::mbar_arrive_expect_tx(bar, 2 * kTile);
-#pragma unroll
-    for (int sub = 0; sub < D / 64; ++sub) {
-        pa::tma_load_2d(stage + sub * kBS * 128, mk, sub * 64, row, bar, pol);
-        pa::tma_load_2d(stage + kTile + sub * kBS * 128, mv, sub * 64, row, bar, pol);
+    if constexpr (D == 128) {
+        pa::tma_load_3d(stage, mk, 0, row, 0, bar, pol);
+        pa::tma_load_3d(stage + kTile, mv, 0, row, 0, bar, pol);
+    } else {
+        pa::tma_load_2d(stage, mk, 0, row, bar, pol);
+        pa::tma_load_2d(stage + kTile, mv, 0, row, bar, pol);
     }
 }
 
@@ -1289,10 +1292,17 @@ pa_status launch_decode(const DecodeArgs& a) {
     if (a.partition_size == 0)
         if (pa_status s = balanced_check(a)) return s;
     CUtensorMap mk, mv;
-    if (pa_status s = cache_tensor_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
-        return s;
-    if (pa_status s = cache_tensor_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
-        return s;
+    if (a.head_dim == 128) {
+        if (pa_status s = cache_tensor_map_tile(&mk, a.k_cache, a.num_blocks, a.num_kv_heads))
+            return s;
+        if (pa_status s = cache_tensor_map_tile(&mv, a.v_cache, a.num_blocks, a.num_kv_heads))
+            return s;
+    } else {
+        if (pa_status s = cache_tensor_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
+            return s;
+        if (pa_status s = cache_tensor_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
+            return s;
+    }
     DecodeParams prm{};
     prm.out = a.out;
     prm.q = a.q;
