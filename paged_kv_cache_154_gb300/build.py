@@ -75,5 +75,38 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines, force: bool = False) -> str:
+    """A separate copy of the library built with extra preprocessor defines
+    (e.g. test hooks): csrc/ compiled into _build_<name>/ and linked into
+    lib<name>.so beside libpa.so. The product library is not touched."""
+    out = os.path.join(HERE, f"lib{name}.so")
+    deps = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                        if f.endswith((".h", ".cuh"))]
+    if (not force and os.path.exists(out) and
+            all(os.path.getmtime(d) <= os.path.getmtime(out) for d in deps)):
+        return out
+    bdir = os.path.join(HERE, f"_build_{name}")
+    os.makedirs(bdir, exist_ok=True)
+    srcs = sources()
+
+    def comp(src):
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
+        cmd = [nvcc()] + ARCH + NVCC_FLAGS + list(defines) + ["-c", src, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+        objs = list(ex.map(comp, srcs))
+    tmp = out + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs,
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stderr}")
+    os.replace(tmp, out)
+    return out
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -41,6 +41,16 @@
 #include "pa_internal.h"
 #include "ptx.cuh"
 
+#ifdef PA_TEST_HOOKS
+// Test builds only (-DPA_TEST_HOOKS): the balanced kernel's first worker
+// skips issuing the copy of its k-th block when k == g_test_skip_copy, so
+// that the wait for that block runs out and the kernel reports it.
+__device__ int g_test_skip_copy = -1;
+extern "C" pa_status pa_test_skip_copy(int k) {
+    return pa::cuda_status(cudaMemcpyToSymbol(g_test_skip_copy, &k, sizeof k), "test hook");
+}
+#endif
+
 namespace {
 
 constexpr int kBS = 16;                  // tokens per block
@@ -398,6 +408,9 @@ __global__ void __launch_bounds__(kWorkerWarps * 32, 3)
     auto issue = [&](int k) {   // warp-uniform
         if (k >= win + 32) refresh(k & ~31);
         const int row = __shfl_sync(0xffffffffu, my_row, k - win);
+#ifdef PA_TEST_HOOKS
+        if (wid == 0 && k == g_test_skip_copy) return;   // this block's wait will run out
+#endif
         if (lane == 0)
             issue_tile<D>(ring + (k % S) * Lay::kStage, bars + 8 * (k % S), &tmap_k, &tmap_v,
                           row, pol);

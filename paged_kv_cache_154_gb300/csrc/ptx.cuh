@@ -8,7 +8,12 @@
 
 namespace pa {
 
-constexpr unsigned long long kWaitNs = 200000000ull;  // 200 ms
+// How long a wait may last before it gives up: 200 ms (a test build of the
+// library sets a shorter limit with -DPA_WAIT_LIMIT_NS=...).
+#ifndef PA_WAIT_LIMIT_NS
+#define PA_WAIT_LIMIT_NS 200000000ull
+#endif
+constexpr unsigned long long kWaitNs = PA_WAIT_LIMIT_NS;
 // error-word bits that mean "some wait already gave up": every other wait
 // that finds one of them set stops spinning at once
 constexpr unsigned int kAbortMask = 0x7u;

@@ -12,6 +12,12 @@ import paged_kv_cache_154_gb300 as pa
 from paged_kv_cache_154_gb300.engine import PagedKVCache
 
 TOL = {"f16": 2e-3, "bf16": 2e-3, "int8": 1e-2, "fp8": 2e-3}   # max abs error on attention outputs
+# Regression guards, far below the tolerances: the kernels' errors on these
+# inputs are about 1e-6 (16-bit), 1e-4 (FP8) and 2e-4 (INT8); a guard about
+# 10x above that catches a kernel that got worse, or a dropped key block,
+# long before the tolerance would. Scaled by the largest |output| where that
+# exceeds 1 (inputs with a wide value range).
+GUARD = {"f16": 1e-4, "bf16": 1e-4, "int8": 2e-3, "fp8": 5e-4}
 THREADS = os.cpu_count() or 1
 
 
@@ -56,7 +62,7 @@ def check_cache_bits(ref, cache):
             raise AssertionError(f"cache differs at {bad.size} bytes, first at byte {bad[0]}")
 
 
-def check_out(ref, out, kv_dtype, out_dtype=torch.float32):
+def check_out(ref, out, kv_dtype, out_dtype=torch.float32, guard=True):
     got = out.double().cpu().numpy()
     err = np.abs(got - ref.out)
     tol = TOL[kv_dtype]
@@ -65,4 +71,7 @@ def check_out(ref, out, kv_dtype, out_dtype=torch.float32):
         assert (err <= bound).all(), f"max excess {(err - bound).max():.3e}"
     else:
         assert err.max() <= tol, f"max abs error {err.max():.3e} > {tol}"
+        if guard:
+            g = GUARD[kv_dtype] * max(1.0, float(np.abs(ref.out).max()))
+            assert err.max() <= g, f"max abs error {err.max():.3e} above the regression guard {g:.1e}"
     return float(err.max())

@@ -46,6 +46,28 @@ def test_small_shapes(case):
     check_out(ref, out, dt)
 
 
+def test_comparison_detects_a_dropped_block():
+    """The comparison sees a kernel that skips one block: the CUDA side gets a
+    valid but different input -- one sequence's length 16 tokens short, its
+    block table unchanged -- and its output must fail against the oracle's
+    full-length result (and stay equal to it elsewhere)."""
+    wl = W.simple("dropped_block", 99, [300, 1000, 700], [1, 1, 1], 32, 8, 128, "bf16")
+    ref, cache, si, out = run_both(wl)
+    check_out(ref, out, "bf16")
+    short = si.context_lens.clone()
+    short[1] -= 16
+    out2 = torch.empty_like(si.out)
+    pa.decode(out2, si.q, cache.k, cache.v, si.block_tables, short, si.max_context_len, wl.scale,
+              None, 1, cache.num_blocks, workspace=si.workspace)
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+    with pytest.raises(AssertionError):
+        check_out(ref, out2, "bf16")
+    # sequences 0 and 2 (one query token each) are untouched
+    err_other = np.abs(out2.double().cpu().numpy()[[0, 2]] - ref.out[[0, 2]]).max()
+    assert err_other <= 1e-4, err_other
+
+
 def test_tiny_config():
     wl = W.tiny()
     ref, cache, si, out = run_both(wl)
