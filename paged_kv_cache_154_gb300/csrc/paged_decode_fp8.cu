@@ -55,11 +55,24 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// two E4M3 codes (low byte first) -> f16x2 (low half first), exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    const __half2_raw h =
-        __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// two E4M3 codes (low byte first) -> f16x2 (low half first), exact: the
+// low / high 16 bits of a word, one conversion instruction each (the 16-bit
+// halves of a register are read in place)
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(d)
+        : "r"(w));
+    return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, hi;\n\t}"
+        : "=r"(d)
+        : "r"(w));
+    return d;
 }
 
 __device__ __forceinline__ float exp2i(int e) {   // 2^e for e in [-126, 127]
@@ -318,8 +331,8 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
             // rr[j]: k-step 2pp + j/2, tokens (j & 1) * 8 + quad, dims 4qc .. 4qc + 3
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                mma_f16(s[j & 1], qa[2 * pp + (j >> 1)], e4m3x2_to_f16x2(rr[j]),
-                        e4m3x2_to_f16x2(rr[j] >> 16));
+                mma_f16(s[j & 1], qa[2 * pp + (j >> 1)], e4m3x2_lo_to_f16x2(rr[j]),
+                        e4m3x2_hi_to_f16x2(rr[j]));
         }
 
         // ---- scales, mask, online softmax (lazy max) ----
@@ -405,11 +418,16 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int c = 2 * pp + half;
-                const uint32_t u0 = rr[2 * half] & keep0, u1 = rr[2 * half + 1] & keep1;
-                mma_f16(o[2 * c], pa_, e4m3x2_to_f16x2(prmt(u0, 0, 0x0020)),
-                        e4m3x2_to_f16x2(prmt(u1, 0, 0x0020)));
-                mma_f16(o[2 * c + 1], pa_, e4m3x2_to_f16x2(prmt(u0, 0, 0x0031)),
-                        e4m3x2_to_f16x2(prmt(u1, 0, 0x0031)));
+                uint32_t u0 = rr[2 * half], u1 = rr[2 * half + 1];
+                if (valid < kBS) {        // the sequence's last block only
+                    u0 &= keep0;
+                    u1 &= keep1;
+                }
+                // one prmt per pair of words: (t, dim a) and (t + 1, dim a) into the low
+                // half, (t, dim b) and (t + 1, dim b) into the high half
+                const uint32_t w0 = prmt(u0, u1, 0x3120), w1 = prmt(u0, u1, 0x7564);
+                mma_f16(o[2 * c], pa_, e4m3x2_lo_to_f16x2(w0), e4m3x2_lo_to_f16x2(w1));
+                mma_f16(o[2 * c + 1], pa_, e4m3x2_hi_to_f16x2(w0), e4m3x2_hi_to_f16x2(w1));
             }
         }
         __syncwarp();
