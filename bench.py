@@ -573,6 +573,13 @@ def measure_e2e(wl, cache, si, names, steps):
     out_h = torch.empty(si.out.shape, dtype=si.out.dtype).pin_memory()
     out_d = torch.empty_like(si.out)
     stream = torch.cuda.current_stream()
+    # the sequences grow by their query run every step: the pool must have room
+    free_blocks = cache.pool.stats()[0]
+    need = sum(((warm + steps) * r + 15) // 16 + 1 for r in q_lens)
+    if need > free_blocks:
+        return {"value": None, "unit": "GB/s",
+                "note": f"pool has {free_blocks} free blocks, {warm + steps} growing steps need "
+                        f"{need}: not measured for this workload"}
     kv_elem = 1 if wl.kv_dtype in ("int8", "fp8") else 2
     per_tok = 2 * wl.num_kv_heads * wl.head_dim * kv_elem + (
         2 * wl.num_kv_heads * 5 if wl.kv_dtype == "int8" else 0)
