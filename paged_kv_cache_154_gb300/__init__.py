@@ -331,6 +331,10 @@ def decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
 
 
 NO_ALLOC_WORKSPACE_BYTES = 40 << 20
+# Arrival counters at the start of every decode workspace (three regions of
+# one uint32 per worker, 2048 workers at most): zero before a buffer's first
+# call, left zero by every call.
+ARRIVAL_BYTES = 3 * 4 * 2048
 
 
 def decode_no_alloc(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,

@@ -151,6 +151,7 @@ def test_device_calls_reject_bad_arguments_on_the_host():
 def test_workspace_size():
     # every workspace starts with 6144 uint32 arrival counters (24576 bytes)
     arr = 24576
+    assert arr == pa.ARRIVAL_BYTES
     # partitioned schedule: o, m, l per (q token, head, partition)
     assert pa.decode_workspace_size(64, 64, 32, 8, 128, 1, 512, 512) == 0
     n = pa.decode_workspace_size(4, 4, 32, 8, 128, 1, 131072, 512)

@@ -13,7 +13,7 @@ import paged_kv_cache_154_gb300 as pa
 from gpu_harness import check_cache_bits, check_out, run_both, THREADS
 
 pytestmark = pytest.mark.gpu
-ARRIVAL_BYTES = 24576         # 6144 uint32 arrival counters at the start of every workspace
+ARRIVAL_BYTES = pa.ARRIVAL_BYTES   # the counters at the start of every workspace
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -191,10 +191,10 @@ def test_empty_inputs_are_no_ops():
 def _written_slots(ws: torch.Tensor, wl, max_q_len: int):
     """Partial slots of the balanced schedule that the last call wrote (the
     workspace past its arrival counters was filled with 0xFF first, so
-    unwritten headers read -1). Layout: 6144 uint32 arrival counters, prefix
+    unwritten headers read -1). Layout: the counters, prefix
     sums (num_seqs + 1 int32, 256-byte aligned), then slots of a 32-byte
     header {seq, kv head, chunk, first token, end token} and fp32 m[RT],
-    l[RT], O[RT][d]."""
+    l[RT], O[RT][d]; each entry ends with the slot's index."""
     G = wl.num_heads // wl.num_kv_heads
     rt = 16 if G * max_q_len <= 16 else 64          # rows per tile of the 16-bit kernels
     slot_bytes = (32 + 4 * rt * (wl.head_dim + 2) + 15) // 16 * 16
@@ -208,7 +208,7 @@ def _written_slots(ws: torch.Tensor, wl, max_q_len: int):
             continue
         f = b[32:32 + 4 * rt * (2 + wl.head_dim)].view(np.float32)
         m, l, o = f[:rt], f[rt:2 * rt], f[2 * rt:].reshape(rt, wl.head_dim)
-        out.append((tuple(int(x) for x in hdr[:5]), rt, m, l, o))
+        out.append((tuple(int(x) for x in hdr[:5]), rt, m, l, o, i))
     return out
 
 
@@ -250,7 +250,7 @@ def test_balanced_partials_match_oracle(case):
     G = wl.num_heads // wl.num_kv_heads
     qsl = wl.query_start_loc
     per_range = {}    # the oracle over one sequence's keys [t0, t1), all heads
-    for (s, g, c, t0, t1), rt, m, l, o in slots:
+    for (s, g, c, t0, t1), rt, m, l, o, _ in slots:
         L = wl.context_lens[s]
         assert 0 <= t0 < t1 <= L and t0 % 16 == 0
         q0, q1 = int(qsl[s]), int(qsl[s + 1])

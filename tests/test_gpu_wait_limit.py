@@ -54,7 +54,7 @@ def test_wait_that_runs_out_is_reported_and_the_next_call_is_correct(test_lib, m
     assert not code & (pa.DEVERR_BAD_BLOCK | pa.DEVERR_BAD_SLOT), hex(code)
     # hook off, counters zeroed again: the same call is correct
     assert test_lib.pa_test_skip_copy(-1) == 0
-    si.workspace[:24576].zero_()
+    si.workspace[:pa.ARRIVAL_BYTES].zero_()
     got.fill_(float("nan"))
     pa.decode(got, *args, workspace=si.workspace)
     torch.cuda.synchronize()
