@@ -1282,6 +1282,8 @@ pa_status launch_decode_int8(const DecodeArgs& a);
 pa_status launch_decode_fp8(const DecodeArgs& a);
 bool prefill_tc_applies(const DecodeArgs& a);
 pa_status launch_prefill_tc(const DecodeArgs& a);
+bool prefix_tc_applies(const DecodeArgs& a);
+pa_status launch_prefix_tc(const DecodeArgs& a);
 
 pa_status launch_decode(const DecodeArgs& a) {
     if ((a.ctx_start || a.lse_out || a.unmasked) &&
@@ -1292,6 +1294,7 @@ pa_status launch_decode(const DecodeArgs& a) {
     if (a.kv_dtype == PA_INT8) return launch_decode_int8(a);
     if (a.kv_dtype == PA_FP8_E4M3) return launch_decode_fp8(a);
     if (prefill_tc_applies(a)) return launch_prefill_tc(a);
+    if (prefix_tc_applies(a)) return launch_prefix_tc(a);
     if (a.partition_size > kMaxPartBlocks * kBS)
         return fail(PA_ERR_UNSUPPORTED, "partition_size %d > %d", a.partition_size,
                     kMaxPartBlocks * kBS);

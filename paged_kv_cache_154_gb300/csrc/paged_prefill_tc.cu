@@ -58,22 +58,35 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyMax = 8.f;
 
 // shared memory (offsets from a 1024-byte aligned base)
-constexpr int kStages = 4;                      // K/V ring
 constexpr int kQBytes = 32 * 1024;              // one Q tile: [2 sub][128 rows][128 B]
 constexpr int kQOff = 0;
-constexpr int kKVOff = kQTiles * kQBytes;       // kStages x (K 16 KB, V 16 KB)
-constexpr int kKVStage = 32 * 1024;
+constexpr int kKVStage = 32 * 1024;             // a K/V stage: K 16 KB, V 16 KB
 constexpr int kKBytes = 16 * 1024;              // [2 sub][64 rows][128 B]
 constexpr int kSubKV = 8 * 1024;                // one 64-dim half of a K (or V) tile
-constexpr int kBarOff = kKVOff + kStages * kKVStage;   // mbarriers and flags
-constexpr int kSmem = kBarOff + 256 + 1024;     // + alignment slack
-// barrier slots: K/V full and empty per stage; per (Q tile x, S buffer b):
-// S full and P full (index 2x + b); per Q tile: O done and the final drain of
-// its MMA warp; V rows past the context zeroed (single use)
-constexpr int kBarKVFull = 0, kBarKVEmpty = kStages, kBarSFull = 2 * kStages,
-              kBarPFull = 2 * kStages + 4, kBarODone = 2 * kStages + 8, kBarFin = 2 * kStages + 10,
-              kBarVZero = 2 * kStages + 12;
-constexpr int kNumBars = 2 * kStages + 13;
+
+// The two modes of the kernel. Prefill (kSplit false): two Q tiles of
+// different rows over the same keys, each K/V tile read by both, a ring of
+// 4 stages. Split keys (kSplit true, the prefix phase of shared-prefix
+// decode): one Q tile of at most 128 rows whose two MMA / softmax pipelines
+// take two different key chunks, each with its own 3 stages of the ring
+// (the second Q tile's shared memory holds the extra stages).
+template <bool kSplit>
+struct TcLayout {
+    static constexpr int kStages = kSplit ? 6 : 4;
+    static constexpr int kPerTile = kSplit ? 3 : 4;     // stages a Q tile's stream cycles through
+    static constexpr int kKVOff = (kSplit ? 1 : kQTiles) * kQBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kKVStage;   // mbarriers and flags
+    static constexpr int kSmem = kBarOff + 256 + 1024;            // + alignment slack
+    // barrier slots: K/V full and empty per stage; per (Q tile x, S buffer
+    // b): S full and P full (index 2x + b); per Q tile: O done and the final
+    // drain of its MMA warp; V rows past the context zeroed (single use)
+    static constexpr int kBarKVFull = 0, kBarKVEmpty = kStages, kBarSFull = 2 * kStages,
+                         kBarPFull = 2 * kStages + 4, kBarODone = 2 * kStages + 8,
+                         kBarFin = 2 * kStages + 10, kBarVZero = 2 * kStages + 12;
+    static constexpr int kNumBars = 2 * kStages + 13;
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+    static_assert(8 * kNumBars + 16 <= 256, "barrier area");
+};
 // TMEM columns (512): O of Q tile x at 128x; two S buffers per Q tile at
 // 256 + 128x + 64b. P of a tile is written over the S buffer it came from
 // (P_hi in its first 32 columns, P_lo in the next 32, two 16-bit values per
@@ -99,6 +112,15 @@ struct PrefillParams {
     float scale_log2;
     int out_f32;
     const int32_t* order;   // task of each CTA, longest first (null: natural order)
+    // split-key mode: CTA i takes chunks 2 j and 2 j + 1 of (sequence, kv
+    // head) i mod (S x H_kv), j = i / (S x H_kv), each chunk_tiles key tiles,
+    // every key visible to every row; each chunk's (m, l, O) goes to partial
+    // slot (sequence x H_kv + kv head) x 2 x pairs + chunk
+    int chunk_tiles;
+    int pairs;
+    uint8_t* slots;
+    int slot_bytes;
+    int slot_rows;
 };
 
 // A task: rows task_off .. task_off + task_rows - 1 of (sequence s, kv head g)
@@ -260,11 +282,17 @@ struct Cvt<__half> {
     }
 };
 
-template <typename T>
+template <typename T, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
     using C = Cvt<T>;
+    using LY = TcLayout<kSplit>;
+    constexpr int kStages = LY::kStages, kPerTile = LY::kPerTile, kKVOff = LY::kKVOff,
+                  kBarOff = LY::kBarOff, kNumBars = LY::kNumBars;
+    constexpr int kBarKVFull = LY::kBarKVFull, kBarKVEmpty = LY::kBarKVEmpty,
+                  kBarSFull = LY::kBarSFull, kBarPFull = LY::kBarPFull,
+                  kBarODone = LY::kBarODone, kBarFin = LY::kBarFin, kBarVZero = LY::kBarVZero;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = pa::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -278,24 +306,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     pa::grid_dependents_launch();
     pa::grid_dependency_wait();
 
-    // task of this CTA: longest first when ordered, else later chunks (longer
-    // key ranges) first
-    const int ntask = p.max_tasks * p.num_seqs * p.num_kv_heads;
-    const Task tk = task_of(p, p.order ? __ldg(p.order + blockIdx.x) : ntask - 1 - (int)blockIdx.x);
-    const int s = tk.s, g = tk.g, L = tk.L, q0 = tk.q0, r = tk.r;
+    // The task of this CTA. Prefill: 256 rows of one (sequence, kv head),
+    // longest first when ordered, else later chunks (longer key ranges)
+    // first; Q tile x holds rows 128 x of the task and both read key tiles
+    // 0 .. tiles - 1. Split keys: all rows of one (sequence, kv head) in Q
+    // tile 0; the stream of Q tile x is key chunk 2 j + x, tiles first[x] ..
+    // first[x] + cnt[x] - 1.
+    int s, g, L, q0, r, task_off, task_rows, end_blocks, tiles, pair = 0;
+    int first0 = 0, first1 = 0, cnt0 = 0, cnt1 = 0;   // (registers, not an indexed array)
+    if constexpr (kSplit) {
+        const int sh = p.num_seqs * p.num_kv_heads;
+        pair = (int)blockIdx.x / sh;
+        s = ((int)blockIdx.x % sh) / p.num_kv_heads;
+        g = ((int)blockIdx.x % sh) % p.num_kv_heads;
+        L = __ldg(p.context_lens + s);
+        if (p.qsl) {
+            q0 = __ldg(p.qsl + s);
+            r = __ldg(p.qsl + s + 1) - q0;
+        } else {
+            q0 = s;
+            r = 1;
+        }
+        task_off = 0;
+        task_rows = min(p.slot_rows, p.group * r);
+        end_blocks = (L + kBS - 1) / kBS;
+        tiles = (end_blocks + kTileBlocks - 1) / kTileBlocks;
+        first0 = 2 * pair * p.chunk_tiles;
+        first1 = first0 + p.chunk_tiles;
+        cnt0 = max(0, min(p.chunk_tiles, tiles - first0));
+        cnt1 = max(0, min(p.chunk_tiles, tiles - first1));
+        if (cnt0 == 0) return;                                   // uniform over the CTA
+    } else {
+        const int ntask = p.max_tasks * p.num_seqs * p.num_kv_heads;
+        const Task tk =
+            task_of(p, p.order ? __ldg(p.order + blockIdx.x) : ntask - 1 - (int)blockIdx.x);
+        s = tk.s;
+        g = tk.g;
+        L = tk.L;
+        q0 = tk.q0;
+        r = tk.r;
+        task_off = tk.task_off;
+        task_rows = tk.task_rows;
+        end_blocks = tk.end_blocks;
+        tiles = tk.tiles;
+        cnt0 = cnt1 = tiles;
+    }
+    auto first_of = [&](int x) { return x ? first1 : first0; };
+    auto cnt_of = [&](int x) { return x ? cnt1 : cnt0; };
     const int G = p.group;
-    const int task_off = tk.task_off, task_rows = tk.task_rows;
     if (task_rows <= 0) return;                                  // uniform over the CTA
-    const int nq = task_rows > kRows ? 2 : 1;                    // Q tiles with rows
-    const int end_blocks = tk.end_blocks, tiles = tk.tiles;
+    // Q tiles with work: prefill, those holding rows; split keys, those with a chunk
+    const int nq = kSplit ? (cnt1 > 0 ? 2 : 1) : (task_rows > kRows ? 2 : 1);
+    // ring stage and parity of the u-th tile of Q tile x's stream
+    auto stage_of = [&](int x, int u) { return kSplit ? x * kPerTile + u % kPerTile : u % kStages; };
+    auto phase_of = [&](int u) { return (u / kPerTile) & 1; };
 
     if (threadIdx.x == 0) {
         // P full and V zeroed take one arrival from each of the four warps of
         // a softmax group; K/V empty one commit from each Q tile's MMA warp
+        // that reads the stage (both in prefill, the owner with split keys)
         for (int i = 0; i < kNumBars; ++i)
             pa::mbar_init(bars + 8 * i, ((i >= kBarPFull && i < kBarODone) || i == kBarVZero) ? 4
-                                        : (i >= kBarKVEmpty && i < kBarKVEmpty + kStages) ? nq
-                                                                                            : 1);
+                                        : (i >= kBarKVEmpty && i < kBarKVEmpty + kStages)
+                                            ? (kSplit ? 1 : nq)
+                                            : 1);
         *abort_flag = 0;
         pa::fence_barrier_init();
         pa::prefetch_tensormap(&tmap_k);
@@ -306,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pa::tc::tmem_relinquish();
     }
     // Q tiles: 128 rows x 128 dims each, 128-byte swizzled K-major (two 64-dim halves)
-    for (int e = threadIdx.x; e < nq * kRows * 16; e += kThreads) {
+    for (int e = threadIdx.x; e < (kSplit ? 1 : nq) * kRows * 16; e += kThreads) {
         const int trow = e >> 4, ch = e & 15;          // task row 0..255
         uint4 v = make_uint4(0, 0, 0, 0);
         if (trow < task_rows) {
@@ -330,8 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ---------------- producer: K/V blocks of each tile ----------------
-        // lane j handles block j of a tile; the block ids of the next tile are
-        // fetched before waiting for the stage
+        // lane j handles block j of a tile
         auto block_row = [&](int t) {
             const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
             if (t >= tiles || lane >= nblk) return -1;
@@ -342,21 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return (blk * p.num_kv_heads + g) * kBS;
         };
-        int issued = 0;
-        int row = block_row(0);
-        for (int t = 0; t < tiles; ++t) {
-            const int st = t % kStages;
-            const int next_row = block_row(t + 1);
-            if (t >= kStages) {   // the stage is free once every product reading tile t - kStages is done
-                const bool ok = __all_sync(
-                    0xffffffffu,
-                    pa::mbar_wait(bars + 8 * (kBarKVEmpty + st), ((t / kStages) - 1) & 1, p.err,
-                                  pa::ERR_WAIT_EMPTY));
-                if (!ok || *abort_flag) {
-                    if (lane == 0) *abort_flag = 1;
-                    break;
-                }
-            }
+        auto load_tile = [&](int t, int st, int row) {
             const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
             const uint32_t bar = bars + 8 * (kBarKVFull + st);
             if (lane == 0) pa::mbar_arrive_expect_tx(bar, nblk * 4 * (kBS * 128));
@@ -369,27 +428,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pa::tma_load_2d(kst + kKBytes + sub * kSubKV, &tmap_v, sub * 64, row, bar);
                 }
             }
-            row = next_row;
-            issued = t + 1;
-        }
-        // drain: no copy may be in flight when the CTA ends; the last kStages
-        // issued tiles are waited once more (each completes whether or not it
-        // was consumed; earlier ones were consumed before their stage was reused)
-        if (lane == 0)
-            for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
-                if (!pa::mbar_wait(bars + 8 * (kBarKVFull + t % kStages), (t / kStages) & 1,
-                                   nullptr, 0)) {
-                    if (p.err) atomicOr(p.err, pa::ERR_WAIT_DRAIN);
-                    break;
+        };
+        // a stage is free once every product reading its previous tile is done
+        auto stage_free = [&](int st, int u) {
+            const bool ok = __all_sync(
+                0xffffffffu, pa::mbar_wait(bars + 8 * (kBarKVEmpty + st), ((u / kPerTile) - 1) & 1,
+                                           p.err, pa::ERR_WAIT_EMPTY));
+            if (!ok || *abort_flag) {
+                if (lane == 0) *abort_flag = 1;
+                return false;
+            }
+            return true;
+        };
+        int issued0 = 0, issued1 = 0;
+        if constexpr (kSplit) {
+            // the two chunks' streams interleaved, each through its own stages
+            bool go = true;
+            for (int u = 0; go && u < max(cnt0, cnt1); ++u)
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    if (!go || u >= cnt_of(x)) continue;
+                    const int st = stage_of(x, u);
+                    if (u >= kPerTile && !stage_free(st, u)) {
+                        go = false;
+                        continue;
+                    }
+                    load_tile(first_of(x) + u, st, block_row(first_of(x) + u));
+                    if (x) issued1 = u + 1;
+                    else issued0 = u + 1;
                 }
+        } else {
+            // the block ids of the next tile are fetched before waiting for the stage
+            int row = block_row(0);
+            for (int t = 0; t < tiles; ++t) {
+                const int st = t % kStages;
+                const int next_row = block_row(t + 1);
+                if (t >= kStages && !stage_free(st, t)) break;
+                load_tile(t, st, row);
+                row = next_row;
+                issued0 = t + 1;
+            }
+        }
+        // drain: no copy may be in flight when the CTA ends; the last kPerTile
+        // issued tiles of each stream are waited once more (each completes
+        // whether or not it was consumed; earlier ones were consumed before
+        // their stage was reused)
+        if (lane == 0)
+            for (int x = 0; x < (kSplit ? 2 : 1); ++x) {
+                const int iss = x ? issued1 : issued0;
+                for (int u = iss > kPerTile ? iss - kPerTile : 0; u < iss; ++u)
+                    if (!pa::mbar_wait(bars + 8 * (kBarKVFull + stage_of(x, u)), phase_of(u),
+                                       nullptr, 0)) {
+                        if (p.err) atomicOr(p.err, pa::ERR_WAIT_DRAIN);
+                        break;
+                    }
+            }
     } else if (warp == 1 || warp == 2 + 4 * kQTiles) {
         // ---------------- MMA issue: one warp per Q tile (one elected lane issues) ----------------
-        // S is double-buffered: QK_x(t) writes buffer t & 1 once PV_x(t - 2),
-        // which read P_x(t - 2) from it, has completed. Order per key tile t:
-        // PV_x(t), then QK_x(t + 2). Each Q tile has its own issuing warp, so the
-        // waits and bookkeeping of one overlap the products of the other on
-        // the shared tensor pipe. Operands are made warp-uniform (read from
-        // lane 0) so the issue stays a converged, uniform instruction stream.
+        // S is double-buffered: QK_x(u) writes buffer u & 1 once PV_x(u - 2),
+        // which read P_x(u - 2) from it, has completed. Order per key tile u
+        // of the stream: PV_x(u), then QK_x(u + 2). Each Q tile has its own
+        // issuing warp, so the waits and bookkeeping of one overlap the
+        // products of the other on the shared tensor pipe. Operands are made
+        // warp-uniform (read from lane 0) so the issue stays a converged,
+        // uniform instruction stream.
         const int x = warp == 1 ? 0 : 1;
         const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
         const uint32_t sb = __shfl_sync(0xffffffffu, base, 0);
@@ -403,29 +505,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // descriptors of every operand start: a descriptor of address a + o is
         // the one of a plus o >> 4 (the 14-bit address field does not overflow
-        // inside shared memory)
-        const uint64_t dq = pa::tc::smem_desc_sw128(sb + kQOff + x * kQBytes, 16, 1024);
+        // inside shared memory); with split keys both Q tiles read Q tile 0
+        const uint64_t dq = pa::tc::smem_desc_sw128(sb + kQOff + (kSplit ? 0 : x) * kQBytes, 16, 1024);
         const uint64_t dk = pa::tc::smem_desc_sw128(sb + kKVOff, 16, 1024);
         const uint64_t dv = pa::tc::smem_desc_sw128(sb + kKVOff + kKBytes, kSubKV, 1024);
         const uint32_t s_col = tm + kSCol + 128 * x, o_col = tm + 128 * x;
-        auto issue_qk = [&](int t) {   // S_x[t & 1] = Q_x K(t)^T
+        auto issue_qk = [&](int u) {   // S_x[u & 1] = Q_x K(u)^T
             pa::tc::fence_after_sync();
-            const uint64_t b0 = dk + (uint64_t)(((t % kStages) * kKVStage) >> 4);
-            const uint32_t d = s_col + 64 * (t & 1);
+            const uint64_t b0 = dk + (uint64_t)((stage_of(x, u) * kKVStage) >> 4);
+            const uint32_t d = s_col + 64 * (u & 1);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t qa = ((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4;
                 const uint32_t kb = ((kk >> 2) * kSubKV + (kk & 3) * 32) >> 4;
                 pa::tc::mma_f16_ss_warp(d, dq + qa, b0 + kb, idesc_qk, kk > 0 ? 1u : 0u);
             }
-            pa::tc::commit_warp(bb + 8 * (kBarSFull + 2 * x + (t & 1)));
+            pa::tc::commit_warp(bb + 8 * (kBarSFull + 2 * x + (u & 1)));
         };
-        auto issue_pv = [&](int t) {   // O_x += P_x(t) V(t)
+        auto issue_pv = [&](int u) {   // O_x += P_x(u) V(u)
             pa::tc::fence_after_sync();
-            const uint64_t v0 = dv + (uint64_t)(((t % kStages) * kKVStage) >> 4);
-            const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
-            const uint32_t pc = s_col + 64 * (t & 1);
-            const uint32_t acc0 = t > 0 ? 1u : 0u;
+            const uint64_t v0 = dv + (uint64_t)((stage_of(x, u) * kKVStage) >> 4);
+            const int nblk = min(kTileBlocks, end_blocks - (first_of(x) + u) * kTileBlocks);
+            const uint32_t pc = s_col + 64 * (u & 1);
+            const uint32_t acc0 = u > 0 ? 1u : 0u;
 #pragma unroll
             for (int kb = 0; kb < kTileBlocks; ++kb) {
                 if (kb < nblk) {
@@ -436,28 +538,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pa::tc::commit_warp(bb + 8 * (kBarODone + x));
         };
-        auto kv_ready = [&](int t) { return wait(bb + 8 * (kBarKVFull + t % kStages), (t / kStages) & 1); };
-        // the last tile may hold V rows past the context, which Q tile 0's
-        // softmax zeroes before its P of that tile is ready
-        const int zero_tile = end_blocks * kBS > L ? tiles - 1 : -1;
+        auto kv_ready = [&](int u) {
+            return wait(bb + 8 * (kBarKVFull + stage_of(x, u)), phase_of(u));
+        };
+        // prefill: the last tile may hold V rows past the context, which Q
+        // tile 0's softmax zeroes before its P of that tile is ready (with
+        // split keys the tile's own softmax group does it before its P)
+        const int zero_tile = !kSplit && end_blocks * kBS > L ? tiles - 1 : -1;
+        const int n = cnt_of(x);
         bool ok = x < nq;
         if (ok) {
             // both S buffers start free: the products of S for tiles 0 and 1
-            for (int t = 0; ok && t < min(tiles, 2); ++t) {
-                ok = kv_ready(t);
-                if (ok) issue_qk(t);
+            for (int u = 0; ok && u < min(n, 2); ++u) {
+                ok = kv_ready(u);
+                if (ok) issue_qk(u);
             }
-            for (int t = 0; ok && t < tiles; ++t) {
-                ok = wait(bb + 8 * (kBarPFull + 2 * x + (t & 1)), (t >> 1) & 1);
-                if (ok && x == 1 && t == zero_tile) ok = wait(bb + 8 * kBarVZero, 0);
+            for (int u = 0; ok && u < n; ++u) {
+                ok = wait(bb + 8 * (kBarPFull + 2 * x + (u & 1)), (u >> 1) & 1);
+                if (ok && x == 1 && u == zero_tile) ok = wait(bb + 8 * kBarVZero, 0);
                 if (!ok) break;
-                issue_pv(t);
-                // every product of this Q tile reading K/V tile t has been issued
-                pa::tc::commit_warp(bb + 8 * (kBarKVEmpty + t % kStages));
-                if (t + 2 < tiles) {
-                    // PV_x(t) read S_x[t & 1]
-                    ok = kv_ready(t + 2) && wait(bb + 8 * (kBarODone + x), t & 1);
-                    if (ok) issue_qk(t + 2);
+                issue_pv(u);
+                // every product of this Q tile reading K/V tile u has been issued
+                pa::tc::commit_warp(bb + 8 * (kBarKVEmpty + stage_of(x, u)));
+                if (u + 2 < n) {
+                    // PV_x(u) read S_x[u & 1]
+                    ok = kv_ready(u + 2) && wait(bb + 8 * (kBarODone + x), u & 1);
+                    if (ok) issue_qk(u + 2);
                 }
             }
             if (!ok && lane == 0) *abort_flag = 1;
@@ -472,26 +578,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int x = (warp - 2) / 4;
         const int lane_base = 32 * (warp & 3);
         const int row = lane_base + lane;                    // tile row = TMEM lane
-        const int row_off = task_off + x * kRows;
-        const int rows = min(kRows, task_rows - x * kRows);
+        const int row_off = kSplit ? 0 : task_off + x * kRows;
+        const int rows = kSplit ? task_rows : min(kRows, task_rows - x * kRows);
         const int gr = row_off + row;
         const bool valid = row < rows;
         const int jq = valid ? gr / G : 0;
-        // keys past a row's bound are masked; padding rows (Q = 0) need no mask
-        const int bound = valid ? min(L - r + jq, L - 1) : 0x7fffffff;
+        // keys past a row's bound are masked; padding rows (Q = 0) need no
+        // mask; with split keys every key before L is visible to every row
+        const int bound = kSplit ? L - 1 : valid ? min(L - r + jq, L - 1) : 0x7fffffff;
         // the smallest bound of the tile's rows: tiles ending at or before it need no mask
-        const int bound_min = min(L - r + row_off / G, L - 1);
+        const int bound_min = kSplit ? L - 1 : min(L - r + row_off / G, L - 1);
         const uint32_t trow = tmem + ((uint32_t)lane_base << 16);
         const uint32_t s_tm = trow + kSCol + 128 * x, o_tm = trow + 128 * x;
         const uint32_t bar_odone = bars + 8 * (kBarODone + x);
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         const int grp_tid = (warp - 2 - 4 * x) * 32 + lane;  // 0..127 within the group
+        const int n = cnt_of(x);
         int done = 0;
-        for (int t = 0; t < tiles; ++t) {
-            const int b = t & 1;                               // S / P buffer of this tile
+        for (int u = 0; u < n; ++u) {
+            const int b = u & 1;                               // S / P buffer of this tile
             bool ok = __all_sync(0xffffffffu, pa::mbar_wait(bars + 8 * (kBarSFull + 2 * x + b),
-                                                            (t >> 1) & 1, p.err, pa::ERR_WAIT_FULL));
+                                                            (u >> 1) & 1, p.err, pa::ERR_WAIT_FULL));
             if (!ok || *abort_flag) {
                 if (lane == 0) *abort_flag = 1;
                 break;
@@ -499,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pa::tc::fence_after_sync();
             float sv[kTok];
             pa::tc::ld_64cols(s_tm + 64 * b, *reinterpret_cast<uint32_t(*)[64]>(sv));
+            const int t = first_of(x) + u;                     // key tile
             const int tok0 = t * kTok;
             if (tok0 + kTok - 1 > bound_min) {               // a tile some row must not see all of
 #pragma unroll
@@ -509,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 4; j < kTok; j += 8)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) m4[u] = max3(m4[u], sv[j + 2 * u], sv[j + 2 * u + 1]);
+                for (int q = 0; q < 4; ++q) m4[q] = max3(m4[q], sv[j + 2 * q], sv[j + 2 * q + 1]);
             float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             mx = mx == -INFINITY ? mx : mx * sl2;            // the scale is positive
             float alpha = 1.f;
@@ -536,11 +645,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[64];
 #pragma unroll
             for (int j = 0; j < kTok / 2; ++j) C::split(sv[2 * j], sv[2 * j + 1], pk[j], pk[32 + j]);
-            // O_x may be rescaled once the P V product of tile t - 1 is done
+            // O_x may be rescaled once the P V product of tile u - 1 is done
             // (rare: the running max moves by more than 2^8 after the first tile)
-            if (t >= 1 && __any_sync(0xffffffffu, moved)) {
+            if (u >= 1 && __any_sync(0xffffffffu, moved)) {
                 ok = __all_sync(0xffffffffu,
-                                pa::mbar_wait(bar_odone, (t - 1) & 1, p.err, pa::ERR_WAIT_FULL));
+                                pa::mbar_wait(bar_odone, (u - 1) & 1, p.err, pa::ERR_WAIT_FULL));
                 if (!ok || *abort_flag) {
                     if (lane == 0) *abort_flag = 1;
                     break;
@@ -559,15 +668,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P over the S buffer it came from (this thread's row only)
             pa::tc::st_64cols(s_tm + 64 * b, pk);
             // V rows past the context (in the sequence's last block) may hold
-            // anything: zero them so that P = 0 never meets a NaN (Q tile 0's
-            // group does it and signals Q tile 1's MMA warp)
+            // anything: zero them so that P = 0 never meets a NaN (prefill: Q
+            // tile 0's group does it and signals Q tile 1's MMA warp; split
+            // keys: the one stream holding that tile)
             const int nblk = min(kTileBlocks, end_blocks - t * kTileBlocks);
             const int tok_end = tok0 + nblk * kBS;
-            if (x == 0 && L < tok_end) {
+            if ((kSplit || x == 0) && L < tok_end) {
                 const int z0 = L - tok0, zrows = tok_end - L;      // local token rows to zero
                 for (int e = grp_tid; e < zrows * 16; e += 128) {
                     const int lr = z0 + e / 16, ch = e % 16;
-                    const uint32_t dst = base + kKVOff + (t % kStages) * kKVStage + kKBytes +
+                    const uint32_t dst = base + kKVOff + stage_of(x, u) * kKVStage + kKBytes +
                                          (ch >> 3) * kSubKV + lr * 128 + ((ch & 7) << 4);
                     asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u)
                                  : "memory");
@@ -580,39 +690,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 pa::mbar_arrive(bars + 8 * (kBarPFull + 2 * x + b));
                 // Q tile 1's product of this tile reads the zeroed rows
-                if (x == 0 && L < tok_end) pa::mbar_arrive(bars + 8 * kBarVZero);
+                if (!kSplit && x == 0 && L < tok_end) pa::mbar_arrive(bars + 8 * kBarVZero);
             }
-            done = t + 1;
+            done = u + 1;
         }
-        // epilogue: O / l for this row
-        if (done == tiles && tiles > 0) {
+        // epilogue: O / l for this row (prefill), or the chunk's partial (m, l, O)
+        if (done == n && n > 0) {
             // the last two P V products, in order (a parity wait tells apart
             // only neighbouring phases of the barrier)
             bool ok = true;
-            for (int t = tiles >= 2 ? tiles - 2 : 0; ok && t < tiles; ++t)
+            for (int u = n >= 2 ? n - 2 : 0; ok && u < n; ++u)
                 ok = __all_sync(0xffffffffu,
-                                pa::mbar_wait(bar_odone, t & 1, p.err, pa::ERR_WAIT_FULL));
+                                pa::mbar_wait(bar_odone, u & 1, p.err, pa::ERR_WAIT_FULL));
             if (ok) {
                 pa::tc::fence_after_sync();
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                const int64_t orow =
-                    valid ? ((int64_t)(q0 + gr / G) * p.num_heads + g * G + gr % G) : 0;
-#pragma unroll
-                for (int qd = 0; qd < D / 32; ++qd) {
-                    float ov[32];
-                    pa::tc::ld_32cols(o_tm + 32 * qd, ov);
+                if constexpr (kSplit) {
+                    const int64_t slot =
+                        ((int64_t)s * p.num_kv_heads + g) * 2 * p.pairs + 2 * pair + x;
+                    uint8_t* const sp = p.slots + slot * (int64_t)p.slot_bytes;
+                    float* const sm_ = reinterpret_cast<float*>(sp + 32);
+                    float* const sl_ = sm_ + p.slot_rows;
+                    float* const so = sl_ + p.slot_rows;
                     if (valid) {
-                        if (p.out_f32) {
-                            float* dst = static_cast<float*>(p.out) + orow * D + 32 * qd;
+                        sm_[row] = m_run;
+                        sl_[row] = l_run;
+                    }
+#pragma unroll
+                    for (int qd = 0; qd < D / 32; ++qd) {
+                        float ov[32];
+                        pa::tc::ld_32cols(o_tm + 32 * qd, ov);
+                        if (valid) {
+                            float* dst = so + (int64_t)row * D + 32 * qd;
 #pragma unroll
                             for (int i = 0; i < 32; i += 4)
                                 *reinterpret_cast<float4*>(dst + i) =
-                                    make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv,
-                                                ov[i + 3] * inv);
-                        } else {
-                            T* dst = static_cast<T*>(p.out) + orow * D + 32 * qd;
+                                    make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+                        }
+                    }
+                } else {
+                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                    const int64_t orow =
+                        valid ? ((int64_t)(q0 + gr / G) * p.num_heads + g * G + gr % G) : 0;
 #pragma unroll
-                            for (int i = 0; i < 32; i += 2) C::store2(dst + i, ov[i] * inv, ov[i + 1] * inv);
+                    for (int qd = 0; qd < D / 32; ++qd) {
+                        float ov[32];
+                        pa::tc::ld_32cols(o_tm + 32 * qd, ov);
+                        if (valid) {
+                            if (p.out_f32) {
+                                float* dst = static_cast<float*>(p.out) + orow * D + 32 * qd;
+#pragma unroll
+                                for (int i = 0; i < 32; i += 4)
+                                    *reinterpret_cast<float4*>(dst + i) =
+                                        make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv,
+                                                    ov[i + 3] * inv);
+                            } else {
+                                T* dst = static_cast<T*>(p.out) + orow * D + 32 * qd;
+#pragma unroll
+                                for (int i = 0; i < 32; i += 2)
+                                    C::store2(dst + i, ov[i] * inv, ov[i + 1] * inv);
+                            }
                         }
                     }
                 }
@@ -627,22 +763,103 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) pa::tc::tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T>
+// Split keys: merges the key chunks of every (sequence, kv head) row, one
+// warp per (sequence, kv head, row) item, into the normalised fp32 output
+// row and its base-2 log-sum-exp, by the log-sum-exp rule: out = sum 2^(m_c
+// - M) O_c / sum 2^(m_c - M) l_c. A sequence with no key writes nothing.
+__global__ void __launch_bounds__(128) prefix_chunk_reduce_kernel(const PrefillParams p,
+                                                                  float* lse_out) {
+    constexpr int EPL = D / 32;
+    pa::grid_dependency_wait();     // every chunk's partial is written
+    pa::grid_dependents_launch();
+    const int lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int row = (int)(item % p.slot_rows);
+    const int64_t seg = item / p.slot_rows;
+    if (seg >= (int64_t)p.num_seqs * p.num_kv_heads) return;
+    const int s = (int)(seg / p.num_kv_heads), g = (int)(seg % p.num_kv_heads);
+    int q0 = s, r = 1;
+    if (p.qsl) {
+        q0 = __ldg(p.qsl + s);
+        r = __ldg(p.qsl + s + 1) - q0;
+    }
+    const int G = p.group;
+    if (row >= min(p.slot_rows, G * r)) return;
+    const int L = __ldg(p.context_lens + s);
+    const int tiles = ((L + kBS - 1) / kBS + kTileBlocks - 1) / kTileBlocks;
+    const int nch = min(2 * p.pairs, (tiles + p.chunk_tiles - 1) / p.chunk_tiles);
+    if (nch <= 0) return;
+    float M = -INFINITY, den = 0.f, acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    for (int c = 0; c < nch; ++c) {
+        const uint8_t* sp = p.slots + (seg * 2 * p.pairs + c) * (int64_t)p.slot_bytes;
+        const float* m = reinterpret_cast<const float*>(sp + 32);
+        const float l = __ldg(m + p.slot_rows + row);
+        if (!(l > 0.f)) continue;
+        const float mc = __ldg(m + row);
+        const float4 o = __ldg(reinterpret_cast<const float4*>(m + 2 * p.slot_rows +
+                                                               (int64_t)row * D + lane * EPL));
+        const float Mn = fmaxf(M, mc);
+        const float a = exp2f(M - Mn), w = exp2f(mc - Mn);
+        den = den * a + w * l;
+        acc[0] = acc[0] * a + w * o.x;
+        acc[1] = acc[1] * a + w * o.y;
+        acc[2] = acc[2] * a + w * o.z;
+        acc[3] = acc[3] * a + w * o.w;
+        M = Mn;
+    }
+    if (!(den > 0.f)) return;
+    const int64_t orow = (int64_t)(q0 + row / G) * p.num_heads + g * G + row % G;
+    const float inv = 1.f / den;
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D + lane * EPL) =
+        make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    if (lane == 0) lse_out[orow] = M + log2f(den);
+}
+
+template <typename T, bool kSplit>
 pa_status launch(const pa::DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                  const PrefillParams& prm, int64_t grid) {
-    auto kern = paged_prefill_tc_kernel<T>;
+    auto kern = paged_prefill_tc_kernel<T, kSplit>;
+    constexpr int smem = TcLayout<kSplit>::kSmem;
     static bool attr_set = false;   // per instantiation; benign race (idempotent)
     if (!attr_set) {
         if (pa_status s = pa::cuda_status(
-                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem),
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                 "prefill: set shared memory size"))
             return s;
         attr_set = true;
     }
     return pa::cuda_status(
-        pa::launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmem, a.stream, mk, mv, prm),
+        pa::launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, a.stream, mk, mv, prm),
         "prefill launch");
 }
+
+PrefillParams base_params(const pa::DecodeArgs& a) {
+    PrefillParams prm{};
+    prm.out = a.out;
+    prm.q = a.q;
+    prm.block_tables = a.block_tables;
+    prm.context_lens = a.context_lens;
+    prm.qsl = a.query_start_loc;
+    prm.err = pa::device_error_word();
+    prm.max_blocks = a.max_blocks_per_seq;
+    prm.num_heads = a.num_heads;
+    prm.num_kv_heads = a.num_kv_heads;
+    prm.group = a.num_heads / a.num_kv_heads;
+    prm.num_seqs = a.num_seqs;
+    prm.num_blocks = a.num_blocks;
+    prm.scale_log2 = a.scale * kLog2e;
+    prm.out_f32 = a.out_dtype == PA_F32;
+    return prm;
+}
+
+// Split keys: key tiles per chunk at least this many (shorter chunks would
+// spend more on the per-chunk prologue and the partials than they save)
+constexpr int kMinChunkTiles = 8;
+// rows of a split-key task (the partial slots of the balanced schedule's
+// 64-row tiles hold them)
+constexpr int kSplitRows = 64;
 
 }  // namespace
 
@@ -666,22 +883,8 @@ pa_status launch_prefill_tc(const DecodeArgs& a) {
         return s;
     if (pa_status s = cache_tensor_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
         return s;
-    PrefillParams prm{};
-    prm.out = a.out;
-    prm.q = a.q;
-    prm.block_tables = a.block_tables;
-    prm.context_lens = a.context_lens;
-    prm.qsl = a.query_start_loc;
-    prm.err = device_error_word();
-    prm.max_blocks = a.max_blocks_per_seq;
-    prm.num_heads = a.num_heads;
-    prm.num_kv_heads = a.num_kv_heads;
-    prm.group = G;
-    prm.num_seqs = a.num_seqs;
-    prm.num_blocks = a.num_blocks;
+    PrefillParams prm = base_params(a);
     prm.max_tasks = (int)max_tasks;
-    prm.scale_log2 = a.scale * kLog2e;
-    prm.out_f32 = a.out_dtype == PA_F32;
     // the task order goes to the start of the balanced schedule's workspace
     // (the caller sized it with pa_decode_workspace_size, 256-byte aligned)
     const BalancedShape ws = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim,
@@ -694,8 +897,60 @@ pa_status launch_prefill_tc(const DecodeArgs& a) {
                 "prefill order launch"))
             return s;
     }
-    if (a.kv_dtype == PA_BF16) return launch<__nv_bfloat16>(a, mk, mv, prm, grid);
-    return launch<__half>(a, mk, mv, prm, grid);
+    if (a.kv_dtype == PA_BF16) return launch<__nv_bfloat16, false>(a, mk, mv, prm, grid);
+    return launch<__half, false>(a, mk, mv, prm, grid);
+}
+
+// The prefix phase of shared-prefix decode over a 16-bit cache with
+// head_dim 128: every key visible to every row (no causal offset), a
+// log-sum-exp per row, 17 to 64 rows per (group, kv head), long prefixes.
+bool prefix_tc_applies(const DecodeArgs& a) {
+    const int64_t rows = (int64_t)(a.num_heads / a.num_kv_heads) * a.max_q_len;
+    return (a.kv_dtype == PA_BF16 || a.kv_dtype == PA_F16) && a.head_dim == 128 &&
+           a.partition_size == 0 && !a.ctx_start && a.lse_out && a.unmasked &&
+           a.out_dtype == PA_F32 && rows > 16 && rows <= kSplitRows &&
+           a.max_context_len >= 2 * kMinChunkTiles * kTok;
+}
+
+// Split keys: (group, kv head) tasks cut into key chunks so that the CTAs
+// (one per SM) about fill the GPU, then the chunks merged per row.
+pa_status launch_prefix_tc(const DecodeArgs& a) {
+    int dev = 0, sms = 0;
+    if (pa_status s = pa::cuda_status(cudaGetDevice(&dev), "cudaGetDevice")) return s;
+    if (pa_status s = pa::cuda_status(
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count"))
+        return s;
+    const int64_t segs = (int64_t)a.num_seqs * a.num_kv_heads;
+    const int64_t tiles_max = ((a.max_context_len + kBS - 1) / kBS + kTileBlocks - 1) / kTileBlocks;
+    const int64_t pairs_by_len = std::max<int64_t>(1, tiles_max / (2 * kMinChunkTiles));
+    const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(sms / segs, pairs_by_len));
+    const int64_t chunk_tiles = (tiles_max + 2 * pairs - 1) / (2 * pairs);
+    const int64_t grid = segs * pairs;
+    // the partials go to the balanced schedule's slots (64-row tiles) of this workspace
+    const BalancedShape ws = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim,
+                                            a.max_q_len, a.max_context_len);
+    if (!a.slots || ws.rows_per_tile != kSplitRows || segs * 2 * pairs > 2 * ws.workers ||
+        grid > 0x7fffffff)
+        return fail(PA_ERR_UNSUPPORTED, "prefix phase: workspace too small for the key chunks");
+    CUtensorMap mk, mv;
+    if (pa_status s = cache_tensor_map(&mk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
+        return s;
+    if (pa_status s = cache_tensor_map(&mv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, 2))
+        return s;
+    PrefillParams prm = base_params(a);
+    prm.chunk_tiles = (int)chunk_tiles;
+    prm.pairs = (int)pairs;
+    prm.slots = static_cast<uint8_t*>(a.slots) + ws.cum_bytes;
+    prm.slot_bytes = (int)ws.slot_bytes;
+    prm.slot_rows = kSplitRows;
+    pa_status st = a.kv_dtype == PA_BF16 ? launch<__nv_bfloat16, true>(a, mk, mv, prm, grid)
+                                         : launch<__half, true>(a, mk, mv, prm, grid);
+    if (st != PA_OK) return st;
+    const int64_t items = segs * kSplitRows;
+    return pa::cuda_status(
+        pa::launch_pdl(prefix_chunk_reduce_kernel, dim3((unsigned)((items + 3) / 4)), dim3(128),
+                       0, a.stream, prm, a.lse_out),
+        "prefix chunk reduce launch");
 }
 
 }  // namespace pa

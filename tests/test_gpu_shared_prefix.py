@@ -48,6 +48,20 @@ CASES = {
                                                  prompt_len=4096, shared_extra_max=15,
                                                  private_max=64, num_heads=32, num_kv_heads=8,
                                                  head_dim=128),
+    # 16-bit caches with d 128 and 17-64 rows per (group, kv head) over long
+    # prefixes take the tensor-core prefix phase: key chunks of each (group,
+    # kv head) in two streams per CTA, merged per row afterwards. Prefixes of
+    # 1,100-2,000 tokens: one chunk pair, some groups with one chunk only;
+    # fp16, verify runs of 1-2 (24-48 rows)
+    "tc_prefix_ragged": lambda: W.best_of_n("sp_tc_ragged", 77, num_groups=3, n_forks=3,
+                                            prompt_len=1100, shared_extra_max=900,
+                                            private_max=40, num_heads=16, num_kv_heads=2,
+                                            head_dim=128, kv_dtype="f16", step_q_max=2),
+    # 4,096-token prefixes over 16 (group, kv head) tasks: four chunk pairs each
+    "tc_prefix_chunks": lambda: W.best_of_n("sp_tc_chunks", 78, num_groups=8, n_forks=5,
+                                            prompt_len=4096, shared_extra_max=15,
+                                            private_max=64, num_heads=16, num_kv_heads=2,
+                                            head_dim=128),
     # a prompt that fills its last block: forks share every prompt block
     "block_aligned_prompt": lambda: W.best_of_n("sp_aligned", 75, num_groups=2, n_forks=3,
                                                 prompt_len=255, shared_extra_max=1,
