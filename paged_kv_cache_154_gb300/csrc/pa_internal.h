@@ -130,6 +130,7 @@ struct DecodeArgs {
     const int32_t* ctx_start;  // [num_seqs] first attended token, a multiple of 16
     float* lse_out;            // [num_q_tokens][num_heads] base-2 log-sum-exp per output row
     int unmasked;              // every query row sees every key < context_len
+    int max_workers;           // balanced 16-bit decode: at most this many worker warps (0: none)
     cudaStream_t stream;
 };
 pa_status launch_decode(const DecodeArgs& a);

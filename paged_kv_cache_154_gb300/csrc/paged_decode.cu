@@ -1198,7 +1198,8 @@ pa_status launch_balanced(const pa::DecodeArgs& a, const CUtensorMap& mk, const 
     if (ctas < 1) return pa::fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
     const pa::BalancedShape shape = pa::balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads,
                                                        a.head_dim, a.max_q_len, a.max_context_len);
-    const int64_t workers = std::min<int64_t>((int64_t)ctas * sms * kWorkerWarps, shape.workers);
+    int64_t workers = std::min<int64_t>((int64_t)ctas * sms * kWorkerWarps, shape.workers);
+    if (a.max_workers > 0) workers = std::min<int64_t>(workers, a.max_workers);
     prm.workers = (int)workers;
     // The in-kernel merge pays off when shares are long. When a call can
     // hold fewer than 8 blocks per worker (a small call), the merges'

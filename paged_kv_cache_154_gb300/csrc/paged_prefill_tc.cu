@@ -78,8 +78,10 @@ struct TcLayout {
     static constexpr int kBarOff = kKVOff + kStages * kKVStage;   // mbarriers and flags
     static constexpr int kSmem = kBarOff + 256 + 1024;            // + alignment slack
     // barrier slots: K/V full and empty per stage; per (Q tile x, S buffer
-    // b): S full and P full (index 2x + b); per Q tile: O done and the final
-    // drain of its MMA warp; V rows past the context zeroed (single use)
+    // b): S full and P full (index 2x + b); per Q tile: O done (one phase
+    // per P V product) and the final commit of its MMA warp (one phase: every
+    // product done, which the epilogue waits for); V rows past the context
+    // zeroed (single use)
     static constexpr int kBarKVFull = 0, kBarKVEmpty = kStages, kBarSFull = 2 * kStages,
                          kBarPFull = 2 * kStages + 4, kBarODone = 2 * kStages + 8,
                          kBarFin = 2 * kStages + 10, kBarVZero = 2 * kStages + 12;
@@ -696,12 +698,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // epilogue: O / l for this row (prefill), or the chunk's partial (m, l, O)
         if (done == n && n > 0) {
-            // the last two P V products, in order (a parity wait tells apart
-            // only neighbouring phases of the barrier)
-            bool ok = true;
-            for (int u = n >= 2 ? n - 2 : 0; ok && u < n; ++u)
-                ok = __all_sync(0xffffffffu,
-                                pa::mbar_wait(bar_odone, u & 1, p.err, pa::ERR_WAIT_FULL));
+            // every product of this Q tile is done: the MMA warp's final
+            // commit, a barrier with one phase in the CTA's life. (Waiting for
+            // the last P V products on the O-done barrier by parity is not
+            // safe: if the last one completes before the wait for the one
+            // before it is observed, the barrier is two phases on and that
+            // parity names a phase that never completes.)
+            bool ok = __all_sync(0xffffffffu, pa::mbar_wait(bars + 8 * (kBarFin + x), 0, p.err,
+                                                            pa::ERR_WAIT_FULL));
             if (ok) {
                 pa::tc::fence_after_sync();
                 if constexpr (kSplit) {
@@ -913,7 +917,24 @@ bool prefix_tc_applies(const DecodeArgs& a) {
 }
 
 // Split keys: (group, kv head) tasks cut into key chunks so that the CTAs
-// (one per SM) about fill the GPU, then the chunks merged per row.
+// (one per SM) about fill the GPU: chunk pairs per task and key tiles per chunk.
+static void split_shape(const DecodeArgs& a, int sms, int64_t* pairs, int64_t* chunk_tiles) {
+    const int64_t segs = (int64_t)a.num_seqs * a.num_kv_heads;
+    const int64_t tiles_max = ((a.max_context_len + kBS - 1) / kBS + kTileBlocks - 1) / kTileBlocks;
+    const int64_t pairs_by_len = std::max<int64_t>(1, tiles_max / (2 * kMinChunkTiles));
+    *pairs = std::max<int64_t>(1, std::min<int64_t>(sms / segs, pairs_by_len));
+    *chunk_tiles = (tiles_max + 2 * *pairs - 1) / (2 * *pairs);
+}
+
+// CTAs of the split-key launch for these arguments (0 where it does not apply).
+int64_t prefix_tc_ctas(const DecodeArgs& a, int sms) {
+    if (!prefix_tc_applies(a)) return 0;
+    int64_t pairs = 0, chunk_tiles = 0;
+    split_shape(a, sms, &pairs, &chunk_tiles);
+    return (int64_t)a.num_seqs * a.num_kv_heads * pairs;
+}
+
+// Split keys, then the chunks merged per row.
 pa_status launch_prefix_tc(const DecodeArgs& a) {
     int dev = 0, sms = 0;
     if (pa_status s = pa::cuda_status(cudaGetDevice(&dev), "cudaGetDevice")) return s;
@@ -921,10 +942,8 @@ pa_status launch_prefix_tc(const DecodeArgs& a) {
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count"))
         return s;
     const int64_t segs = (int64_t)a.num_seqs * a.num_kv_heads;
-    const int64_t tiles_max = ((a.max_context_len + kBS - 1) / kBS + kTileBlocks - 1) / kTileBlocks;
-    const int64_t pairs_by_len = std::max<int64_t>(1, tiles_max / (2 * kMinChunkTiles));
-    const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(sms / segs, pairs_by_len));
-    const int64_t chunk_tiles = (tiles_max + 2 * pairs - 1) / (2 * pairs);
+    int64_t pairs = 0, chunk_tiles = 0;
+    split_shape(a, sms, &pairs, &chunk_tiles);
     const int64_t grid = segs * pairs;
     // the partials go to the balanced schedule's slots (64-row tiles) of this workspace
     const BalancedShape ws = balanced_shape(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim,

@@ -25,10 +25,15 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
 #include "pa_internal.h"
 #include "ptx.cuh"
+
+namespace pa {
+int64_t prefix_tc_ctas(const DecodeArgs& a, int sms);
+}
 
 namespace {
 
@@ -130,6 +135,48 @@ __global__ void __launch_bounds__(128)
             static_cast<__nv_bfloat16*>(out)[base + e] = __float2bfloat16_rn(x);
         }
     }
+}
+
+// A second stream of this device and two events: the suffix phase runs on
+// it beside the prefix phase when the prefix phase leaves SMs free (its
+// tensor-core kernel holds one CTA per SM). Created once per device, kept
+// for the life of the process; the fork and the join are stream-ordered
+// event records and waits, which graph capture turns into edges.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+// held from an event record to the wait that reads it, so calls from
+// several host threads do not interleave their records
+std::mutex& side_mutex() {
+    static std::mutex mu;
+    return mu;
+}
+
+pa_status side_stream(SideStream* out) {
+    static std::mutex mu;
+    static std::vector<SideStream> per_device;
+    int dev = 0;
+    if (pa_status s = pa::cuda_status(cudaGetDevice(&dev), "cudaGetDevice")) return s;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)per_device.size() <= dev) per_device.resize(dev + 1);
+    SideStream& ss = per_device[dev];
+    if (!ss.stream) {
+        SideStream t;
+        if (pa_status s = pa::cuda_status(
+                cudaStreamCreateWithFlags(&t.stream, cudaStreamNonBlocking), "side stream"))
+            return s;
+        if (pa_status s = pa::cuda_status(
+                cudaEventCreateWithFlags(&t.fork, cudaEventDisableTiming), "side stream event"))
+            return s;
+        if (pa_status s = pa::cuda_status(
+                cudaEventCreateWithFlags(&t.join, cudaEventDisableTiming), "side stream event"))
+            return s;
+        ss = t;
+    }
+    *out = ss;
+    return PA_OK;
 }
 
 // Workspace: the arrival counters (kept zero; the two phases use them one
@@ -327,6 +374,26 @@ extern "C" pa_status pa_decode_shared_prefix(
     a.lse_out = lse_a;
     a.unmasked = 1;
     a.stream = st;
+    // With the prefix phase on the tensor-core kernel (one CTA per SM, SMs
+    // to spare), the suffix phase runs beside it on the side stream, with
+    // its workers capped to the free SMs (three CTAs of four warps each).
+    int dev = 0, sms = 0;
+    if (pa_status s = pa::cuda_status(cudaGetDevice(&dev), "cudaGetDevice")) return s;
+    if (pa_status s = pa::cuda_status(
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count"))
+        return s;
+    const int64_t tc_ctas = pa::prefix_tc_ctas(a, sms);
+    const int64_t free_sms = sms - tc_ctas;
+    SideStream side{};
+    const bool beside = tc_ctas > 0 && free_sms >= sms / 16;
+    if (beside) {
+        if (pa_status s = side_stream(&side)) return s;
+        std::lock_guard<std::mutex> lock(side_mutex());
+        if (pa_status s = pa::cuda_status(cudaEventRecord(side.fork, st), "fork record")) return s;
+        if (pa_status s = pa::cuda_status(cudaStreamWaitEvent(side.stream, side.fork, 0),
+                                          "fork wait"))
+            return s;
+    }
     if (pa_status s = pa::launch_decode(a)) return s;
 
     // phase 2: every sequence from the end of its group's prefix
@@ -344,7 +411,18 @@ extern "C" pa_status pa_decode_shared_prefix(
     a.ctx_start = ctx_start;
     a.lse_out = lse_b;
     a.unmasked = 0;
+    if (beside) {
+        a.stream = side.stream;
+        a.max_workers = (int)(free_sms * 3 * 4);
+    }
     if (pa_status s = pa::launch_decode(a)) return s;
+    if (beside) {   // the merge waits for the suffix phase
+        std::lock_guard<std::mutex> lock(side_mutex());
+        if (pa_status s = pa::cuda_status(cudaEventRecord(side.join, side.stream), "join record"))
+            return s;
+        if (pa_status s = pa::cuda_status(cudaStreamWaitEvent(st, side.join, 0), "join wait"))
+            return s;
+    }
 
     // phase 3: merge the two states of every row
     const unsigned grid = (unsigned)((rows + 3) / 4);

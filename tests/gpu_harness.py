@@ -49,7 +49,7 @@ def run_both(wl, partition_size=0, out_dtype=torch.float32, oracle_run=None,
     assert np.array_equal(si.context_lens.cpu().numpy(), ref.context_lens)
     out = cache.step(si, wl.scale, partition_size)
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     return ref, cache, si, out
 
 

@@ -60,7 +60,7 @@ def test_comparison_detects_a_dropped_block():
     pa.decode(out2, si.q, cache.k, cache.v, si.block_tables, short, si.max_context_len, wl.scale,
               None, 1, cache.num_blocks, workspace=si.workspace)
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     with pytest.raises(AssertionError):
         check_out(ref, out2, "bf16")
     # sequences 0 and 2 (one query token each) are untouched
@@ -241,7 +241,7 @@ def test_balanced_partials_match_oracle(case):
     si.workspace[:ARRIVAL_BYTES].zero_()
     cache.step(si, wl.scale, 0)
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     check_out(ref, si.out, "bf16")
     # the decode kernel's merges leave every arrival counter at zero
     assert not si.workspace[:ARRIVAL_BYTES].any()
@@ -311,7 +311,7 @@ def test_one_workspace_serves_calls_of_any_shape():
                       si.max_context_len, wl.scale, si.query_start_loc, si.max_q_len,
                       cache.num_blocks, workspace=big)
             torch.cuda.synchronize()
-            assert pa.device_error() == 0
+            assert (code := pa.device_error()) == 0, hex(code)
             check_out(ref, si.out, "bf16")
             assert not big[:ARRIVAL_BYTES].any()
 
@@ -335,7 +335,7 @@ def test_nonzero_arrival_counters_are_reported(fill):
     si.out.fill_(float("nan"))
     pa.decode(si.out, *args, workspace=si.workspace)
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     check_out(ref, si.out, "bf16")
     assert not si.workspace[:ARRIVAL_BYTES].any()
 
@@ -362,7 +362,7 @@ def test_writes_stay_inside_workspace_and_output(case):
               si.max_context_len, wl.scale, si.query_start_loc, si.max_q_len, cache.num_blocks,
               workspace=ws[:need])
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     check_out(ref, out[:nq], "bf16")
     assert bool((ws[need:] == 0xA5).all()), "bytes written past the workspace"
     assert bool(out[nq:].isnan().all()), "rows written past the output"
@@ -459,7 +459,7 @@ def test_graph_replay_matches_eager():
         g_write.replay()
         g_attend.replay()
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     assert torch.equal(si.out, eager)
     check_cache_bits(ref, cache)
 

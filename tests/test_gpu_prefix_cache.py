@@ -71,7 +71,7 @@ def test_second_request_reuses_the_system_prompt_blocks():
               torch.from_numpy(cl).cuda(), L, 1.0 / np.sqrt(D), num_blocks=cache.num_blocks,
               workspace=ws)
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     # the cache, read back, holds B's own K/V at B's positions (reused blocks included)
     host = oracle.empty_cache("bf16", cache.num_blocks, HKV, 16, D)
     host.k[...] = cache.k.view(torch.int16).cpu().numpy().view(np.uint16)

@@ -127,7 +127,7 @@ def test_raw_api_prefix_covering_a_whole_sequence():
                             torch.from_numpy(gs).to(dev), torch.from_numpy(pl).to(dev), 2, 64,
                             num_blocks=cache.num_blocks, workspace=ws)
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     o, _, _ = oracle.attend(q.double().numpy(), ref.cache, bt2, cl2, None, wl.num_heads,
                             wl.scale)
     assert np.abs(out.double().cpu().numpy() - o).max() <= 2e-3

@@ -58,5 +58,5 @@ def test_wait_that_runs_out_is_reported_and_the_next_call_is_correct(test_lib, m
     got.fill_(float("nan"))
     pa.decode(got, *args, workspace=si.workspace)
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     check_out(ref, got, "bf16")

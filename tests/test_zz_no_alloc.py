@@ -59,7 +59,7 @@ def _pair(wl, cache, si, q):
     pa.decode(ref, q, *args, partition_size=512, workspace=si.workspace)
     pa.decode_no_alloc(got, q, *args, partition_size=512)
     torch.cuda.synchronize()
-    assert pa.device_error() == 0
+    assert (code := pa.device_error()) == 0, hex(code)
     return ref, got
 
 
