@@ -35,7 +35,8 @@ PROFILES = {
     "llama3_8b": ("paged_decode_llama3_8b.md", _DEC16),
     "llama2_70b_best_of_5": ("paged_decode_llama2_70b_best_of_5.md", _DEC16),
     "llama2_70b_best_of_5+read_once": ("shared_prefix_llama2_70b_best_of_5.md",
-                                       _DEC16 + ("shared_prefix.cu",)),
+                                       _DEC16 + ("shared_prefix.cu", "paged_prefill_tc.cu",
+                                                 "tcgen05.cuh")),
     "long_context": ("paged_decode_long_context.md", _DEC16),
     "mixed_int8": ("paged_decode_int8_mixed.md", ("paged_decode_int8.cu", "balanced.cuh",
                                                   "ptx.cuh")),
@@ -275,13 +276,25 @@ def launches_per_step(si, partition_size, prefill_tc=False, kv_dtype="bf16", gro
     if si.pairs is not None:
         n += 1                                          # copy_blocks
     if si.shared is not None:
-        # prep, the prefix phase, the suffix phase, the merge of the two
-        return (n + 2 + decode_launches(group * si.shared.max_group_q_len)
-                + decode_launches(group * si.max_q_len))
+        # prep, the prefix phase (on the tensor cores: split-key kernel and
+        # chunk reduce), the suffix phase (always with its reduce kernel),
+        # the merge of the two
+        prefix = (2 if prefix_tc_runs(kv_dtype, si, group)
+                  else decode_launches(group * si.shared.max_group_q_len))
+        return n + 2 + prefix + 2
     if prefill_tc:
         return n + 2                                    # task order, tensor-core prefill
     return n + decode_launches(group * si.max_q_len, partition_size == 0,
                                si.max_context_len > partition_size)
+
+
+def prefix_tc_runs(kv_dtype, si, group, head_dim=128) -> bool:
+    """Does the read-once prefix phase run on the tensor-core kernel (16-bit
+    cache, head_dim 128, 17-64 rows per group and KV head, prefixes of at
+    least 1,024 tokens)?"""
+    rows = group * si.shared.max_group_q_len
+    return (kv_dtype in ("f16", "bf16") and head_dim == 128 and 16 < rows <= 64
+            and int(max(si.shared.prefix_len_host)) >= 1024)
 
 
 def roofline_kernel(wl, si, partition_size, prefill_tc):
@@ -296,9 +309,14 @@ def roofline_kernel(wl, si, partition_size, prefill_tc):
         return ("pa_decode (paged_prefill_tc_kernel: Q K^T and P V on the tcgen05 tensor "
                 "cores, accumulators in TMEM)")
     if si.shared is not None:
-        return (f"pa_decode_shared_prefix (prefix_prep_kernel, "
-                f"{balanced16(G * si.shared.max_group_q_len)} for the prefixes, "
-                f"{balanced16(G * si.max_q_len)} for the suffixes, prefix_merge_kernel)")
+        prefix = ("paged_prefill_tc_kernel in split-key mode (tcgen05, TMEM) + "
+                  "prefix_chunk_reduce_kernel" if prefix_tc_runs(wl.kv_dtype, si, G, wl.head_dim)
+                  else balanced16(G * si.shared.max_group_q_len))
+        suffix = ("paged_decode_balanced_kernel" if G * si.max_q_len <= 16
+                  else "paged_decode_rows_kernel") + " + segment_reduce_rows_kernel"
+        return (f"pa_decode_shared_prefix (prefix_prep_kernel, {prefix} for the prefixes, "
+                f"{suffix} for the suffixes on a second stream beside them, "
+                f"prefix_merge_kernel)")
     if wl.kv_dtype == "int8":
         return "pa_decode (paged_decode_int8_kernel + segment_reduce_kernel)"
     if wl.kv_dtype == "fp8":

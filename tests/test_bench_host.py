@@ -2,6 +2,7 @@
 kernel the roofline names, and the rule that a profile's recorded DRAM
 traffic is reported only for the workload and kernel source it was captured
 on."""
+import numpy as np
 import os
 import sys
 from types import SimpleNamespace
@@ -19,8 +20,8 @@ def _si(max_q_len=1, max_context_len=4096, pairs=None, shared=None):
                            shared=shared)
 
 
-def _wl(kv="bf16", H=32, Hkv=8):
-    return SimpleNamespace(kv_dtype=kv, num_heads=H, num_kv_heads=Hkv)
+def _wl(kv="bf16", H=32, Hkv=8, d=128):
+    return SimpleNamespace(kv_dtype=kv, num_heads=H, num_kv_heads=Hkv, head_dim=d)
 
 
 @pytest.mark.parametrize("kv, group, qlen, expect", [
@@ -41,9 +42,17 @@ def test_launches_with_copies_partitions_prefill_and_shared_prefix():
     assert bench.launches_per_step(_si(max_context_len=400), 512, False, "bf16", 4) == 2
     assert bench.launches_per_step(_si(), 0, True, "bf16", 4) == 3            # order + prefill
     # best-of-5 shape: 5 forks x 8 q heads per KV head in the prefix phase
-    # (64-row kernel + reduce), 8 rows in the suffix phase
-    sp = SimpleNamespace(max_group_q_len=5)
-    assert bench.launches_per_step(_si(shared=sp), 0, False, "bf16", 8) == 1 + 2 + 2 + 1
+    # (4,096-token prefixes: split-key tensor-core kernel + chunk reduce;
+    # short prefixes: 64-row kernel + reduce), 8 rows in the suffix phase
+    # (decode + reduce, on the second stream); prep and merge
+    sp = SimpleNamespace(max_group_q_len=5, prefix_len_host=np.array([4096] * 8))
+    assert bench.prefix_tc_runs("bf16", _si(shared=sp), 8)
+    assert bench.launches_per_step(_si(shared=sp), 0, False, "bf16", 8) == 1 + 2 + 2 + 2
+    short = SimpleNamespace(max_group_q_len=5, prefix_len_host=np.array([512] * 8))
+    assert not bench.prefix_tc_runs("bf16", _si(shared=short), 8)
+    assert bench.launches_per_step(_si(shared=short), 0, False, "bf16", 8) == 1 + 2 + 2 + 2
+    assert not bench.prefix_tc_runs("bf16", _si(shared=SimpleNamespace(
+        max_group_q_len=1, prefix_len_host=np.array([4096]))), 8)     # 8 rows: per-warp kernel
 
 
 def test_roofline_kernel_names_what_runs():
@@ -54,6 +63,9 @@ def test_roofline_kernel_names_what_runs():
     assert "fp8" in bench.roofline_kernel(_wl("fp8"), _si(), 0, False)
     assert "split_kv_reduce" in bench.roofline_kernel(_wl(), _si(), 512, False)
     assert "tcgen05" in bench.roofline_kernel(_wl(), _si(), 0, True)
+    sp = SimpleNamespace(max_group_q_len=5, prefix_len_host=np.array([4096] * 8))
+    name = bench.roofline_kernel(_wl(H=64), _si(shared=sp), 0, False)
+    assert "split-key" in name and "second stream" in name
 
 
 def test_recorded_traffic_only_for_the_profiled_workload():
