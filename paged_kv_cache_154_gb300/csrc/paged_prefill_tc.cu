@@ -597,6 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_run = -INFINITY, l_run = 0.f;
         const int grp_tid = (warp - 2 - 4 * x) * 32 + lane;  // 0..127 within the group
         const int n = cnt_of(x);
+        const bool live = lane_base < rows;                  // warp-uniform
         int done = 0;
         for (int u = 0; u < n; ++u) {
             const int b = u & 1;                               // S / P buffer of this tile
@@ -607,10 +608,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             pa::tc::fence_after_sync();
-            float sv[kTok];
-            pa::tc::ld_64cols(s_tm + 64 * b, *reinterpret_cast<uint32_t(*)[64]>(sv));
             const int t = first_of(x) + u;                     // key tile
             const int tok0 = t * kTok;
+            // A warp whose 32 rows are all padding (Q = 0: S, and so P, are
+            // zero in TMEM already) skips the softmax; it still waits for S
+            // and arrives on P full in order, which keeps the barrier phases.
+            if (live) {
+            float sv[kTok];
+            pa::tc::ld_64cols(s_tm + 64 * b, *reinterpret_cast<uint32_t(*)[64]>(sv));
             if (tok0 + kTok - 1 > bound_min) {               // a tile some row must not see all of
 #pragma unroll
                 for (int j = 0; j < kTok; ++j)
@@ -669,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // P over the S buffer it came from (this thread's row only)
             pa::tc::st_64cols(s_tm + 64 * b, pk);
+            }
             // V rows past the context (in the sequence's last block) may hold
             // anything: zero them so that P = 0 never meets a NaN (prefill: Q
             // tile 0's group does it and signals Q tile 1's MMA warp; split
@@ -697,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             done = u + 1;
         }
         // epilogue: O / l for this row (prefill), or the chunk's partial (m, l, O)
-        if (done == n && n > 0) {
+        if (live && done == n && n > 0) {
             // every product of this Q tile is done: the MMA warp's final
             // commit, a barrier with one phase in the CTA's life. (Waiting for
             // the last P V products on the O-done barrier by parity is not
