@@ -189,11 +189,11 @@ enum TileKind { kTile16Bit = 0, kTileInt8 = 1, kTileFp8 = 2 };
 
 // Query rows per tile: 16 while a KV head has at most 16 rows (G q heads x
 // the longest query run), else 64 for the 16-bit kernels (four warps of 16
-// rows share each block) and 32 for the INT8 kernel; the FP8 kernel always
-// uses 16 (one warp per tile, further rows as further chunks).
+// rows share each block); the INT8 and FP8 kernels always use 16 (one warp
+// per tile, further rows as further chunks).
 inline int tile_rows(int64_t rows, int kind) {
-    if (rows <= 16 || kind == kTileFp8) return 16;
-    return kind == kTileInt8 ? 32 : 64;
+    if (rows <= 16 || kind == kTileFp8 || kind == kTileInt8) return 16;
+    return 64;
 }
 
 // The workspace is sized for every kernel family: the worker cap from the

@@ -165,7 +165,7 @@ def test_workspace_size():
     slot64 = 32 + 4 * 16 * 66
     assert pa.decode_workspace_size(1, 1, 8, 2, 64, 1, 17, 0) == arr + 256 + 2 * (2 * 2) * slot64
     # 32 q heads on one KV head with verify runs of 5 (160 rows): slots sized for the
-    # 64-row tiles of the 16-bit kernels (the INT8 kernel's 32-row tiles fit in them)
+    # 64-row tiles of the 16-bit kernels (the INT8 and FP8 kernels use 16-row tiles)
     slot_big = 32 + 4 * 64 * 130
     assert pa.decode_workspace_size(256, 400, 32, 1, 128, 5, 16384, 0) == \
         arr + 1280 + 2 * 2048 * slot_big
