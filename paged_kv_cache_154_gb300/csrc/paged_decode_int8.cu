@@ -72,11 +72,11 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
     return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// fp16 pair (1152 + z0, 1152 + z1): subtracting it from (1024 + (code ^ 0x80))
-// leaves code - zp exactly.
-__device__ __forceinline__ uint32_t zp_bias(int z0, int z1) {
-    __half2 h = __halves2half2(__int2half_rn(1152 + z0), __int2half_rn(1152 + z1));
-    return *reinterpret_cast<uint32_t*>(&h);
+// fp16 pair (1152 + z_i, 1152 + z_j) for the zero points in bytes i and j of
+// the word zw: (z ^ 0x80) = z + 128 placed in the mantissa of 1024.0, as the
+// codes are. Subtracting it from (1024 + (code ^ 0x80)) leaves code - zp exactly.
+__device__ __forceinline__ uint32_t zp_pair(uint32_t zw, int i, int j) {
+    return prmt(zw ^ 0x80808080u, kMagic, 0x4040u | (uint32_t)i | ((uint32_t)j << 8));
 }
 
 // (code - zp) of the two code bytes in the low (sel 0x4140) or high (0x4342)
@@ -354,15 +354,16 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
         const uint8_t* sp = scales + st * kScaleBytes;
         const float* ksc = reinterpret_cast<const float*>(sp);
         const float* vsc = ksc + 16;
-        const int8_t* kzp = reinterpret_cast<const int8_t*>(sp + 128);
-        const int8_t* vzp = kzp + 16;
+        const uint32_t* kzw = reinterpret_cast<const uint32_t*>(sp + 128);   // 4 zero points a word
+        const uint32_t* vzw = kzw + 4;
         const int tok0 = cur.b * kBS;
         const int valid = L - tok0;   // tokens of this block inside the context (>= 1)
 
         // ---- S = Q (K codes - zp)^T over the block's 16 tokens (two n-tiles of 8) ----
         // the lane's K fragments hold tokens quad (n-tile 0) and 8 + quad (n-tile 1)
-        const uint32_t zk0 = zp_bias(kzp[quad], kzp[quad]);
-        const uint32_t zk1 = zp_bias(kzp[8 + quad], kzp[8 + quad]);
+        const int qb = quad & 3;
+        const uint32_t zk0 = zp_pair(kzw[quad >> 2], qb, qb);
+        const uint32_t zk1 = zp_pair(kzw[2 + (quad >> 2)], qb, qb);
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int pp = 0; pp < KCH / 2; ++pp) {
@@ -462,8 +463,9 @@ __global__ void __launch_bounds__(kWorkerWarps * 32)
 
         // ---- O += P' (V codes - zp) ----
         // the lane's V pairs: tokens 2qc, 2qc + 1 (b0) and 2qc + 8, 2qc + 9 (b1)
-        const uint32_t zv0 = zp_bias(vzp[t0], vzp[t0 + 1]);
-        const uint32_t zv1 = zp_bias(vzp[t0 + 8], vzp[t0 + 9]);
+        const int tb = t0 & 3;   // tokens t0, t0 + 1 are bytes tb, tb + 1 of word t0 / 4
+        const uint32_t zv0 = zp_pair(vzw[t0 >> 2], tb, tb + 1);
+        const uint32_t zv1 = zp_pair(vzw[2 + (t0 >> 2)], tb, tb + 1);
 #pragma unroll
         for (int pp = 0; pp < KCH / 2; ++pp) {
             uint32_t rr[4];
