@@ -559,19 +559,22 @@ def run_ours(args, rank, world, local):
 
 def measure_e2e(wl, cache, si, names, steps):
     """The same metric through the public API, as a user's decode loop runs
-    it, every step: the host pool reserves each sequence's new slots (its
-    copy-on-write pairs come back) and writes the block tables and lengths;
-    those, the step's q and new K/V rows are copied from pinned host memory
-    to the device; pa_copy_blocks (when there are pairs), pa_append_kv and
-    pa_decode run; the output is copied back to pinned host memory and the
-    stream synchronised. The sequences grow by their query run each step,
-    and each step's bytes are counted from its own lengths."""
+    it, every step: the host pool reserves the step's new slots in one call
+    (pa_seq_append_slots_batch; the copy-on-write pairs come back) and writes
+    the block tables and lengths; those, the step's q and new K/V rows are
+    packed in one pinned host buffer and copied to the device in one copy;
+    pa_copy_blocks (when there are pairs), pa_append_kv and pa_decode run;
+    the output is copied back to pinned host memory and the stream
+    synchronised. The sequences grow by their query run each step, and each
+    step's bytes are counted from its own lengths."""
     import numpy as np
     import torch
     import paged_kv_cache_154_gb300 as pa
     dev = si.q.device
     seqs = [names[op.seq] for op in wl.step]
     q_lens = [int(op.k.shape[0]) for op in wl.step]
+    seqs_np = np.asarray(seqs, np.int32)
+    q_lens_np = np.asarray(q_lens, np.int32)
     r_max = max(q_lens)
     T = sum(q_lens)
     warm = 3
@@ -580,13 +583,29 @@ def measure_e2e(wl, cache, si, names, steps):
     ws_bytes = pa.decode_workspace_size(len(seqs), T, wl.num_heads, wl.num_kv_heads,
                                         wl.head_dim, r_max, max_len_final, 0)
     ws = pa.zeroed_workspace(ws_bytes, dev)
-    # device inputs of fixed shape; pinned host staging buffers
-    h = {"q": si.q.cpu().pin_memory(), "key": si.key.cpu().pin_memory(),
-         "value": si.value.cpu().pin_memory(),
-         "slots": torch.empty(T, dtype=torch.int64).pin_memory(),
-         "bt": torch.empty((len(seqs), cap_blocks), dtype=torch.int32).pin_memory(),
-         "cl": torch.empty(len(seqs), dtype=torch.int32).pin_memory()}
-    d = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in h.items()}
+    # one pinned host staging buffer and one device buffer holding every
+    # input of a step, as typed views at 256-byte offsets
+    parts = [("slots", (T,), torch.int64), ("bt", (len(seqs), cap_blocks), torch.int32),
+             ("cl", (len(seqs),), torch.int32), ("q", tuple(si.q.shape), si.q.dtype),
+             ("key", tuple(si.key.shape), si.key.dtype),
+             ("value", tuple(si.value.shape), si.value.dtype)]
+    offs, total = {}, 0
+    for name, shape, dt in parts:
+        offs[name] = total
+        nb = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        total += (nb + 255) // 256 * 256
+    stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    stage_d = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(buf, name):
+        _, shape, dt = next(x for x in parts if x[0] == name)
+        nb = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        return buf[offs[name]:offs[name] + nb].view(dt).view(shape)
+
+    h = {name: view(stage_h, name) for name, _, _ in parts}
+    d = {name: view(stage_d, name) for name, _, _ in parts}
+    for name in ("q", "key", "value"):
+        h[name].copy_(getattr(si, name).cpu())
     qsl = si.query_start_loc            # fixed: the run lengths do not change
     out_h = torch.empty(si.out.shape, dtype=si.out.dtype).pin_memory()
     out_d = torch.empty_like(si.out)
@@ -602,29 +621,25 @@ def measure_e2e(wl, cache, si, names, steps):
     per_tok = 2 * wl.num_kv_heads * wl.head_dim * kv_elem + (
         2 * wl.num_kv_heads * 5 if wl.kv_dtype == "int8" else 0)
     fixed = T * wl.num_heads * wl.head_dim * (2 + 4) + T * per_tok
+    slots_np = h["slots"].numpy()
+    bt_np, cl_np = h["bt"].numpy(), h["cl"].numpy()
+    pr_h = torch.empty((len(seqs), 2), dtype=torch.int32).pin_memory()
+    pr_d = torch.empty((len(seqs), 2), dtype=torch.int32, device=dev)
     times, nbytes, h2d_last = [], 0, 0
     for k in range(warm + steps):
         t0 = time.perf_counter()
-        pairs, off = [], 0
-        slots_np = h["slots"].numpy()
-        for s, r in zip(seqs, q_lens):
-            sl, pair = cache.pool.seq_append_slots(s, r)
-            slots_np[off:off + r] = sl
-            off += r
-            if pair is not None:
-                pairs.append(pair)
-        bt, cl = cache.pool.block_tables(seqs, cap_blocks)
-        h["bt"].numpy()[:] = bt
-        h["cl"].numpy()[:] = cl
-        for name in h:
-            d[name].copy_(h[name], non_blocking=True)
-        h2d = sum(t.numel() * t.element_size() for t in h.values())
-        if pairs:
-            pr_h = torch.tensor(pairs, dtype=torch.int32).pin_memory()
-            pr = pr_h.to(dev, non_blocking=True)
-            h2d += pr_h.numel() * 4
-            pa.copy_blocks(cache.k, cache.v, pr, cache.num_blocks, cache.k_scale, cache.v_scale,
-                           cache.k_zp, cache.v_zp)
+        _, pairs = cache.pool.seq_append_slots_batch(seqs_np, q_lens_np, slots_out=slots_np)
+        bt, cl = cache.pool.block_tables(seqs_np, cap_blocks)
+        bt_np[:] = bt
+        cl_np[:] = cl
+        stage_d.copy_(stage_h, non_blocking=True)
+        h2d = total
+        if len(pairs):
+            pr_h[:len(pairs)] = torch.from_numpy(pairs)
+            pr_d[:len(pairs)].copy_(pr_h[:len(pairs)], non_blocking=True)
+            h2d += len(pairs) * 8
+            pa.copy_blocks(cache.k, cache.v, pr_d[:len(pairs)], cache.num_blocks, cache.k_scale,
+                           cache.v_scale, cache.k_zp, cache.v_zp)
         pa.append_kv(d["key"], d["value"], cache.k, cache.v, d["slots"], cache.num_blocks,
                      cache.k_scale, cache.v_scale, cache.k_zp, cache.v_zp)
         max_len = int(cl.max())
@@ -642,8 +657,9 @@ def measure_e2e(wl, cache, si, names, steps):
     return {"value": round(nbytes / sum(times) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d_last), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(1e3 * statistics.mean(times), 4), "steps": len(times),
-            "path": "host pool (pa_seq_append_slots, pa_pool_block_tables) + pinned H2D + "
-                    "pa_copy_blocks/pa_append_kv/pa_decode + D2H, per step"}
+            "path": "host pool (pa_seq_append_slots_batch, pa_pool_block_tables) + one pinned "
+                    "H2D copy of the step's inputs + pa_copy_blocks/pa_append_kv/pa_decode + D2H, "
+                    "per step"}
 
 
 def cpu_baseline(wl, budget_s=12.0, sample_seqs=None):

@@ -116,6 +116,18 @@ pa_status pa_seq_append_slots(pa_pool* pool, int32_t seq, int32_t n_tokens,
                               int64_t* slots_out, int32_t* cow_pair_out,
                               int32_t* n_cow);
 
+/* A decode step's reservations in one call: for i = 0 .. n-1 in order,
+ * pa_seq_append_slots(seqs[i], n_tokens[i]), its slots written contiguously
+ * to slots_out (sum of n_tokens entries) and its copy-on-write pair, if any,
+ * appended to cow_pairs_out (int32 [n][2], may be NULL if no sequence needs
+ * one) with the number of pairs in *n_cow. On an error the sequences before
+ * the failing one keep their reservations (each reservation is itself
+ * all-or-nothing) and *n_cow counts their pairs. */
+pa_status pa_seq_append_slots_batch(pa_pool* pool, const int32_t* seqs,
+                                    const int32_t* n_tokens, int32_t n,
+                                    int64_t* slots_out, int32_t* cow_pairs_out,
+                                    int32_t* n_cow);
+
 /* Release a sequence: refcount - 1 on each block; blocks reaching 0 go back
  * to the end of the free list in table order ([p3] release). */
 pa_status pa_seq_free(pa_pool* pool, int32_t seq);

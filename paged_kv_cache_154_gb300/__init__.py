@@ -42,6 +42,7 @@ _SIGS = {
     "pa_seq_create": ([_P, _P], ctypes.c_int),
     "pa_seq_fork": ([_P, _I32, _P], ctypes.c_int),
     "pa_seq_append_slots": ([_P, _I32, _I32, _P, _P, _P], ctypes.c_int),
+    "pa_seq_append_slots_batch": ([_P, _P, _P, _I32, _P, _P, _P], ctypes.c_int),
     "pa_seq_free": ([_P, _I32], ctypes.c_int),
     "pa_seq_len": ([_P, _I32, _P], ctypes.c_int),
     "pa_pool_block_tables": ([_P, _P, _I32, _I32, _P, _P], ctypes.c_int),
@@ -157,6 +158,23 @@ class Pool:
         _check(lib().pa_seq_append_slots(self._h, seq, n, slots.ctypes.data, pair.ctypes.data,
                                          ctypes.addressof(ncow)))
         return slots[:n], ((int(pair[0]), int(pair[1])) if ncow.value else None)
+
+    def seq_append_slots_batch(self, seqs: Sequence[int], counts: Sequence[int],
+                               slots_out: Optional[np.ndarray] = None
+                               ) -> Tuple[np.ndarray, np.ndarray]:
+        """One step's reservations in one call (pa_seq_append_slots_batch):
+        the slots of every sequence in order (into slots_out if given, int64
+        [sum(counts)]) and the copy-on-write pairs, int32 [k][2]."""
+        s = np.ascontiguousarray(seqs, dtype=np.int32)
+        c = np.ascontiguousarray(counts, dtype=np.int32)
+        total = int(c.sum())
+        slots = slots_out if slots_out is not None else np.zeros(max(total, 1), np.int64)
+        pairs = np.zeros((max(len(s), 1), 2), np.int32)
+        ncow = _I32()
+        _check(lib().pa_seq_append_slots_batch(self._h, s.ctypes.data, c.ctypes.data, len(s),
+                                               slots.ctypes.data, pairs.ctypes.data,
+                                               ctypes.addressof(ncow)))
+        return slots[:total], pairs[:ncow.value]
 
     def seq_free(self, seq: int) -> None:
         _check(lib().pa_seq_free(self._h, seq))

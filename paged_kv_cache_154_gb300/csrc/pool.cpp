@@ -329,6 +329,32 @@ extern "C" pa_status pa_seq_append_slots(pa_pool* p, int32_t seq, int32_t n_toke
     return PA_OK;
 }
 
+extern "C" pa_status pa_seq_append_slots_batch(pa_pool* p, const int32_t* seqs,
+                                               const int32_t* n_tokens, int32_t n,
+                                               int64_t* slots_out, int32_t* cow_pairs_out,
+                                               int32_t* n_cow) {
+    if (!p) return pa::fail(PA_ERR_INVALID_ARG, "NULL pool");
+    if (n < 0 || (n > 0 && (!seqs || !n_tokens)))
+        return pa::fail(PA_ERR_INVALID_ARG, "batch of %d sequences without arrays", n);
+    if (!n_cow) return pa::fail(PA_ERR_INVALID_ARG, "n_cow is NULL");
+    *n_cow = 0;
+    int64_t off = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        // without cow_pairs_out the single call refuses a copy before it changes anything
+        int32_t pair[2], one = 0;
+        if (pa_status s = pa_seq_append_slots(p, seqs[i], n_tokens[i], slots_out + off,
+                                              cow_pairs_out ? pair : nullptr, &one))
+            return s;   // the sequences before i keep their reservations
+        off += n_tokens[i] > 0 ? n_tokens[i] : 0;
+        if (one) {
+            cow_pairs_out[2 * *n_cow] = pair[0];
+            cow_pairs_out[2 * *n_cow + 1] = pair[1];
+            ++*n_cow;
+        }
+    }
+    return PA_OK;
+}
+
 extern "C" pa_status pa_seq_append_tokens(pa_pool* p, int32_t seq, const int32_t* token_ids,
                                           int32_t n_tokens, int64_t* slots_out,
                                           int32_t* cow_pair_out, int32_t* n_cow) {

@@ -186,6 +186,25 @@ void pool_trace(int nb, int ops, int max_cached) {
                 for (int t = 0; t < n; ++t) CHECK(slots[t] >= 0 && slots[t] < (int64_t)nb * 16);
                 if (ncow) CHECK(pair[0] != pair[1] && pair[0] >= 0 && pair[1] < nb);
             }
+        } else if (k < 66) {
+            // a decode step's reservations in one call over a run of live sequences
+            const int n = 1 + rnd((int)live.size());
+            std::vector<int32_t> cnt(n), prs(2 * n);
+            int64_t total = 0;
+            for (auto& c : cnt) total += (c = rnd(5));
+            std::vector<int64_t> sl(total + 1);
+            int32_t nc = -1;
+            const pa_status st = pa_seq_append_slots_batch(p, live.data(), cnt.data(), n,
+                                                           sl.data(), prs.data(), &nc);
+            CHECK(st == PA_OK || st == PA_ERR_OUT_OF_BLOCKS);
+            CHECK(nc >= 0 && nc <= n);
+            g_oob += st == PA_ERR_OUT_OF_BLOCKS;
+            g_cow += nc;
+            if (st == PA_OK)
+                for (int64_t t = 0; t < total; ++t) CHECK(sl[t] >= 0 && sl[t] < (int64_t)nb * 16);
+            for (int c = 0; c < nc; ++c)
+                CHECK(prs[2 * c] != prs[2 * c + 1] && prs[2 * c] >= 0 && prs[2 * c + 1] < nb);
+            for (int i = 0; i < n; ++i) by_tokens[i] = 0;
         } else if (k < 80) {
             const int i = rnd((int)live.size());
             CHECK(pa_seq_free(p, live[i]) == PA_OK);
@@ -220,6 +239,13 @@ void pool_trace(int nb, int ops, int max_cached) {
             CHECK(pa_seq_append_slots(p, live[0], -1, slots.data(), pair, &ncow) ==
                   PA_ERR_INVALID_ARG);
             CHECK(pa_seq_append_slots(p, live[0], 3, nullptr, pair, &ncow) == PA_ERR_INVALID_ARG);
+            const int32_t bad_n[1] = {-2};
+            CHECK(pa_seq_append_slots_batch(p, live.data(), bad_n, 1, slots.data(), nullptr,
+                                            &ncow) == PA_ERR_INVALID_ARG && ncow == 0);
+            CHECK(pa_seq_append_slots_batch(p, live.data(), nullptr, 1, slots.data(), nullptr,
+                                            &ncow) == PA_ERR_INVALID_ARG);
+            CHECK(pa_seq_append_slots_batch(p, nullptr, nullptr, 0, nullptr, nullptr, &ncow) ==
+                  PA_OK && ncow == 0);
             int32_t r;
             CHECK(pa_pool_refcount(p, nb, &r) == PA_ERR_INVALID_ARG);
             int32_t t1[1];

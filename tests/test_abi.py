@@ -93,6 +93,62 @@ def test_pool_matches_oracle_model_on_random_ops():
                 assert c.refcount(b) == m.ref[b]
 
 
+def test_batched_reservations_match_the_model_step_by_step():
+    """pa_seq_append_slots_batch against the allocator model on decode steps
+    of forked sequences (every fork's first append into a shared tail block
+    copies it): slots in sequence order, the copy-on-write pairs in order,
+    the same state as one reservation per sequence; a step that runs out of
+    blocks keeps the reservations before the failing sequence."""
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        order = rng.permutation(200).astype(np.int32)
+        c = pa.Pool(200, 16, order)
+        m = BlockPool(200, 16, order)
+        seqs = []
+        for g in range(int(rng.integers(1, 5))):
+            root = c.seq_create()
+            assert m.create() == root
+            n0 = int(rng.integers(1, 60))
+            c.seq_append_slots(root, n0)
+            m.append_slots(root, n0)
+            seqs.append(root)
+            for f in range(int(rng.integers(0, 4))):
+                a = c.seq_fork(root)
+                assert m.fork(root) == a
+                seqs.append(a)
+        for step in range(12):
+            counts = rng.integers(0, 6, size=len(seqs)).astype(np.int32)
+            want_slots, want_pairs, failed = [], [], None
+            for i, (s, r) in enumerate(zip(seqs, counts)):
+                try:
+                    ms, mp = m.append_slots(s, int(r))
+                except OutOfBlocks:
+                    failed = i
+                    break
+                want_slots += ms
+                if mp is not None:
+                    want_pairs.append(list(mp))
+            if failed is not None:
+                with pytest.raises(pa.PAError) as e:
+                    c.seq_append_slots_batch(seqs, counts)
+                assert e.value.status == 3
+                break
+            got_slots, got_pairs = c.seq_append_slots_batch(seqs, counts)
+            assert got_slots.tolist() == want_slots
+            assert got_pairs.tolist() == want_pairs
+            tables, lens = c.block_tables(seqs, 64)
+            for i, s in enumerate(seqs):
+                t = m.block_table(s)
+                assert tables[i, :len(t)].tolist() == t and lens[i] == m.lens[s]
+            assert c.stats() == m.stats()
+    # state after a failing step: the sequences before the failing one were reserved
+    c = pa.Pool(4, 16, np.arange(4, dtype=np.int32))
+    a, b = c.seq_create(), c.seq_create()
+    with pytest.raises(pa.PAError):
+        c.seq_append_slots_batch([a, b], [48, 48])      # 3 blocks, then 3 more of 4
+    assert c.seq_len(a) == 48 and c.seq_len(b) == 0
+
+
 def test_pool_errors():
     with pytest.raises(pa.PAError) as e:
         pa.Pool(8, 32)
