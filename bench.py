@@ -40,6 +40,8 @@ PROFILES = {
     "long_context": ("paged_decode_long_context.md", _DEC16),
     "mixed_int8": ("paged_decode_int8_mixed.md", ("paged_decode_int8.cu", "balanced.cuh",
                                                   "ptx.cuh")),
+    "mqa_int8_verify": ("paged_decode_int8_tc_verify.md", ("paged_decode_int8_tc.cu", "balanced.cuh",
+                                                          "ptx.cuh", "tcgen05.cuh")),
     "llama3_8b_fp8": ("paged_decode_fp8_llama3_8b.md", ("paged_decode_fp8.cu", "balanced.cuh",
                                                         "ptx.cuh")),
     "paged_prefill": ("paged_prefill_tc_llama3_8b_chunked.md",
@@ -297,6 +299,17 @@ def prefix_tc_runs(kv_dtype, si, group, head_dim=128) -> bool:
             and int(max(si.shared.prefix_len_host)) >= 1024)
 
 
+def int8_tc_runs(wl, si) -> bool:
+    """Whether an INT8 call takes the tensor-core kernel: head_dim 128, more
+    than 16 query rows per KV head at most and at least 64 on average (the
+    library's own rule)."""
+    G = wl.num_heads // wl.num_kv_heads
+    n_seqs = si.context_lens.shape[0]
+    n_q = si.q.shape[0]
+    return (wl.head_dim == 128 and G * si.max_q_len > 16 and G * n_q >= 64 * n_seqs
+            and n_seqs <= 1536)
+
+
 def roofline_kernel(wl, si, partition_size, prefill_tc):
     """The kernels the timed attention call launches."""
     G = wl.num_heads // wl.num_kv_heads
@@ -318,7 +331,9 @@ def roofline_kernel(wl, si, partition_size, prefill_tc):
                 f"{suffix} for the suffixes on a second stream beside them, "
                 f"prefix_merge_kernel)")
     if wl.kv_dtype == "int8":
-        return "pa_decode (paged_decode_int8_kernel + segment_reduce_kernel)"
+        return ("pa_decode (paged_decode_int8_tc_kernel: tokens in M on the tcgen05 tensor cores, "
+                "+ segment_reduce_kernel)" if int8_tc_runs(wl, si) else
+                "pa_decode (paged_decode_int8_kernel + segment_reduce_kernel)")
     if wl.kv_dtype == "fp8":
         return "pa_decode (paged_decode_fp8_kernel + segment_reduce_kernel)"
     if partition_size == 0:

@@ -215,6 +215,13 @@ inline BalancedShape balanced_shape(int num_seqs, int num_heads, int num_kv_head
     return b;
 }
 
+// INT8 decode with tokens in the M dimension of tensor-core products
+// (paged_decode_int8_tc.cu): for more than 16 query rows per KV head at
+// head_dim 128; int8_tc_applies says whether a call takes it.
+struct DecodeArgs;
+bool int8_tc_applies(const DecodeArgs& a);
+pa_status launch_decode_int8_tc(const DecodeArgs& a);
+
 // Limits of the balanced schedule that the host can check.
 inline pa_status balanced_check(const DecodeArgs& a) {
     if (a.num_seqs > kBalancedMaxSeqs)

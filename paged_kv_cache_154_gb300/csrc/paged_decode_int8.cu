@@ -564,6 +564,7 @@ namespace pa {
 pa_status launch_decode_int8(const DecodeArgs& a) {
     if (a.partition_size != 0)
         return fail(PA_ERR_UNSUPPORTED, "INT8 caches use the balanced schedule (partition_size 0)");
+    if (int8_tc_applies(a)) return launch_decode_int8_tc(a);
     if (pa_status s = balanced_check(a)) return s;
     if (((uintptr_t)a.k_scale | (uintptr_t)a.v_scale | (uintptr_t)a.k_zp | (uintptr_t)a.v_zp) % 16)
         return fail(PA_ERR_INVALID_ARG, "k_scale, v_scale, k_zp and v_zp must be 16-byte aligned");

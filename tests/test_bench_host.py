@@ -15,9 +15,10 @@ if ROOT not in sys.path:
 import bench  # noqa: E402
 
 
-def _si(max_q_len=1, max_context_len=4096, pairs=None, shared=None):
+def _si(max_q_len=1, max_context_len=4096, pairs=None, shared=None, n_seqs=8, n_q=None):
     return SimpleNamespace(max_q_len=max_q_len, max_context_len=max_context_len, pairs=pairs,
-                           shared=shared)
+                           shared=shared, context_lens=np.zeros(n_seqs),
+                           q=np.zeros((n_seqs if n_q is None else n_q, 1, 1)))
 
 
 def _wl(kv="bf16", H=32, Hkv=8, d=128):
@@ -60,6 +61,11 @@ def test_roofline_kernel_names_what_runs():
     assert "rows_kernel + segment_reduce" in bench.roofline_kernel(_wl(), _si(max_q_len=5), 0,
                                                                    False)
     assert "int8" in bench.roofline_kernel(_wl("int8"), _si(), 0, False)
+    # INT8 with 64 rows per KV head on average: the tensor-core kernel (MQA,
+    # 8 sequences with 16 query tokens); 48 on average: the per-warp kernel
+    mqa = _wl("int8", H=32, Hkv=1)
+    assert "int8_tc" in bench.roofline_kernel(mqa, _si(max_q_len=5, n_q=16), 0, False)
+    assert "int8_kernel" in bench.roofline_kernel(mqa, _si(max_q_len=5, n_q=12), 0, False)
     assert "fp8" in bench.roofline_kernel(_wl("fp8"), _si(), 0, False)
     assert "split_kv_reduce" in bench.roofline_kernel(_wl(), _si(), 512, False)
     assert "tcgen05" in bench.roofline_kernel(_wl(), _si(), 0, True)

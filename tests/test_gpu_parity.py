@@ -340,6 +340,37 @@ def test_nonzero_arrival_counters_are_reported(fill):
     assert not si.workspace[:ARRIVAL_BYTES].any()
 
 
+def test_int8_tensor_core_writes_stay_inside_workspace_and_output():
+    """The INT8 tensor-core kernel's 96-row partial slots: a call sized by the
+    workspace query writes nothing past it nor past the output, leaves the
+    arrival counters zero, and matches the oracle."""
+    from paged_kv_cache_154_gb300.engine import PagedKVCache
+    wl = W.simple("int8_tc_ws", 530, [9000, 40, 2500, 600, 1800], [3, 2, 5, 4, 2], 32, 1, 128,
+                  "int8")
+    cache = PagedKVCache(wl.num_blocks, wl.num_kv_heads, wl.head_dim, wl.kv_dtype,
+                         free_order=wl.free_order)
+    names = {}
+    for ops in wl.phases:
+        cache.run_phase(ops, names)
+    si = cache.prepare_step(wl.step, names, wl.q, torch.float32, 0)
+    cache.write_step(si)
+    ref = oracle.run(wl, threads=THREADS)
+    need = si.workspace.numel()
+    ws = torch.full((need + (1 << 16),), 0xA5, dtype=torch.uint8, device="cuda")
+    ws[:ARRIVAL_BYTES].zero_()
+    nq = si.out.shape[0]
+    out = torch.full((nq + 4,) + tuple(si.out.shape[1:]), float("nan"), device="cuda")
+    pa.decode(out[:nq], si.q, cache.k, cache.v, si.block_tables, si.context_lens,
+              si.max_context_len, wl.scale, si.query_start_loc, si.max_q_len, cache.num_blocks,
+              cache.k_scale, cache.v_scale, cache.k_zp, cache.v_zp, workspace=ws[:need])
+    torch.cuda.synchronize()
+    assert (code := pa.device_error()) == 0, hex(code)
+    check_out(ref, out[:nq], "int8")
+    assert bool((ws[need:] == 0xA5).all()), "bytes written past the workspace"
+    assert bool(out[nq:].isnan().all()), "rows written past the output"
+    assert not ws[:ARRIVAL_BYTES].any()
+
+
 @pytest.mark.parametrize("case", [
     ("spare_warps_mqa", [20000], [1], 8, 1, 128),        # 1250 workers: 2 spare warps
     ("spare_warps_d64", [1000, 77], [1, 1], 4, 1, 64),   # 2 x 63 = 126 workers, 68 blocks
@@ -387,12 +418,21 @@ INT8_SMALL = [
      torch.bfloat16),
     ("int8_d64_f16q", [33, 700, 64, 129], [1, 2, 1, 3], 8, 2, 64, torch.float16),
     ("int8_mha", [200, 31], [1, 1], 4, 4, 128, torch.bfloat16),
-    # at least 32 query rows per KV head at d = 128 (also run through the
-    # opt-in tensor-core kernel below): contexts of 1 and 2 tokens, partial
-    # tiles, a long sequence cut across many shares, fp16 q
+    # 64 query rows per KV head on average at d = 128 (the tensor-core
+    # kernel, tokens in M): contexts of 1 and 2 tokens, partial tiles, a long
+    # sequence cut across many shares, fp16 q
     ("int8_mqa_tc_f16q", [1, 2, 17, 64, 65, 4097, 333, 16], [1, 1, 2, 1, 5, 1, 4, 1], 32, 1,
      128, torch.float16),
-    ("int8_gqa8_verify_tc", [900, 45, 3000, 7], [4, 5, 3, 1], 32, 4, 128, torch.bfloat16),
+    # GQA verify runs, 26 rows on average (the per-warp kernel's row chunks)
+    ("int8_gqa8_verify", [900, 45, 3000, 7], [4, 5, 3, 1], 32, 4, 128, torch.bfloat16),
+    # the tensor-core kernel: 40 sequences of 64 rows whose blocks are cut
+    # into pieces across the CTAs' shares (partial slots and their merge)
+    ("int8_tc_rows64_many", [50 + (37 * i * i) % 4900 for i in range(40)], [2] * 40, 32, 1, 128,
+     torch.bfloat16),
+    # the tensor-core kernel with two KV heads and 16 q heads each: 48 and 80
+    # rows (column padding to 64 and 96), causal verify masks, fp16 q
+    ("int8_tc_gqa16_verify", [1200, 33, 2600, 700, 129, 3100], [3, 5, 4, 5, 3, 4], 32, 2, 128,
+     torch.float16),
 ]
 
 
@@ -408,9 +448,10 @@ def test_int8_small_shapes(case):
     check_out(ref, out, "int8")
 
 
+@pytest.mark.parametrize("qlens", [[2, 1], [3, 2]], ids=["per_warp", "tensor_core"])
 @pytest.mark.parametrize("qdt", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
-def test_int8_output_in_q_dtype(qdt):
-    wl = W.simple("int8_out16", 77, [300, 1000], [2, 1], 32, 1, 128, "int8", q_dtype=qdt)
+def test_int8_output_in_q_dtype(qdt, qlens):
+    wl = W.simple("int8_out16", 77, [300, 1000], qlens, 32, 1, 128, "int8", q_dtype=qdt)
     ref, cache, si, out = run_both(wl, out_dtype=qdt)
     check_out(ref, out, "int8", qdt)
 
@@ -423,15 +464,17 @@ def test_mixed_int8_config():
     check_out(ref, out, "int8")
 
 
-@pytest.mark.parametrize("heads", [(16, 2), (32, 1)], ids=["gqa8", "mqa32"])
-def test_int8_wide_value_range(heads):
+@pytest.mark.parametrize("heads,qlens", [((16, 2), [1, 3, 1]), ((32, 1), [1, 3, 1]),
+                                         ((32, 1), [4, 5, 3])],
+                         ids=["gqa8", "mqa32", "mqa32_tensor_core"])
+def test_int8_wide_value_range(heads, qlens):
     """K/V rows scaled by 2^-6 .. 2^0 (per token and head) and q rows by
     2^-6 .. 2^6: the running power-of-two V reference must keep the small
     rows, and the per-row power-of-two q scaling must make the fp16
     conversion of q exact. (Outputs stay of order one, the regime the 1e-2
     tolerance is stated for; the fp16 weights carry 2^-11 relative error, below
     the INT8 quantisation step of 1/255 of a row's range.)"""
-    wl = W.simple("int8_range", 91, [800, 1200, 50], [1, 3, 1], heads[0], heads[1], 128, "int8",
+    wl = W.simple("int8_range", 91, [800, 1200, 50], qlens, heads[0], heads[1], 128, "int8",
                   q_dtype=torch.bfloat16)
     rng = np.random.default_rng(0)
     for op in wl.phases[0] + wl.step:

@@ -367,7 +367,8 @@ def long_context(lens=(32768, 65536, 100000, 131072), shard: int = 0) -> Workloa
 
 
 def mixed_int8(batch: int = 256, median: int = 1024, cap: int = 16384,
-               verify_fraction: float = 0.2, shard: int = 0) -> Workload:
+               verify_fraction: float = 0.2, shard: int = 0,
+               name: str = "mixed_mqa_int8_verify") -> Workload:
     """Continuous-batching mixed step: 256 sequences with lognormal lengths
     (median 1024, sigma 1, capped at 16384), MQA 32 q / 1 KV head, head_dim
     128, INT8 KV; 20% of sequences carry a verify run of 2-5 query tokens."""
@@ -380,9 +381,16 @@ def mixed_int8(batch: int = 256, median: int = 1024, cap: int = 16384,
     q_lens[ver] = rng.integers(2, 6, size=nver)
     lens = np.minimum(np.rint(raw), cap).astype(np.int64)
     lens = np.maximum(lens, q_lens)
-    return simple("mixed_mqa_int8_verify", seed, lens, q_lens,
+    return simple(name, seed, lens, q_lens,
                   num_heads=32, num_kv_heads=1, head_dim=128, kv_dtype="int8",
                   q_dtype=torch.bfloat16)
+
+
+def mqa_int8_verify(shard: int = 0) -> Workload:
+    """Speculative-decoding verify step over an INT8 cache: the mixed step's
+    256 sequences and lengths with every sequence verifying 2-5 draft tokens
+    (64-160 query rows per KV head; MQA 32 q / 1 KV head, head_dim 128)."""
+    return mixed_int8(verify_fraction=1.0, shard=shard, name="mqa_int8_verify_all")
 
 
 NAMED = {
@@ -391,6 +399,7 @@ NAMED = {
     "llama2_70b_best_of_5": llama2_70b_best_of_5,
     "long_context": long_context,
     "mixed_int8": mixed_int8,
+    "mqa_int8_verify": mqa_int8_verify,
     "llama3_8b_fp8": llama3_8b_fp8,
     "paged_prefill": paged_prefill,
 }
