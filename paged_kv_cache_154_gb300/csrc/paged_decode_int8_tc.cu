@@ -239,51 +239,229 @@ struct Extra {
     const int8_t* v_zp;
 };
 
+// Shares balanced by cost, not by blocks. The blocks of a segment
+// (sequence, kv head, row chunk) cost block_cost(rows) units each -- a tile's
+// softmax grows with its rows -- and a segment's start costs kSegCost more
+// (its epilogue, the next Q and the exact maxima of its first tile come to
+// about two 32-row tiles). Segments are laid out as in the balanced schedule
+// (sequence, then kv head, then chunk); the total B of units is cut into W
+// equal ranges, and a block belongs to the share whose range holds its first
+// unit. Every share holds at least kMinShareUnits units, so every share
+// holds the first unit of some block.
+constexpr int kSegCost = 48;
+constexpr int kMinShareUnits = kSegCost + 8 * 5;
+__host__ __device__ __forceinline__ int block_cost(int rows) { return 2 + ((rows + 31) >> 5); }
+
+__device__ __forceinline__ int chunk_rows(const pa::sched::Params& p, int r, int c) {
+    return min(kRT, p.group * r - c * kRT);
+}
+
+// units of chunk c of a sequence (L tokens, query run r); its blocks in *nbs
+__device__ __forceinline__ int seg_units(const pa::sched::Params& p, int L, int r, int c, int* nbs) {
+    *nbs = pa::sched::chunk_blocks(p, L, r, 0, c);
+    return *nbs > 0 ? kSegCost + *nbs * block_cost(chunk_rows(p, r, c)) : 0;
+}
+
+__device__ __forceinline__ int seq_units(const pa::sched::Params& p, int s, int C) {
+    int q0, nbs, u = 0;
+    const int L = __ldg(p.context_lens + s), r = pa::sched::query_run(p.qsl, s, &q0);
+    for (int c = 0; c < C; ++c) u += seg_units(p, L, r, c, &nbs);
+    return u;
+}
+
+// cum[s] = units of the sequences before s (every kv head), chunks[s] = C_s,
+// by one CTA (a block-wide scan); CTA 0 copies cum for the reduce kernel.
+__device__ void build_cost_prefix(int32_t* cum, uint8_t* chunks, const pa::sched::Params& p) {
+    __shared__ int32_t warp_tot[32];
+    pa::grid_dependents_launch();   // the reduce kernel may be scheduled early
+    pa::grid_dependency_wait();     // inputs written by the previous kernel are visible
+    const int n = p.num_seqs;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (n + nt - 1) / nt;
+    const int a = min(n, tid * per), b = min(n, a + per);
+    int32_t local = 0;
+    for (int i = a; i < b; ++i) {
+        const int c = pa::sched::chunks_of(p, i);
+        chunks[i] = (uint8_t)c;
+        local += p.num_kv_heads * seq_units(p, i, c);
+    }
+    const int lane = tid & 31, warp = tid >> 5;
+    int32_t x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = nt >> 5;
+        int32_t t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    int32_t run = x - local + (warp > 0 ? warp_tot[warp - 1] : 0);
+    for (int i = a; i < b; ++i) {
+        cum[i] = run;
+        run += p.num_kv_heads * seq_units(p, i, chunks[i]);
+    }
+    if (tid == nt - 1) cum[n] = run;
+    __syncthreads();
+    if (blockIdx.x == 0 && p.cum_out)
+        for (int i = tid; i <= n; i += nt) p.cum_out[i] = cum[i];
+}
+
 // The tiles of a share in order: up to 8 blocks at a time of the current
-// segment (sequence, kv head, row chunk), never past the segment's or the
-// share's end. Every role walks its own copy.
+// segment, never past the segment's end or the share's last block. Every
+// role walks its own copy.
 struct Cursor {
-    Pos cur;
-    int64_t f, f1;      // next virtual block; end of the share
+    Pos cur;            // sequence, kv head, chunk, block, blocks, chunks of the sequence
+    int64_t u0;         // first unit of the segment (its block 0)
+    int w;              // units per block of the segment
+    int64_t f1;         // end of the share's units
+    int lim;            // blocks of the segment in this share or before it
+    bool done, cut;     // past the share's last block; its last segment continues after it
     int seg_b0;         // the segment's block where this share's piece starts
     bool seg_first;     // the piece is the share's first
     int L, r, q0, rows; // of the current segment
 
+    __device__ __forceinline__ int64_t start(int bb) const {
+        return bb == 0 ? u0 : u0 + kSegCost + (int64_t)bb * w;
+    }
+    // this segment's blocks whose first unit lies before f1
+    __device__ __forceinline__ int limit() const {
+        if (f1 <= u0) return 0;
+        const int64_t over = f1 - u0 - kSegCost;   // start(bb) < f1 <=> bb * w < over (bb >= 1)
+        const int64_t more = over > 0 ? (over + w - 1) / w - 1 : 0;
+        return (int)min((int64_t)cur.nbs, 1 + max((int64_t)0, more));
+    }
     __device__ __forceinline__ void load(const pa::sched::Params& p) {
         L = __ldg(p.context_lens + cur.s);
         r = pa::sched::query_run(p.qsl, cur.s, &q0);
-        rows = min(kRT, p.group * r - cur.c * kRT);
+        rows = chunk_rows(p, r, cur.c);
+        w = block_cost(rows);
     }
-    __device__ __forceinline__ void init(const pa::sched::Params& p, const int32_t* cum,
-                                         const uint8_t* chunks, int64_t fa, int64_t fb) {
-        cur = pa::sched::locate(p, cum, chunks, fa);
-        f = fa;
-        f1 = fb;
-        seg_b0 = cur.b;
-        seg_first = true;
-        load(p);
-    }
-    __device__ __forceinline__ bool more() const { return f < f1; }
-    __device__ __forceinline__ int blocks() const {
-        int nb = min(kTileBlocks, cur.nbs - cur.b);
-        if ((int64_t)nb > f1 - f) nb = (int)(f1 - f);
-        return nb;
-    }
-    __device__ __forceinline__ bool piece_first() const { return cur.b == seg_b0; }
-    __device__ __forceinline__ bool piece_last(int nb) const {
-        return cur.b + nb == cur.nbs || f + nb == f1;
-    }
-    __device__ __forceinline__ int cols() const { return (rows + 31) & ~31; }   // MMA N
-    __device__ __forceinline__ void advance(const pa::sched::Params& p, const int32_t* cum,
-                                            const uint8_t* chunks, int nb) {
-        cur.b += nb;
-        f += nb;
-        if (f < f1 && cur.b == cur.nbs) {
-            pa::sched::next_segment(p, cur, cum, chunks);
-            seg_b0 = 0;
-            seg_first = false;
-            load(p);
+    // from segment (s, g, c) starting at unit u, the first one with blocks;
+    // false past the last sequence
+    __device__ bool settle(const pa::sched::Params& p, const uint8_t* chunks) {
+        for (;;) {
+            int q0_, nbs;
+            const int Ls = __ldg(p.context_lens + cur.s);
+            const int rs = pa::sched::query_run(p.qsl, cur.s, &q0_);
+            seg_units(p, Ls, rs, cur.c, &nbs);
+            if (nbs > 0) {
+                cur.nbs = nbs;
+                load(p);
+                return true;
+            }
+            if (++cur.c >= cur.C) {
+                cur.c = 0;
+                if (++cur.g >= p.num_kv_heads) {
+                    cur.g = 0;
+                    if (++cur.s >= p.num_seqs) return false;
+                    cur.C = chunks[cur.s];
+                }
+            }
         }
+    }
+    __device__ void init(const pa::sched::Params& p, const int32_t* cum, const uint8_t* chunks,
+                         int64_t fa, int64_t fb) {
+        f1 = fb;
+        done = cut = false;
+        seg_first = true;
+        // the sequence holding unit fa, then its kv head and chunk
+        int lo = 0, hi = p.num_seqs;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cum[mid] <= fa) lo = mid;
+            else hi = mid;
+        }
+        cur.s = lo;
+        cur.C = chunks[lo];
+        const int64_t span = (cum[lo + 1] - cum[lo]) / p.num_kv_heads;
+        cur.g = (int)((fa - cum[lo]) / span);
+        u0 = cum[lo] + (int64_t)cur.g * span;
+        int q0_, nbs;
+        const int Ls = __ldg(p.context_lens + lo), rs = pa::sched::query_run(p.qsl, lo, &q0_);
+        for (cur.c = 0; cur.c < cur.C; ++cur.c) {
+            const int un = seg_units(p, Ls, rs, cur.c, &nbs);
+            if (fa < u0 + un) break;
+            u0 += un;
+        }
+        cur.nbs = nbs;
+        load(p);
+        // the first block whose first unit is at or after fa
+        const int64_t rem = fa - u0;
+        int b0 = 0;
+        if (rem > 0) b0 = (int)max((int64_t)1, (rem - kSegCost + w - 1) / w);
+        if (b0 >= cur.nbs) {
+            u0 += kSegCost + (int64_t)cur.nbs * w;
+            cur.b = 0;
+            if (++cur.c >= cur.C) {
+                cur.c = 0;
+                if (++cur.g >= p.num_kv_heads) {
+                    cur.g = 0;
+                    if (++cur.s >= p.num_seqs) {
+                        done = true;
+                        return;
+                    }
+                    cur.C = chunks[cur.s];
+                }
+            }
+            if (!settle(p, chunks)) {
+                done = true;
+                return;
+            }
+            b0 = 0;
+        }
+        cur.b = b0;
+        seg_b0 = b0;
+        lim = limit();
+        done = cur.b >= lim;
+    }
+    __device__ __forceinline__ bool more() const { return !done; }
+    __device__ __forceinline__ int blocks() const { return min(kTileBlocks, lim - cur.b); }
+    __device__ __forceinline__ bool piece_first() const { return cur.b == seg_b0; }
+    __device__ __forceinline__ bool piece_last(int nb) const { return cur.b + nb == lim; }
+    __device__ __forceinline__ int cols() const { return (rows + 31) & ~31; }   // MMA N
+    __device__ void advance(const pa::sched::Params& p, const int32_t* cum, const uint8_t* chunks,
+                            int nb) {
+        cur.b += nb;
+        if (cur.b < lim) return;
+        if (lim < cur.nbs) {            // the segment continues in the next share
+            done = cut = true;
+            return;
+        }
+        // the next segment with blocks, if it starts in this share
+        const int64_t next_u0 = u0 + kSegCost + (int64_t)cur.nbs * w;
+        const Pos keep = cur;
+        if (++cur.c >= cur.C) {
+            cur.c = 0;
+            if (++cur.g >= p.num_kv_heads) {
+                cur.g = 0;
+                if (++cur.s >= p.num_seqs) {
+                    cur = keep;
+                    done = true;
+                    return;
+                }
+                cur.C = chunks[cur.s];
+            }
+        }
+        if (next_u0 >= f1 || !settle(p, chunks)) {
+            cur = keep;
+            done = true;
+            return;
+        }
+        u0 = next_u0;
+        cur.b = 0;
+        seg_b0 = 0;
+        seg_first = false;
+        lim = limit();
     }
 };
 
@@ -304,10 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t* const cum = reinterpret_cast<int32_t*>(smem + kHdrOff);
     uint8_t* const chunks = reinterpret_cast<uint8_t*>(cum + p.num_seqs + 1);
 
-    pa::sched::build_prefix(cum, chunks, p);       // every thread; waits for the previous kernel
+    build_cost_prefix(cum, chunks, p);             // every thread; waits for the previous kernel
     const int64_t B = cum[p.num_seqs];
     const int64_t wid = blockIdx.x;
-    const int64_t W = pa::sched::share_count(p, B);
+    const int64_t W = max((int64_t)1, min((int64_t)p.workers, B / kMinShareUnits));
     const int64_t f0 = pa::sched::share_start(wid, B, W);
     const int64_t f1 = pa::sched::share_start(wid + 1, B, W);
     if (threadIdx.x == 0) pa::sched::write_merge_record(p, wid, 0, 0, 0);   // none unless set later
@@ -382,10 +560,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.err) atomicOr(p.err, pa::ERR_WAIT_DRAIN);
                     break;
                 }
-            if (ok)
-                pa::sched::record_last_segment(p, wid, f1, B, it.cur.b == it.cur.nbs, it.seg_b0,
-                                               it.cur.nbs - it.cur.b, it.seg_first, it.q0,
-                                               it.rows);
+            // a segment cut by this share's end and started in it: this CTA
+            // owns its merge, up to the share holding its last block
+            if (ok && it.cut && it.seg_b0 == 0)
+                pa::sched::write_merge_record(p, wid, 1,
+                                              pa::sched::share_of(it.start(it.cur.nbs - 1), B, W),
+                                              it.seg_first ? 0 : 1, it.q0, it.rows);
         }
     } else if (warp <= 4) {
         // ---------------- converters: one token per thread ----------------
@@ -732,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- epilogue of the piece: thread t holds dim t of every row ----
                 wait_w(bar(kODone + b), (u >> 1) & 1, pa::ERR_WAIT_FULL);
                 tc::fence_after_sync();
-                const bool complete = it.seg_b0 == 0 && it.cur.b + nb == it.cur.nbs;
+                const bool complete = it.seg_b0 == 0 && it.cur.b + nb == it.cur.nbs;   // whole segment
                 pa::sched::Slot sl(p.slots + (2 * wid + (it.seg_first ? 0 : 1)) * (int64_t)p.slot_bytes,
                                    kRT);
                 if (32 * q4 < rows) {                      // warp-uniform (a TMEM load)
@@ -946,8 +1126,12 @@ namespace pa {
 bool int8_tc_applies(const DecodeArgs& a) {
     const int64_t rows = (int64_t)(a.num_heads / a.num_kv_heads) * a.max_q_len;
     const int64_t avg_rows_x = (int64_t)(a.num_heads / a.num_kv_heads) * a.num_q_tokens;
+    // the cost units of a call fit the schedule's 32-bit prefix sums
+    const int64_t chunks = (rows + kRT - 1) / kRT;
+    const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * chunks *
+                          (kSegCost + (int64_t)(a.max_context_len + kBS - 1) / kBS * block_cost(kRT));
     return a.kv_dtype == PA_INT8 && a.head_dim == D && a.block_size == kBS && rows > 16 &&
-           avg_rows_x >= 64 * (int64_t)a.num_seqs &&
+           avg_rows_x >= 64 * (int64_t)a.num_seqs && units < 0x7fffffffll &&
            a.num_seqs <= kMaxSeqs && a.partition_size == 0 && !a.lse_out && !a.ctx_start &&
            a.slots != nullptr;
 }
