@@ -1,6 +1,6 @@
 // Paged decode attention over an INT8 cache on the 5th-generation tensor
-// cores (tcgen05, TMEM), for calls with more than 16 query rows per KV head
-// (MQA, GQA with verify runs) and head_dim 128.
+// cores (tcgen05, TMEM), for calls averaging at least 64 query rows per KV
+// head (MQA or GQA verify steps) at head_dim 128.
 //
 // The cache holds codes x_q with one fp32 scale and int8 zero point per
 // (token, kv head); a value is (x_q - zp) * scale ("cs336 lecture 10",
@@ -31,15 +31,17 @@
 //                    holds the column sums of P, so the denominators need no
 //                    column reduction.
 //
-// Work split: the balanced schedule (balanced.cuh) with one share per CTA
-// (one CTA per SM) and row chunks of 96; segments cut by share boundaries go
-// to partial slots that segment_reduce_kernel merges. Roles: warp 0 streams
-// the code tiles (TMA, one 16-token block per lane) into a 4-stage ring;
-// warps 1-4 convert (one token per thread, its scales and zero point by
-// plain loads one tile ahead); warps 5-8 run the softmax and the epilogue; warp 9
-// issues the MMAs. Every wait is bounded; a wait that gives up sets an error
-// bit, after which every other wait of the call returns at once, and the
-// roles run out their loops without further copies or products.
+// Work split: the segments of the balanced schedule (balanced.cuh) with row
+// chunks of 96, cut into one share per CTA (one CTA per SM) by cost rather
+// than by blocks (see "Shares balanced by cost" below); segments cut by share
+// boundaries go to partial slots that segment_reduce_kernel merges. Roles:
+// warp 0 streams the code tiles (TMA, one 16-token block per lane) into a
+// 4-stage ring; warps 1-4 convert (one token per thread, its scales and zero
+// point by plain loads one tile ahead); warps 5-8 run the softmax and the
+// epilogue; warp 9 issues the MMAs. Every wait is bounded; a wait that gives
+// up sets an error bit, after which every other wait of the call returns at
+// once, and the roles run out their loops without further copies or
+// products.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
