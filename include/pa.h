@@ -285,7 +285,13 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_tokens,
  *                  where share boundaries cut one, the pieces' partials
  *                  (m, l, O) are merged with the log-sum-exp rule (by the
  *                  decode kernel itself for F16/BF16 caches with at most 16
- *                  query rows per KV head, else by a reduce kernel). A multiple
+ *                  query rows per KV head, else by a reduce kernel). An INT8
+ *                  call at head_dim 128 averaging at least 64 query rows per
+ *                  KV head (num_heads / num_kv_heads x num_q_tokens /
+ *                  num_seqs) with at most 1536 sequences runs on the tensor
+ *                  cores with one share per SM, shares cut by cost; its
+ *                  partial slots hold 96 rows, and it uses as many SMs as the
+ *                  workspace size above has room for. A multiple
  *                  of 16 up to 4096 selects fixed split-KV partitions of that
  *                  many tokens (one CTA per partition, KV head and sequence).
  *   workspace      device memory of pa_decode_workspace_size() bytes,
